@@ -1,0 +1,417 @@
+"""Benchmark of the GB300 routed-expert MoE block (one JSON line on stdout).
+
+Default workload: the 4-token verify window (one MoE layer, 512 Q2_0 experts, top-10, inputs
+x_j = x_0 + 0.3 N(0,1), seed 0).  A step is one strata_moe_layer call (router GEMV, top-10,
+grouping, Q2_0 SwiGLU experts, combine) on inputs resident in HBM; the step's working set fits in
+the 129 MB L2, so a 256 MB buffer is written between timed steps (flush excluded from the step
+time, which is taken with CUDA events around each step on the launching stream).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+--config 0..4 selects the other workloads of the block (decode 1 token; verify window; 48-layer
+decode stack; 2,048-token prefill; 8,192-token x 48-layer prefill).  --impl reference times the
+CPU oracle (plain C, double precision) on the host cores on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (the block shards by requests; no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) / TC util (prefill)"
+E = 512
+BLOB = 1382400
+ROUTER_BYTES = 512 * 2560 * 2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+DEFAULT_STEPS = {0: 4000, 1: 4000, 2: 100, 3: 50, 4: 3}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (median SM clock, throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# workload set-up
+# ------------------------------------------------------------------------------------------------
+def setup_device(cfg_id, seed, dev):
+    import torch
+
+    import quantized_routed_expert_top10_gb300 as qre
+    cfg = gen.config_inputs(cfg_id, seed)
+    L, T = cfg["L"], cfg["T"]
+    table = torch.from_numpy(gen.SCALE_TABLE.view(np.int16)).to(dev)
+    arena = torch.empty(L * E * BLOB, dtype=torch.uint8, device=dev)
+    tmp = torch.empty(E * BLOB, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for l in range(L):
+        gen.device_canonical_blobs(seed, l, 0, E, table.data_ptr(), tmp.data_ptr(), BLOB, s)
+        qre.strata_pack_q2_0_device(tmp, BLOB, arena[l * E * BLOB:], BLOB, E)
+    del tmp
+    wr = torch.from_numpy(np.stack(cfg["wr"]).view(np.int16)).to(dev)
+    bias = None
+    if cfg["bias"][0] is not None:
+        bias = torch.from_numpy(np.stack(cfg["bias"])).to(dev)
+    exs = [qre.experts(arena[l * E * BLOB:], E, 1) for l in range(L)]
+    x_host = cfg["x"]
+    torch.cuda.synchronize()
+    return cfg, arena, wr, bias, exs, x_host
+
+
+def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws):
+    """One pass of the whole hot path over the batch (x_in is never modified)."""
+    T, L = cfg["T"], cfg["L"]
+    if L == 1:
+        qre.strata_moe_layer(exs[0], wr[0], None if bias is None else bias[0], x_in, T, 0, out, ids, None, ws)
+        return out
+    x_work.copy_(x_in)
+    qre.strata_moe_stack(exs, wr, bias, L, x_work, T, None, None, ws)
+    return x_work
+
+
+def launches_per_step(T, L):
+    # T <= 8: fused routing + gate/up + down + combine; else rmsnorm (stacks) + router GEMM + top-k + 3 grouping
+    # kernels + quantise + gate/up + down + combine.
+    if T <= 8:
+        return 4 * L
+    return (8 + (1 if L > 1 else 0)) * L
+
+
+def measure_gb300(args, rank, world, local_rank):
+    import torch
+
+    import quantized_routed_expert_top10_gb300 as qre
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg_id = args.config
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg_id]
+    W = max(3, args.warmup)
+    cfg, arena, wr, bias, exs, x_host = setup_device(cfg_id, args.seed, dev)
+    T, L = cfg["T"], cfg["L"]
+    x_in = torch.from_numpy(x_host).to(dev)
+    x_work = torch.empty_like(x_in)
+    out = torch.empty_like(x_in)
+    ids = torch.empty(T, 10, dtype=torch.int32, device=dev)
+    ws_bytes = qre.strata_moe_workspace_bytes(T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    qre.strata_moe_workspace_init(ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    need_flush = L == 1 and cfg_id in (0, 1)  # working set < L2; the stacks and prefill stream > L2
+    stream = torch.cuda.current_stream()
+
+    for _ in range(W):
+        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws)
+    torch.cuda.synchronize()
+    st = qre.strata_poll_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        if need_flush:
+            flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if wall < 1.0:
+        time.sleep(0.3)
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(np.sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    st = qre.strata_poll_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
+    ids_h = ids.cpu().numpy()
+    value = world * T * K / (total_ms / 1e3)
+
+    # ---- dominant kernel: the Q2_0 expert step (gate/up + down), CUDA events on the same stream ----
+    roof = expert_roofline(qre, cfg, exs, x_in, ids, ws, stream, flush if need_flush else None, T, dev)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush if need_flush else None, dev,
+                      max(20, min(K, 500)), world)
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "q2_0 weights x int16-split activations (dp4a), fp32 accumulate",
+        "data": "synthetic (seeded Philox4x32-10 inputs; random Q2_0 experts; no trained weights)",
+        "config": {
+            "workload": cfg["name"],
+            "tokens": T,
+            "layers": L,
+            "experts": E,
+            "top_k": 10,
+            "hidden": 2560,
+            "ffn": 640,
+            "q2_offset": 1,
+            "seed": args.seed,
+            "l2": "256 MB buffer written between timed steps (flush excluded)" if need_flush
+            else "working set larger than L2 (no flush)",
+            "distinct_experts_last_step": int(len(np.unique(ids_h))) if L == 1 else None,
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(T, L) * K,
+    }
+    return result, cfg, ids_h
+
+
+def expert_roofline(qre, cfg, exs, x_in, ids, ws, stream, flush, T, dev):
+    """Average duration of strata_moe_experts (the Q2_0 gate/up and down kernels plus the tile builder
+    and activation quantiser) against its algorithmic bytes: distinct experts x 1,382,400 B."""
+    import torch
+    if cfg["L"] != 1:
+        return None
+    hbm, _, _, how = load_peaks()
+    off = torch.empty(513, dtype=torch.int32, device=dev)
+    pair = torch.empty(T * 10, dtype=torch.int32, device=dev)
+    active = torch.empty(512, dtype=torch.int32, device=dev)
+    na = torch.empty(1, dtype=torch.int32, device=dev)
+    parts = torch.empty(T * 10 * 2560, dtype=torch.float32, device=dev)
+    qre.strata_moe_group(ids, T, 512, off, pair, active, na, ws)
+    torch.cuda.synchronize()
+    D = int(na.item())
+    n = 200 if T <= 8 else 20
+    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(3):
+        qre.strata_moe_experts(exs[0], x_in, T, off, pair, active, na, parts, ws)
+    for i in range(n):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        s_ev[i].record(stream)
+        qre.strata_moe_experts(exs[0], x_in, T, off, pair, active, na, parts, ws)
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    avg_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]))
+    bytes_alg = D * BLOB
+    achieved = bytes_alg / (avg_ms / 1e3) / 1e9
+    return {"kernel": "strata_moe_experts (q2 gate/up + down)", "bound": "hbm", "achieved": achieved,
+            "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+            "bytes_per_launch": bytes_alg, "distinct_experts": D, "avg_launch_ms": avg_ms,
+            "peak_source": f"{how} (MEASURED_PEAKS.json hbm_gbs)" if how == "measured" else "fallback 6.8 TB/s"}
+
+
+def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, world):
+    import torch
+    T, L = cfg["T"], cfg["L"]
+    hx = torch.from_numpy(x_host).pin_memory()
+    hout = torch.empty_like(hx).pin_memory()
+    dx = torch.empty(hx.shape, dtype=torch.float32, device=dev)
+    dout = torch.empty_like(dx)
+    tot = 0.0
+    for i in range(n + 3):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dx.copy_(hx, non_blocking=True)
+        if L == 1:
+            qre.strata_moe_layer(exs[0], wr[0], None if bias is None else bias[0], dx, T, 0, dout, None, None, ws)
+            hout.copy_(dout, non_blocking=True)
+        else:
+            qre.strata_moe_stack(exs, wr, bias, L, dx, T, None, None, ws)
+            hout.copy_(dx, non_blocking=True)
+        stream.synchronize()
+        if i >= 3:
+            tot += time.perf_counter() - t0
+    nbytes = T * 2560 * 4
+    return {"value": world * T * n / tot, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "steps": n, "timing": "host wall clock per step incl. stream sync"}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_sample(cfg_id, seed, budget_s=12.0, max_reps=None):
+    """Time the oracle on a bounded sample of the workload; returns (tokens/s, threads, description)."""
+    import oracle
+    cfg = gen.config_inputs(cfg_id, seed, L=1 if cfg_id in (2, 4) else None)
+    x = cfg["x"]
+    T = x.shape[0]
+    tok = T if T <= 4 else 4
+    xs = x[:tok]
+    wr, bias = cfg["wr"][0], cfg["bias"][0]
+    residual = cfg["residual"]
+    r = oracle.route(xs, wr, bias, residual=residual)
+    blobs = [None] * E
+    for e in np.unique(r["ids"]):
+        blobs[int(e)] = gen.canonical_blob(seed, 0, int(e))
+    threads = max(1, min(os.cpu_count() or 1, tok))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.moe_layer(xs, wr, bias, blobs, residual=residual, n_threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_reps and reps >= max_reps):
+            break
+    layers = cfg_id in (2, 4)
+    tps = tok * reps / el
+    if layers:
+        tps /= 48.0  # one layer timed; a token of the workload passes 48 layers
+    desc = (f"{tok} token(s) x 1 layer of {cfg['name']}, repeated {reps}x in {el:.1f} s"
+            + (", per-token time x48 layers" if layers else ""))
+    return tps, threads, desc, el / reps
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return None
+    cfg_id = args.config
+    K = args.steps if args.steps is not None else 5
+    W = args.warmup
+    cfg = gen.CONFIGS[cfg_id]
+    for _ in range(min(W, 1)):
+        oracle_sample(cfg_id, args.seed, budget_s=0.0, max_reps=1)
+    step_s = []
+    threads = 1
+    desc = ""
+    for _ in range(K):
+        tps, threads, desc, per = oracle_sample(cfg_id, args.seed, budget_s=0.0, max_reps=1)
+        step_s.append(per)
+    tok = min(cfg["T"], 4)
+    value = tok * K / float(np.sum(step_s)) / (48.0 if cfg_id in (2, 4) else 1.0)
+    cpu = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+            "steps": K, "warmup": W, "ms_per_step": 1e3 * float(np.mean(step_s)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["name"]}, "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = reference_arm(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, cfg, ids = measure_gb300(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            tps, threads, desc, _ = oracle_sample(args.config, args.seed)
+            res["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                   "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

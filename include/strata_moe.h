@@ -1,0 +1,164 @@
+/* strata_moe.h -- C ABI of the GB300 (sm_103a) routed-expert MoE block.
+ *
+ * The block (one layer of a 48-layer, 512-expert, top-10 model; H = 2560, FF = 640):
+ *   1. router logits   l[t][e] = sum_h x[t][h] * Wr[e][h] (+ bias[e])            (BF16 GEMV/GEMM)
+ *   2. top-10           softmax over E, stable descending order, first 10, renormalised
+ *   3. grouping         pairs (t, k) counting-sorted by expert
+ *   4. expert FFN       y = down(silu(gate x) * (up x)) with Q2_0 weights dequantised in-kernel
+ *   5. combine          out[t] = sum_k w[t][k] * y[t][k]   (+ x[t] for residual layers)
+ * Sources, by page title and section:
+ *   - zwxr.cn news/242664 "MoE 遇上消费级显卡", section "一次路由的完整旅程": moe_route's BF16 GEMV
+ *     (project_bf16) to 512 logits, native_router_top10 (softmax over all 512, stable descending
+ *     argsort, gather, renormalise with ggml's lower clamp -> ids[10], weights[10]), the grouped
+ *     expert kernel, and moe_combine.
+ *   - ai.thesatyajit.com "Strata engine", section "The byte budget, in code": H = 2560, FF = 640,
+ *     QK = 64, blob = 3 * H*FF*18/64 = 1,382,400 bytes; section "The CPU kernels": Q2_0 codes
+ *     {0,1,2,3} mean {-1,0,1,2} x scale, and the in-block bit order of unpack64_q2_0.
+ *   - momoyeyu.github.io "ai-infra-strata", section "提示词处理": tokens gathered per expert so one
+ *     weight read serves several tokens; the dequantisation is fused into the matrix kernel.
+ *   - The SwiGLU form and the rmsnorm residual stack come from the benchmark statement of the block.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller unless marked "host".  The library never
+ *     allocates or frees device memory; scratch lives in the caller's workspace `ws`.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work; they
+ *     return before it runs and do not synchronise, except strata_poll_status.
+ *   - Arguments checkable on the host are checked first; a bad one returns an error and enqueues
+ *     nothing.  T == 0 is a valid empty call (returns STRATA_OK, enqueues nothing).
+ *   - Conditions only the device can see (an expert id >= E, a bounded wait that expired) set
+ *     bits in a status word inside `ws`; read it with strata_poll_status.  Kernels never trap.
+ *   - fp32 tensors are row-major and 16-byte aligned; ws must be 256-byte aligned and initialised
+ *     once with strata_moe_workspace_init before first use; afterwards every call leaves it
+ *     reusable.  Two calls that share a ws must not overlap in time (same stream, or ordered).
+ *
+ * Packed expert blob ("GPU layout", written by strata_pack_q2_0*; same 1,382,400 bytes as the
+ * canonical blob, every chunk 256-byte aligned when the blob is):
+ *   canonical: gate [640][2560], up [640][2560], down [2560][640], each row-major, as Q2_0 blocks of
+ *     64 consecutive weights {fp16 d, 16 code bytes}; weight i of a block in code byte i/4 at bits
+ *     2*(i%4); value d * (c - q2_offset).
+ *   packed gate/up region, bytes [0, 921600): for row tile rt = 0..4 (rows 128*rt ..), for k-block
+ *     kb = 0..39, a 4608-byte chunk at (rt*40 + kb)*4608:
+ *        [0, 2048)    gate codes of the tile's 128 rows, 16 bytes per row, row order
+ *        [2048, 4096) up codes, same order
+ *        [4096, 4608) per row r: {fp16 gate d, fp16 up d} at 4096 + 4*r
+ *   packed down region, bytes [921600, 1382400): for row tile rt = 0..19, kb = 0..9, a 2304-byte
+ *     chunk at 921600 + (rt*10 + kb)*2304: [0, 2048) codes of 128 rows, [2048, 2304) fp16 d per row.
+ *   Code bytes keep the canonical in-block order.
+ */
+#ifndef STRATA_MOE_H_
+#define STRATA_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define STRATA_MOE_H 2560
+#define STRATA_MOE_FF 640
+#define STRATA_MOE_E_MAX 512
+#define STRATA_MOE_K 10
+#define STRATA_MOE_QK 64
+#define STRATA_MOE_BLOB_BYTES 1382400
+#define STRATA_MOE_T_MAX 8192 /* the pages' largest prefill chunk (8,192 tokens) */
+
+/* strata_moe_layer flags */
+#define STRATA_MOE_RESIDUAL_RMSNORM 1 /* out = x + moe(rmsnorm(x)), rmsnorm(x) = x / sqrt(mean(x^2) + 1e-6) */
+
+typedef enum strata_status {
+  STRATA_OK = 0,
+  STRATA_E_INVAL = -1,       /* null pointer, size out of range, bad enum value */
+  STRATA_E_ALIGN = -2,       /* a pointer or stride breaks the alignment rule of its argument */
+  STRATA_E_UNSUPPORTED = -3, /* a shape this build does not implement */
+  STRATA_E_CUDA = -4,        /* a CUDA runtime call (launch, copy) failed */
+  STRATA_E_TIMEOUT = -5,     /* a bounded device-side wait expired (device status) */
+  STRATA_E_WORKSPACE = -6,   /* ws_bytes smaller than strata_moe_workspace_bytes(T) */
+  STRATA_E_CORRUPT = -7      /* the device saw invalid data, e.g. an expert id >= E (device status) */
+} strata_status;
+
+/* The experts of one layer. */
+typedef struct strata_experts {
+  const void* blobs;   /* device: expert e's packed blob at blobs + e * blob_stride; 256-byte aligned */
+  int64_t blob_stride; /* bytes; multiple of 256 and >= STRATA_MOE_BLOB_BYTES */
+  int32_t n_expert;    /* E: experts routed over; multiple of 32 in [32, 512] */
+  int32_t q2_offset;   /* 1: codes {0,1,2,3} = {-1,0,1,2} x d (the pages); 2: the c-2 reading */
+} strata_experts_t;
+
+/* Bytes of workspace a call with T tokens needs (any entry point below). */
+size_t strata_moe_workspace_bytes(int32_t T);
+
+/* Zero the workspace's counters and status word (enqueued on stream). Call once after allocating. */
+strata_status strata_moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 1-2. x fp32 [T][2560] (the router input, already normalised if the layer normalises);
+ * w_router bf16 bit patterns [E][2560]; bias fp32 [E] or NULL; E = n_expert (multiple of 32 in
+ * [32, 512]).  Outputs: ids int32 [T][10] in descending probability (equal probabilities: lower
+ * id first), weights fp32 [T][10] = p / max(sum of the 10 p, 2^-14); logits fp32 [T][E] or NULL
+ * (includes the bias).  Logits accumulate in fp32. */
+strata_status strata_moe_route(const float* x, int32_t T, const uint16_t* w_router, const float* bias,
+                               int32_t n_expert, int32_t* ids, float* weights, float* logits, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Step 3. ids int32 [T][10] -> expert_off int32 [E+1] (exclusive prefix of per-expert counts),
+ * pair int32 [T*10]: pair numbers p = t*10 + k sorted by expert, ascending p within an expert;
+ * active int32 [E]: experts with >= 1 pair in increasing id (entries past n_active undefined);
+ * n_active int32 [1].  An id outside [0, E) sets STRATA_E_CORRUPT in the status word and that
+ * pair is dropped. */
+strata_status strata_moe_group(const int32_t* ids, int32_t T, int32_t n_expert, int32_t* expert_off,
+                               int32_t* pair, int32_t* active, int32_t* n_active, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Step 4. For every pair p = t*10 + k listed by the grouping: parts[p][:] = expert(x[t]) with the
+ * expert that owns p.  x fp32 [T][2560]; grouping arrays as strata_moe_group writes them; parts
+ * fp32 [T][10][2560].  Weights are the packed blobs of ex (host pointer to the struct). */
+strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int32_t T,
+                                 const int32_t* expert_off, const int32_t* pair, const int32_t* active,
+                                 const int32_t* n_active, float* parts, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Step 5. out[t][h] = (residual ? residual[t][h] : 0) + (sum over k = 0..9, in order, of
+ * weights[t][k] * parts[t][k][h]).  residual may be NULL; out may alias residual. */
+strata_status strata_moe_combine(const float* parts, const float* weights, int32_t T,
+                                 const float* residual, float* out, void* stream);
+
+/* Steps 1-5 for one layer. flags = 0: out = moe(x); flags = STRATA_MOE_RESIDUAL_RMSNORM: out =
+ * x + moe(rmsnorm(x)) with router and experts both reading rmsnorm(x).  out may alias x.  ids /
+ * weights (nullable) receive the routing.  Workspace as for any call with T tokens. */
+strata_status strata_moe_layer(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
+                               const float* x, int32_t T, int32_t flags, float* out, int32_t* ids,
+                               float* weights, void* ws, size_t ws_bytes, void* stream);
+
+/* n_layers residual layers in sequence on x (in place): x <- x + moe_l(rmsnorm(x)).
+ * ex: host array [n_layers]; w_router: device bf16 [n_layers][E][2560]; bias: device fp32
+ * [n_layers][E] or NULL; ids / weights (nullable): device [n_layers][T][10]. */
+strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
+                               int32_t n_layers, float* x, int32_t T, int32_t* ids, float* weights,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Canonical -> packed blob layout, host memory (host pointers), n_blobs consecutive blobs of
+ * STRATA_MOE_BLOB_BYTES each.  Pure byte permutation; src and dst must not overlap. */
+strata_status strata_pack_q2_0(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs);
+
+/* Packed -> canonical, host memory: the inverse of strata_pack_q2_0. */
+strata_status strata_unpack_q2_0(const uint8_t* packed, uint8_t* canonical, int64_t n_blobs);
+
+/* Canonical -> packed on the device: blob j from canonical + j*src_stride to packed +
+ * j*dst_stride (dst_stride multiple of 256, dst 256-byte aligned, src 2-byte aligned). */
+strata_status strata_pack_q2_0_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed,
+                                      int64_t dst_stride, int64_t n_blobs, void* stream);
+
+/* Synchronise stream, read and return the workspace status word (STRATA_OK if no device-side
+ * error was recorded since the last strata_moe_workspace_init or strata_clear_status). */
+strata_status strata_poll_status(const void* ws, void* stream);
+
+/* Reset the workspace status word (enqueued on stream). */
+strata_status strata_clear_status(void* ws, void* stream);
+
+/* Static string naming a status code. */
+const char* strata_status_str(strata_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STRATA_MOE_H_ */

@@ -68,6 +68,10 @@ def lib():
                                     _c_f64p]
         L.oracle_rmsnorm.restype = None
         L.oracle_rmsnorm.argtypes = [_c_f64p, ctypes.c_int, ctypes.c_double, _c_f64p]
+        L.oracle_route_tokens.restype = ctypes.c_int
+        L.oracle_route_tokens.argtypes = [_c_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _c_u16p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         L.oracle_moe_layer.restype = ctypes.c_int
         L.oracle_moe_layer.argtypes = [
             _c_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u16p,
@@ -161,6 +165,23 @@ def rmsnorm(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     out = np.empty_like(x)
     lib().oracle_rmsnorm(x, x.size, eps, out)
     return out
+
+
+def route(x, w_router, bias=None, residual=False, K=10, n_threads=None):
+    """Steps 1-2 for x fp32[T][H]: dict(ids [T][K], w [T][K], logits [T][E])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    T, H = x.shape
+    E = w_router.shape[0]
+    ids = np.empty((T, K), dtype=np.int32)
+    w = np.empty((T, K), dtype=np.float64)
+    logits = np.empty((T, E), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    nt = n_threads if n_threads else max(1, min(os.cpu_count() or 1, T))
+    rc = lib().oracle_route_tokens(x, T, H, E, K, np.ascontiguousarray(w_router, dtype=np.uint16), _ptr(b),
+                                   1 if residual else 0, _ptr(ids), _ptr(w), _ptr(logits), nt)
+    if rc:
+        raise ValueError("oracle_route_tokens: bad argument")
+    return dict(ids=ids, w=w, logits=logits)
 
 
 def moe_layer(x, w_router, bias, blobs, q2_offset=1, residual=False, ids_in=None, H=None, FF=None,

@@ -309,3 +309,72 @@ int oracle_moe_layer(const float* x, int T, int H, int FF, int E, int K, const u
   free(th);
   return rc;
 }
+
+typedef struct {
+  const float* x;
+  int T, H, E, K;
+  const uint16_t* w_router;
+  const float* bias;
+  int residual;
+  int32_t* ids_out;
+  double* w_out;
+  double* logits_out;
+  int n_threads, tid;
+} route_job;
+
+static void* route_worker(void* arg) {
+  route_job* j = (route_job*)arg;
+  double* xn = (double*)malloc(sizeof(double) * (size_t)j->H);
+  double* logits = (double*)malloc(sizeof(double) * (size_t)j->E);
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)j->K);
+  double* w = (double*)malloc(sizeof(double) * (size_t)j->K);
+  for (int t = j->tid; t < j->T; t += j->n_threads) {
+    for (int h = 0; h < j->H; ++h) xn[h] = (double)j->x[(int64_t)t * j->H + h];
+    if (j->residual) oracle_rmsnorm(xn, j->H, 1e-6, xn);
+    oracle_router_logits(xn, j->H, j->E, j->w_router, j->bias, logits);
+    oracle_top_k(logits, j->E, j->K, ids, w, NULL);
+    if (j->ids_out) memcpy(j->ids_out + (int64_t)t * j->K, ids, sizeof(int32_t) * (size_t)j->K);
+    if (j->w_out) memcpy(j->w_out + (int64_t)t * j->K, w, sizeof(double) * (size_t)j->K);
+    if (j->logits_out) memcpy(j->logits_out + (int64_t)t * j->E, logits, sizeof(double) * (size_t)j->E);
+  }
+  free(xn);
+  free(logits);
+  free(ids);
+  free(w);
+  return NULL;
+}
+
+int oracle_route_tokens(const float* x, int T, int H, int E, int K, const uint16_t* w_router,
+                        const float* bias, int residual, int32_t* ids_out, double* w_out,
+                        double* logits_out, int n_threads) {
+  if (T < 0 || H <= 0 || E <= 0 || K <= 0 || K > E || !x || !w_router) return -1;
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > T) n_threads = T > 0 ? T : 1;
+  route_job* jobs = (route_job*)calloc((size_t)n_threads, sizeof(route_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+  for (int i = 0; i < n_threads; ++i) {
+    route_job* j = &jobs[i];
+    j->x = x;
+    j->T = T;
+    j->H = H;
+    j->E = E;
+    j->K = K;
+    j->w_router = w_router;
+    j->bias = bias;
+    j->residual = residual;
+    j->ids_out = ids_out;
+    j->w_out = w_out;
+    j->logits_out = logits_out;
+    j->n_threads = n_threads;
+    j->tid = i;
+  }
+  if (n_threads == 1) {
+    route_worker(&jobs[0]);
+  } else {
+    for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, route_worker, &jobs[i]);
+    for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  }
+  free(jobs);
+  free(th);
+  return 0;
+}

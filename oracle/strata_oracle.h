@@ -71,6 +71,12 @@ void oracle_expert(const uint8_t* blob, int H, int FF, int q2_offset, const doub
 /* x / sqrt(mean(x^2) + eps). */
 void oracle_rmsnorm(const double* x, int H, double eps, double* xn);
 
+/* Steps 1-2 only for T tokens (router input = x, or rmsnorm(x) when residual): ids [T][K],
+ * w [T][K], logits [T][E] (each nullable). n_threads splits tokens. Returns 0 or -1. */
+int oracle_route_tokens(const float* x, int T, int H, int E, int K, const uint16_t* w_router,
+                        const float* bias, int residual, int32_t* ids_out, double* w_out,
+                        double* logits_out, int n_threads);
+
 /* One MoE layer for T tokens.
  *   x: fp32 [T][H].  w_router: bf16 [E][H].  bias: fp32 [E] or NULL.
  *   blobs: E pointers to canonical blobs (an entry may be NULL if that expert is never routed).

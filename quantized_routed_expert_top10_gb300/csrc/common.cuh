@@ -1,0 +1,254 @@
+// Internal definitions shared by the sm_103a kernels of the routed-expert MoE block.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "strata_moe.h"
+
+namespace strata {
+
+// Dimensions fixed by the model ("The byte budget, in code": H = 2560, FF = 640, QK = 64, top-10).
+constexpr int H = STRATA_MOE_H;
+constexpr int FF = STRATA_MOE_FF;
+constexpr int K = STRATA_MOE_K;
+constexpr int QK = STRATA_MOE_QK;
+constexpr int EMAX = STRATA_MOE_E_MAX;
+constexpr int TMAX = STRATA_MOE_T_MAX;
+constexpr int KB_GU = H / QK;  // 40 k-blocks along gate/up's contraction
+constexpr int KB_D = FF / QK;  // 10 k-blocks along down's contraction
+constexpr int RT = 128;        // rows per packed row tile
+constexpr int RT_GU = FF / RT; // 5 gate/up row tiles
+constexpr int RT_D = H / RT;   // 20 down row tiles
+constexpr int GU_CHUNK = 4608; // bytes per (rt, kb) gate+up chunk
+constexpr int D_CHUNK = 2304;  // bytes per (rt, kb) down chunk
+constexpr int64_t D_REGION = 921600;
+constexpr int64_t BLOB = STRATA_MOE_BLOB_BYTES;
+
+// GEMV expert path: up to NT tokens of one expert per tile; the gate/up contraction is split
+// S_SPLIT ways when the call is small (decode), so enough CTAs stream the weights.
+constexpr int NT = 8;
+constexpr int S_SPLIT = 4;
+constexpr int DECODE_T_MAX = 8;  // T <= this: fused single-kernel routing (router + top-10 + grouping)
+
+// Device status bits (ws word 0).
+constexpr int ST_CORRUPT = 1;
+constexpr int ST_TIMEOUT = 2;
+
+// A 64-wide block of an activation vector, quantised to 16-bit integers q ~= v / s and split into
+// hi (signed) and lo (unsigned) bytes, laid out for the Q2_0 code masks: word (q4, m) holds the
+// values of weights 16*q4 + 4*b + m, b = 0..3 (byte b), matching (codes & (3 << 2m)) of code word q4.
+struct __align__(16) QBlock {
+  uint32_t hi[16];
+  uint32_t lo[16];
+  float s64;    // s / 64, s = max|v| / 32767
+  int32_t qoff; // 64 * q2_offset * sum(q)
+  int32_t pad[2];
+};
+static_assert(sizeof(QBlock) == 144, "QBlock layout");
+
+struct __align__(16) Tile {
+  int32_t e;   // expert id
+  int32_t q0;  // first slot (index into the sorted pair array)
+  int32_t n;   // tokens in the tile (1..NT)
+  int32_t pad;
+};
+
+// Workspace layout for a call with T tokens (byte offsets, each 256-aligned).  The first
+// WS_HEADER bytes (status word and counters) are the same for every T and are zeroed once by
+// strata_moe_workspace_init; kernels that use a counter reset it before they finish.
+constexpr size_t WS_HEADER = 4096;
+constexpr size_t WS_STATUS = 0;     // int32 status word
+constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
+constexpr size_t WS_CNT_GU = 256;   // int32 [max_tiles(DECODE_T_MAX)][RT_GU] split counters
+
+struct WsLayout {
+  size_t status, cnt_route, cnt_gu;
+  size_t logits;      // fp32 [T][EMAX]
+  size_t ids;         // int32 [T][K]
+  size_t weights;     // fp32 [T][K]
+  size_t xn;          // fp32 [T][H] normalised input (residual layers, T > DECODE_T_MAX)
+  size_t expert_off;  // int32 [EMAX + 1]
+  size_t pair;        // int32 [T*K]
+  size_t active;      // int32 [EMAX]
+  size_t n_active;    // int32 [4]: n_active, n_tiles
+  size_t tiles;       // Tile [max_tiles]
+  size_t chunk_cnt;   // int32 [n_chunks][EMAX]
+  size_t qx;          // QBlock [T][KB_GU]
+  size_t partial;     // fp32 [max_tiles][RT_GU][S_SPLIT][NT][RT][2] (decode split-K partials)
+  size_t hq;          // QBlock [T*K][KB_D]
+  size_t parts;       // fp32 [T*K][H]
+  size_t total;
+  int max_tiles;
+  int n_chunks;
+};
+
+constexpr int GROUP_CHUNK = 2048;  // pairs per grouping chunk
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Each expert's n_e pairs need ceil(n_e / NT) tiles: at most P / NT + min(P, EMAX) in all.
+inline int max_tiles_for(int T) {
+  const int P = T * K;
+  return P / NT + (P < EMAX ? P : EMAX);
+}
+
+inline WsLayout ws_layout(int T) {
+  WsLayout L{};
+  const int P = T * K;
+  L.max_tiles = max_tiles_for(T);
+  L.n_chunks = (P + GROUP_CHUNK - 1) / GROUP_CHUNK;
+  if (L.n_chunks < 1) L.n_chunks = 1;
+  L.status = WS_STATUS;
+  L.cnt_route = WS_CNT_ROUTE;
+  L.cnt_gu = WS_CNT_GU;
+  size_t o = WS_HEADER;
+  auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+  L.logits = take(sizeof(float) * (size_t)T * EMAX);
+  L.ids = take(sizeof(int32_t) * (size_t)P);
+  L.weights = take(sizeof(float) * (size_t)P);
+  L.xn = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);
+  L.expert_off = take(sizeof(int32_t) * (EMAX + 1));
+  L.pair = take(sizeof(int32_t) * (size_t)P);
+  L.active = take(sizeof(int32_t) * EMAX);
+  L.n_active = take(sizeof(int32_t) * 4);
+  L.tiles = take(sizeof(Tile) * (size_t)L.max_tiles);
+  L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.n_chunks * EMAX);
+  L.qx = take(sizeof(QBlock) * (size_t)T * KB_GU);
+  // sized for min(T, DECODE_T_MAX) so the total grows with T (a workspace sized for T serves any T' <= T)
+  const int Td = T < DECODE_T_MAX ? T : DECODE_T_MAX;
+  L.partial = take(sizeof(float) * (size_t)max_tiles_for(Td) * RT_GU * S_SPLIT * NT * RT * 2);
+  L.hq = take(sizeof(QBlock) * (size_t)P * KB_D);
+  L.parts = take(sizeof(float) * (size_t)P * H);
+  L.total = T > 0 ? o : WS_HEADER;
+  return L;
+}
+static_assert(WS_CNT_GU + sizeof(int32_t) * (size_t)(DECODE_T_MAX * K / NT + DECODE_T_MAX * K) * RT_GU <= WS_HEADER,
+              "decode split counters must fit in the workspace header");
+
+// ---------------------------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Quantise one 64-value block held as two values per lane (lane l: v0 = v[2l], v1 = v[2l+1]) into
+// a QBlock.  Must be called by a full warp; `tmp` is 64 int32 of shared memory for this warp.
+__device__ __forceinline__ void quantise_block_warp(float v0, float v1, int q2_offset, QBlock* dst,
+                                                    int32_t* tmp) {
+  const int lane = threadIdx.x & 31;
+  const float amax = warp_max(fmaxf(fabsf(v0), fabsf(v1)));
+  int q0 = 0, q1 = 0;
+  if (amax > 0.f) {
+    const float inv = 32767.f / amax;
+    q0 = max(-32767, min(32767, __float2int_rn(v0 * inv)));
+    q1 = max(-32767, min(32767, __float2int_rn(v1 * inv)));
+  }
+  tmp[2 * lane] = q0;
+  tmp[2 * lane + 1] = q1;
+  int qs = q0 + q1;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+  __syncwarp();
+  // lane -> word: lanes 0..15 hi words, 16..31 lo words; word index w = q4 * 4 + m.
+  const int w = lane & 15;
+  const int q4 = w >> 2, m = w & 3;
+  uint32_t word = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int v = tmp[16 * q4 + 4 * b + m];
+    const uint32_t byte = (lane < 16) ? (uint32_t)((v >> 8) & 0xFF) : (uint32_t)(v & 0xFF);
+    word |= byte << (8 * b);
+  }
+  if (lane < 16) dst->hi[w] = word; else dst->lo[w] = word;
+  if (lane == 0) {
+    dst->s64 = (amax > 0.f) ? (amax / 32767.f) * (1.f / 64.f) : 0.f;
+    dst->qoff = 64 * q2_offset * qs;
+  }
+  __syncwarp();
+}
+
+// Sum over the code masks of one 16-byte Q2_0 code row against one QBlock's words, returning
+// 64 * (sum_i c_i * q_i); the caller subtracts qoff and scales by d * s64.
+struct Masked { uint32_t m[16]; };
+
+__device__ __forceinline__ Masked mask_codes(uint4 c) {
+  Masked r;
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    r.m[4 * q + 0] = w[q] & 0x03030303u;
+    r.m[4 * q + 1] = w[q] & 0x0C0C0C0Cu;
+    r.m[4 * q + 2] = w[q] & 0x30303030u;
+    r.m[4 * q + 3] = w[q] & 0xC0C0C0C0u;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int dot64(const Masked& c, const uint32_t* hi, const uint32_t* lo) {
+  int ah[4] = {0, 0, 0, 0}, al[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      ah[m] = dp4a_us(c.m[4 * q + m], hi[4 * q + m], ah[m]);
+      al[m] = dp4a_uu(c.m[4 * q + m], lo[4 * q + m], al[m]);
+    }
+  }
+  // ah[m] = 4^m * S_hi,m  ->  64 * S_hi = 64 ah0 + 16 ah1 + 4 ah2 + ah3 (exact in int32).
+  const int sh = ((ah[0] * 4 + ah[1]) * 4 + ah[2]) * 4 + ah[3];
+  const int sl = ((al[0] * 4 + al[1]) * 4 + al[2]) * 4 + al[3];
+  return sh * 256 + sl;
+}
+
+}  // namespace strata
+
+// Launchers implemented in the .cu files (all enqueue on `stream`, return cudaGetLastError()).
+namespace strata {
+cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
+                                const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
+                                float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s);
+cudaError_t launch_router_logits(const float* x, int T, const uint16_t* w_router, const float* bias,
+                                 int E, float* logits, cudaStream_t s);
+cudaError_t launch_top_k(const float* logits, int T, int E, int32_t* ids, float* weights, cudaStream_t s);
+cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair,
+                         int32_t* active, int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s);
+cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
+                               int T, const WsLayout& L, char* ws, cudaStream_t s);
+cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s);
+cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t* pair, const WsLayout& L,
+                                char* ws, float* parts, cudaStream_t s);
+cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
+                           float* out, cudaStream_t s);
+cudaError_t launch_pack_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed,
+                               int64_t dst_stride, int64_t n_blobs, cudaStream_t s);
+}  // namespace strata
+
+namespace strata {
+void pack_host(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs);
+void unpack_host(const uint8_t* packed, uint8_t* canonical, int64_t n_blobs);
+}  // namespace strata

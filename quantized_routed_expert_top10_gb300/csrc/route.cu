@@ -1,0 +1,551 @@
+// Router (steps 1-2) and token grouping (step 3) of the routed-expert MoE block, sm_103a.
+//
+// zwxr.cn news/242664, section "一次路由的完整旅程": moe_route projects the normalised activation
+// with a BF16 GEMV to 512 expert logits; native_router_top10 does a softmax over all 512, a stable
+// descending argsort, gathers the first 10 and renormalises with ggml's lower clamp.
+// momoyeyu.github.io "ai-infra-strata", section "提示词处理": tokens are gathered per expert so a
+// single read of an expert's weights serves every token routed to it.
+#include "common.cuh"
+
+namespace strata {
+namespace {
+
+constexpr float kRenormFloor = 6.103515625e-05f;  // 2^-14
+
+// ---------------------------------------------------------------------------------------------
+// top-k of one token's logits by one warp: softmax over E (E % 32 == 0, E <= 512), the K
+// largest probabilities in descending order (lower id first on equal values), renormalised.
+// ---------------------------------------------------------------------------------------------
+__device__ void top_k_warp(const float* logits, int E, int32_t* ids, float* weights) {
+  const int lane = threadIdx.x & 31;
+  const int per = E >> 5;
+  float l[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) l[j] = (j < per) ? __ldcg(logits + lane + 32 * j) : -INFINITY;
+  float m = l[0];
+#pragma unroll
+  for (int j = 1; j < 16; ++j) m = fmaxf(m, l[j]);
+  m = warp_max(m);
+  float p[16];
+  float z = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    p[j] = (j < per) ? expf(l[j] - m) : 0.f;
+    z += p[j];
+  }
+  z = warp_sum(z);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) p[j] = (j < per) ? p[j] / z : -1.f;
+  uint32_t taken = 0;
+  float sel_p[K];
+  int sel_id[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float bv = -2.f;
+    int bid = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (!((taken >> j) & 1u) && p[j] > bv) {  // ids grow with j: first max is the lowest id
+        bv = p[j];
+        bid = lane + 32 * j;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+      if (ov > bv || (ov == bv && oid < bid)) {
+        bv = ov;
+        bid = oid;
+      }
+    }
+    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    sel_p[k] = bv;
+    sel_id[k] = bid;
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < K; ++k) s += sel_p[k];
+  const float denom = fmaxf(s, kRenormFloor);
+  if (lane < K) {
+    float pk = sel_p[0];
+    int ik = sel_id[0];
+#pragma unroll
+    for (int k = 1; k < K; ++k)
+      if (lane == k) { pk = sel_p[k]; ik = sel_id[k]; }
+    ids[lane] = ik;
+    weights[lane] = pk / denom;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Grouping: counting sort of pair numbers p = t*K + k by expert (stable), active experts, tiles.
+// ---------------------------------------------------------------------------------------------
+
+// Exclusive scan of cnt[0..E) in shared memory by a whole CTA of 128..1024 threads; returns the
+// total; out may alias cnt.  scratch: >= 32 ints.
+__device__ int cta_exclusive_scan(const int* cnt, int* out, int E, int* scratch) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (E + nt - 1) / nt;
+  const int b0 = tid * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (b0 + i < E) local += cnt[b0 + i];
+  // warp-level inclusive scan of the per-thread sums
+  const int lane = tid & 31, warp = tid >> 5;
+  int v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nt >> 5;
+    int w = (lane < nw) ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < nw) scratch[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int total = scratch[(nt >> 5) - 1];
+  int run = v - local + (warp ? scratch[warp - 1] : 0);
+  __syncthreads();
+  for (int i = 0; i < per; ++i) {
+    if (b0 + i < E) {
+      const int c = cnt[b0 + i];
+      out[b0 + i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// From per-expert counts (shared) build expert_off, active, n_active and the tile list.
+// Whole CTA; cnt is shared [E]; sh_off, sh_tile shared [E]; scratch shared [>= 32].
+__device__ void finish_grouping(const int* cnt, int E, int* sh_off, int* sh_tile, int* scratch,
+                                int32_t* expert_off, int32_t* active, int32_t* n_active_tiles, Tile* tiles,
+                                int max_tiles) {
+  const int tid = threadIdx.x;
+  const int total = cta_exclusive_scan(cnt, sh_off, E, scratch);
+  for (int e = tid; e < E; e += blockDim.x) expert_off[e] = sh_off[e];
+  if (tid == 0) expert_off[E] = total;
+  // active list: exclusive scan of (cnt > 0) flags (reuse sh_tile as the flag array)
+  for (int e = tid; e < E; e += blockDim.x) sh_tile[e] = cnt[e] > 0 ? 1 : 0;
+  __syncthreads();
+  const int na = cta_exclusive_scan(sh_tile, sh_tile, E, scratch);
+  for (int e = tid; e < E; e += blockDim.x)
+    if (cnt[e] > 0) active[sh_tile[e]] = e;
+  __syncthreads();
+  // tiles: ceil(cnt / NT) per expert
+  for (int e = tid; e < E; e += blockDim.x) sh_tile[e] = (cnt[e] + NT - 1) / NT;
+  __syncthreads();
+  const int ntiles = cta_exclusive_scan(sh_tile, sh_tile, E, scratch);
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int c = cnt[e];
+    const int nt = (c + NT - 1) / NT;
+    for (int j = 0; j < nt; ++j) {
+      const int idx = sh_tile[e] + j;
+      if (idx < max_tiles) {
+        Tile tl;
+        tl.e = e;
+        tl.q0 = sh_off[e] + j * NT;
+        tl.n = min(NT, c - j * NT);
+        tl.pad = 0;
+        tiles[idx] = tl;
+      }
+    }
+  }
+  if (tid == 0) {
+    n_active_tiles[0] = na;
+    n_active_tiles[1] = ntiles < max_tiles ? ntiles : max_tiles;
+  }
+}
+
+// Stable scatter of pairs [p0, p1) by one warp: fill[e] (shared) holds the next slot of expert e.
+__device__ void stable_scatter_warp(const int32_t* ids, int p0, int p1, int E, int* fill, int32_t* pair) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    int e = (p < p1) ? ids[p] : -1;
+    if (e >= E || e < 0) e = -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & lt);
+    int pos = 0;
+    if (e >= 0) pos = fill[e] + rank;
+    __syncwarp();
+    if (e >= 0) {
+      pair[pos] = p;
+      if ((same >> lane) == 1u) fill[e] += __popc(same);  // highest lane of the group
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode routing: one kernel for T <= DECODE_T_MAX.  Every CTA computes 4 logits rows (one per
+// warp) for all tokens and quantises a share of the expert input; the last CTA to finish runs
+// top-k for every token, the grouping and the tile list.
+// ---------------------------------------------------------------------------------------------
+template <int TT>
+__global__ void __launch_bounds__(128) route_decode_kernel(
+    const float* __restrict__ x, int T, int apply_rmsnorm, const uint16_t* __restrict__ wr,
+    const float* __restrict__ bias, int E, int q2_offset, float* __restrict__ logits,
+    float* __restrict__ logits_user, int32_t* __restrict__ ids, float* __restrict__ weights,
+    int32_t* __restrict__ expert_off, int32_t* __restrict__ pair, int32_t* __restrict__ active,
+    int32_t* __restrict__ n_active_tiles, Tile* __restrict__ tiles, int max_tiles, QBlock* __restrict__ qx,
+    int* __restrict__ counter, int* __restrict__ status) {
+  __shared__ float s_inv[TT];
+  __shared__ float s_red[4][TT];
+  __shared__ int32_t s_tmp[4][64];
+  __shared__ int s_cnt[EMAX];
+  __shared__ int s_off[EMAX];
+  __shared__ int s_tile[EMAX];
+  __shared__ int s_scratch[32];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // 1/rms per token (every CTA recomputes it; x is tiny and L2-resident).
+  if (apply_rmsnorm) {
+    float ss[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) ss[t] = 0.f;
+    for (int h = tid; h < H; h += 128) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+        if (t < T) { const float v = x[(size_t)t * H + h]; ss[t] += v * v; }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const float r = warp_sum(ss[t]);
+      if (lane == 0) s_red[warp][t] = r;
+    }
+    __syncthreads();
+    if (tid < TT) {
+      const float r = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
+      s_inv[tid] = 1.f / sqrtf(r / (float)H + 1e-6f);
+    }
+  } else if (tid < TT) {
+    s_inv[tid] = 1.f;
+  }
+  __syncthreads();
+
+  // Router GEMV: warp -> expert row e; lane covers 8 columns per step, 10 steps.
+  const int e = blockIdx.x * 4 + warp;
+  if (e < E) {
+    float acc[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
+#pragma unroll 5
+    for (int i = 0; i < H / 256; ++i) {
+      const int c = 8 * lane + 256 * i;
+      const uint4 wv = __ldg(wrow + (c >> 3));
+      float wf[8];
+      wf[0] = __uint_as_float(wv.x << 16); wf[1] = __uint_as_float(wv.x & 0xffff0000u);
+      wf[2] = __uint_as_float(wv.y << 16); wf[3] = __uint_as_float(wv.y & 0xffff0000u);
+      wf[4] = __uint_as_float(wv.z << 16); wf[5] = __uint_as_float(wv.z & 0xffff0000u);
+      wf[6] = __uint_as_float(wv.w << 16); wf[7] = __uint_as_float(wv.w & 0xffff0000u);
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        if (t < T) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H + c));
+          const float4 b = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H + c + 4));
+          float s = acc[t];
+          s = fmaf(wf[0], a.x, s); s = fmaf(wf[1], a.y, s); s = fmaf(wf[2], a.z, s); s = fmaf(wf[3], a.w, s);
+          s = fmaf(wf[4], b.x, s); s = fmaf(wf[5], b.y, s); s = fmaf(wf[6], b.z, s); s = fmaf(wf[7], b.w, s);
+          acc[t] = s;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const float r = warp_sum(acc[t]);
+      if (lane == 0 && t < T) {
+        const float v = r * s_inv[t] + (bias ? bias[e] : 0.f);
+        logits[(size_t)t * EMAX + e] = v;
+        if (logits_user) logits_user[(size_t)t * E + e] = v;
+      }
+    }
+  }
+
+  // Quantise the expert input (rmsnorm(x) or x), one 64-block per warp.
+  {
+    const int nblk = T * KB_GU;
+    for (int b = blockIdx.x * 4 + warp; b < nblk; b += gridDim.x * 4) {
+      const int t = b / KB_GU, kb = b % KB_GU;
+      const float2 v = *reinterpret_cast<const float2*>(x + (size_t)t * H + kb * QK + 2 * lane);
+      quantise_block_warp(v.x * s_inv[t], v.y * s_inv[t], q2_offset, qx + b, s_tmp[warp]);
+    }
+  }
+
+  // Last CTA: top-k for all tokens, then grouping.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(counter, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = warp; t < T; t += 4) top_k_warp(logits + (size_t)t * EMAX, E, ids + t * K, weights + t * K);
+  for (int i = tid; i < E; i += 128) s_cnt[i] = 0;
+  __syncthreads();
+  const int P = T * K;
+  for (int p = tid; p < P; p += 128) {
+    const int ee = ids[p];
+    if (ee < 0 || ee >= E) set_status(status, ST_CORRUPT);
+    else atomicAdd(&s_cnt[ee], 1);
+  }
+  __syncthreads();
+  finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
+  __syncthreads();
+  if (warp == 0) stable_scatter_warp(ids, 0, P, E, s_off, pair);
+  if (tid == 0) *counter = 0;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Prefill routing kernels.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, float* __restrict__ xn) {
+  __shared__ float s_red[8];
+  const int t = blockIdx.x;
+  const float* xr = x + (size_t)t * H;
+  float ss = 0.f;
+  for (int h = threadIdx.x; h < H; h += 256) { const float v = xr[h]; ss += v * v; }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += s_red[w];
+  const float inv = 1.f / sqrtf(tot / (float)H + 1e-6f);
+  for (int h = threadIdx.x; h < H; h += 256) xn[(size_t)t * H + h] = xr[h] * inv;
+}
+
+// logits[t][e] = sum_h x[t][h] * W[e][h] + bias[e], fp32 FFMA GEMM: 64 tokens x 64 experts per
+// CTA, 256 threads with 4 x 4 outputs each, k-steps of 32.
+__global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restrict__ x, int T,
+                                                          const uint16_t* __restrict__ wr,
+                                                          const float* __restrict__ bias, int E,
+                                                          float* __restrict__ logits, int ld_logits) {
+  __shared__ float sx[32][64 + 4];
+  __shared__ float sw[32][64 + 4];
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;  // outputs rows t0 + ty*4 .., cols e0 + tx*4 ..
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += 32) {
+    // load 64 x 32 of x and of W (transposed into [k][row])
+    for (int i = tid; i < 64 * 32; i += 256) {
+      const int r = i >> 5, k = i & 31;
+      const int t = t0 + r;
+      sx[k][r] = (t < T) ? x[(size_t)t * H + k0 + k] : 0.f;
+      const int e = e0 + r;
+      sw[k][r] = (e < E) ? __uint_as_float((uint32_t)wr[(size_t)e * H + k0 + k] << 16) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&sx[k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&sw[k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) logits[(size_t)t * ld_logits + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ logits, int ld, int T, int E,
+                                                    int32_t* __restrict__ ids, float* __restrict__ weights) {
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (t < T) top_k_warp(logits + (size_t)t * ld, E, ids + t * K, weights + t * K);
+}
+
+__global__ void __launch_bounds__(256) group_hist_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                         int32_t* __restrict__ chunk_cnt, int* status) {
+  __shared__ int cnt[EMAX];
+  for (int i = threadIdx.x; i < E; i += 256) cnt[i] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
+  for (int p = p0 + threadIdx.x; p < p1; p += 256) {
+    const int e = ids[p];
+    if (e < 0 || e >= E) set_status(status, ST_CORRUPT);
+    else atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += 256) chunk_cnt[(size_t)blockIdx.x * EMAX + i] = cnt[i];
+}
+
+// One CTA of 512 threads: per-expert running base over chunks (chunk_cnt becomes exclusive bases
+// within each expert), then offsets, active list and tiles.
+__global__ void __launch_bounds__(512) group_scan_kernel(int n_chunks, int E, int32_t* __restrict__ chunk_cnt,
+                                                         int32_t* __restrict__ expert_off,
+                                                         int32_t* __restrict__ active,
+                                                         int32_t* __restrict__ n_active_tiles,
+                                                         Tile* __restrict__ tiles, int max_tiles) {
+  __shared__ int s_cnt[EMAX], s_off[EMAX], s_tile[EMAX], s_scratch[32];
+  const int e = threadIdx.x;
+  if (e < E) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int v = chunk_cnt[(size_t)c * EMAX + e];
+      chunk_cnt[(size_t)c * EMAX + e] = run;
+      run += v;
+    }
+    s_cnt[e] = run;
+  }
+  __syncthreads();
+  finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
+}
+
+// One warp per chunk: stable scatter starting from expert_off[e] + chunk base.
+__global__ void __launch_bounds__(32) group_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                           const int32_t* __restrict__ chunk_cnt,
+                                                           const int32_t* __restrict__ expert_off,
+                                                           int32_t* __restrict__ pair) {
+  __shared__ int fill[EMAX];
+  for (int i = threadIdx.x; i < E; i += 32)
+    fill[i] = expert_off[i] + chunk_cnt[(size_t)blockIdx.x * EMAX + i];
+  __syncwarp();
+  const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
+  stable_scatter_warp(ids, p0, p1, E, fill, pair);
+}
+
+// Tiles from a caller-provided grouping (strata_moe_experts): one CTA.  The arrays come from the
+// caller, so every expert id and slot range is checked; a bad entry sets ST_CORRUPT and is skipped.
+__global__ void __launch_bounds__(512) build_tiles_kernel(const int32_t* __restrict__ expert_off,
+                                                          const int32_t* __restrict__ active,
+                                                          const int32_t* __restrict__ n_active_in, int E, int P,
+                                                          int32_t* __restrict__ n_active_tiles,
+                                                          Tile* __restrict__ tiles, int max_tiles, int* status) {
+  __shared__ int s_nt[EMAX], s_scratch[32];
+  const int na = max(0, min(*n_active_in, E));
+  const int i = threadIdx.x;
+  int c = 0, e = 0, q0 = 0;
+  if (i < na) {
+    e = active[i];
+    if (e < 0 || e >= E) {
+      set_status(status, ST_CORRUPT);
+    } else {
+      q0 = expert_off[e];
+      c = expert_off[e + 1] - q0;
+      if (q0 < 0 || c < 0 || q0 + c > P) {
+        set_status(status, ST_CORRUPT);
+        c = 0;
+      }
+    }
+  }
+  s_nt[i] = (c + NT - 1) / NT;
+  __syncthreads();
+  const int ntiles = cta_exclusive_scan(s_nt, s_nt, EMAX, s_scratch);
+  const int nt = (c + NT - 1) / NT;
+  for (int j = 0; j < nt; ++j) {
+    const int idx = s_nt[i] + j;
+    if (idx < max_tiles) {
+      Tile tl;
+      tl.e = e;
+      tl.q0 = q0 + j * NT;
+      tl.n = min(NT, c - j * NT);
+      tl.pad = 0;
+      tiles[idx] = tl;
+    }
+  }
+  if (i == 0) {
+    n_active_tiles[0] = na;
+    n_active_tiles[1] = ntiles < max_tiles ? ntiles : max_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(128) quantise_x_kernel(const float* __restrict__ x, int T, int q2_offset,
+                                                         QBlock* __restrict__ qx) {
+  __shared__ int32_t tmp[4][64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 4 + warp;
+  if (b >= T * KB_GU) return;
+  const int t = b / KB_GU, kb = b % KB_GU;
+  const float2 v = *reinterpret_cast<const float2*>(x + (size_t)t * H + kb * QK + 2 * lane);
+  quantise_block_warp(v.x, v.y, q2_offset, qx + b, tmp[warp]);
+}
+
+}  // namespace
+
+cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
+                                const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
+                                float* logits_out, const WsLayout& L, char* ws, cudaStream_t s) {
+  const int grid = (E + 3) / 4;
+#define STRATA_ROUTE_ARGS                                                                           \
+  x, T, apply_rmsnorm, w_router, bias, E, q2_offset, (float*)(ws + L.logits), logits_out, ids, weights, \
+      (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair), (int32_t*)(ws + L.active),              \
+      (int32_t*)(ws + L.n_active), (Tile*)(ws + L.tiles), L.max_tiles, (QBlock*)(ws + L.qx),           \
+      (int*)(ws + L.cnt_route), (int*)(ws + L.status)
+  if (T <= 1) route_decode_kernel<1><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
+  else if (T <= 2) route_decode_kernel<2><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
+  else if (T <= 4) route_decode_kernel<4><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
+  else route_decode_kernel<8><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
+#undef STRATA_ROUTE_ARGS
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s) {
+  rmsnorm_kernel<<<T, 256, 0, s>>>(x, xn);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_logits(const float* x, int T, const uint16_t* w_router, const float* bias, int E,
+                                 float* logits, cudaStream_t s) {
+  dim3 grid((T + 63) / 64, (E + 63) / 64);
+  router_gemm_kernel<<<grid, 256, 0, s>>>(x, T, w_router, bias, E, logits, E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_top_k(const float* logits, int T, int E, int32_t* ids, float* weights, cudaStream_t s) {
+  top_k_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, E, T, E, ids, weights);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair, int32_t* active,
+                         int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s) {
+  const int P = T * K;
+  int32_t* chunk_cnt = (int32_t*)(ws + L.chunk_cnt);
+  int32_t* nat = (int32_t*)(ws + L.n_active);
+  group_hist_kernel<<<L.n_chunks, 256, 0, s>>>(ids, P, E, chunk_cnt, (int*)(ws + L.status));
+  group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat, (Tile*)(ws + L.tiles),
+                                      L.max_tiles);
+  group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair);
+  if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
+                               int T, const WsLayout& L, char* ws, cudaStream_t s) {
+  build_tiles_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, E, T * K, (int32_t*)(ws + L.n_active),
+                                       (Tile*)(ws + L.tiles), L.max_tiles, (int*)(ws + L.status));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s) {
+  const int nblk = T * KB_GU;
+  quantise_x_kernel<<<(nblk + 3) / 4, 128, 0, s>>>(x, T, q2_offset, qx);
+  return cudaGetLastError();
+}
+
+}  // namespace strata

@@ -1,0 +1,128 @@
+"""Shared helpers of the GPU parity tests: device inputs, C-ABI calls and the comparison rules.
+
+Comparison rules (from the statement of the block):
+  - router ids and grouping bit-exact, except that where the oracle's 10th and 11th logits are
+    within 1e-4 any tied expert may be chosen, and ids whose logits are within 1e-4 may swap order;
+  - expert / combine outputs: max|gpu - oracle| <= 2e-3 * max|oracle| (fp32 accumulation).
+Outputs are compared with the oracle run on the GPU's own ids (teacher forcing), so a tie that
+picks another expert is checked against that expert's real output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import gen
+import oracle
+import quantized_routed_expert_top10_gb300 as qre
+
+TIE = 1e-4
+REL_TOL = 2e-3
+DEV = torch.device("cuda:0")
+B = qre.BLOB_BYTES
+
+
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+_table = None
+
+
+def scale_table_dev():
+    global _table
+    if _table is None:
+        _table = to_dev(gen.SCALE_TABLE.view(np.uint16))
+    return _table
+
+
+def device_canonical(seed, layer, e0, n, out=None):
+    if out is None:
+        out = torch.empty(n * B, dtype=torch.uint8, device=DEV)
+    gen.device_canonical_blobs(seed, layer, e0, n, scale_table_dev().data_ptr(), out.data_ptr(), B,
+                               torch.cuda.current_stream().cuda_stream)
+    return out
+
+
+def device_packed_layer(seed, layer, E=512, out=None, tmp=None):
+    """Packed blobs of one layer's E experts, generated and packed on the GPU."""
+    canon = device_canonical(seed, layer, 0, E, tmp)
+    if out is None:
+        out = torch.empty(E * B, dtype=torch.uint8, device=DEV)
+    qre.strata_pack_q2_0_device(canon, B, out, B, E)
+    return out
+
+
+def host_packed(canon_list):
+    canon = np.concatenate(canon_list)
+    packed = np.empty_like(canon)
+    qre.strata_pack_q2_0(canon, packed, len(canon_list))
+    return to_dev(packed)
+
+
+class BlobCache:
+    """Canonical blobs from the host generator, drawn on demand (the oracle's inputs)."""
+
+    def __init__(self, seed):
+        self.seed = seed
+        self.cache = {}
+
+    def get(self, layer, e):
+        key = (layer, e)
+        if key not in self.cache:
+            self.cache[key] = gen.canonical_blob(self.seed, layer, e)
+        return self.cache[key]
+
+    def layer_list(self, layer, ids, E=512):
+        need = set(np.unique(ids).tolist())
+        return [self.get(layer, e) if e in need else None for e in range(E)]
+
+
+def workspace(T):
+    n = qre.strata_moe_workspace_bytes(T)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    qre.strata_moe_workspace_init(ws)
+    return ws
+
+
+def check_routing(gpu_ids: np.ndarray, ref_ids: np.ndarray, ref_logits: np.ndarray) -> int:
+    """Assert the GPU ids are the oracle's up to 1e-4 ties; returns how many tokens needed the rule."""
+    T = gpu_ids.shape[0]
+    ties = 0
+    for t in range(T):
+        g = gpu_ids[t]
+        if np.array_equal(g, ref_ids[t]):
+            continue
+        ties += 1
+        l = ref_logits[t]
+        assert len(set(g.tolist())) == g.size, f"token {t}: repeated ids {g}"
+        l10 = np.sort(l)[-10]
+        chosen = l[g]
+        others = np.delete(l, g)
+        assert chosen.min() >= l10 - TIE, f"token {t}: {g} is not a top-10 of the oracle logits"
+        assert others.max() <= chosen.min() + TIE, f"token {t}: an unchosen expert beats a chosen one"
+        assert np.all(np.diff(chosen) <= TIE), f"token {t}: order not descending within 1e-4"
+    return ties
+
+
+def check_close(gpu: np.ndarray, ref: np.ndarray, what: str):
+    err = np.abs(gpu.astype(np.float64) - ref).max() if ref.size else 0.0
+    bound = REL_TOL * np.abs(ref).max() if ref.size else 0.0
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e}"
+    return err, bound
+
+
+def run_layer(blobs, wr, bias, x, flags=0, q2_offset=1, E=512, ws=None):
+    T = x.shape[0]
+    ws = workspace(T) if ws is None else ws
+    xd = to_dev(x)
+    out = torch.empty(T, qre.H, dtype=torch.float32, device=DEV)
+    ids = torch.empty(T, qre.K, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, qre.K, dtype=torch.float32, device=DEV)
+    ex = qre.experts(blobs, E, q2_offset)
+    qre.strata_moe_layer(ex, to_dev(wr), None if bias is None else to_dev(bias), xd, T, flags, out, ids, w, ws)
+    st = qre.strata_poll_status(ws)
+    assert st == 0, qre.STATUS.get(st, st)
+    return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()

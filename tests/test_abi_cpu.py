@@ -1,0 +1,140 @@
+"""C ABI checks that need no GPU: the library loads and exports every symbol the header declares,
+the host packer is a byte permutation that matches the layout the header documents, and host-side
+argument checks reject bad calls before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gen
+import quantized_routed_expert_top10_gb300 as qre
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "strata_moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(strata_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(qre.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return qre.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) == 14
+    assert sorted(names) == sorted(qre.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in qre.STATUS.items():
+        assert qre.strata_status_str(code).startswith(name)
+    assert "unknown" in qre.strata_status_str(42)
+
+
+def test_workspace_sizes(lib):
+    assert qre.strata_moe_workspace_bytes(-1) == 0
+    assert qre.strata_moe_workspace_bytes(8193) == 0
+    sizes = [qre.strata_moe_workspace_bytes(t) for t in (0, 1, 4, 8, 9, 2048, 8192)]
+    assert sizes[0] == 4096
+    assert all(b > a for a, b in zip(sizes, sizes[1:]))
+    assert all(s % 256 == 0 for s in sizes)
+
+
+def test_pack_round_trip_and_documented_layout(lib):
+    n = 2
+    canon = np.concatenate([gen.canonical_blob(3, 1, e) for e in range(n)])
+    packed = np.zeros_like(canon)
+    qre.strata_pack_q2_0(canon, packed, n)
+    assert not np.array_equal(packed, canon)
+    assert np.array_equal(np.sort(packed), np.sort(canon))
+    back = np.zeros_like(canon)
+    qre.strata_unpack_q2_0(packed, back, n)
+    np.testing.assert_array_equal(back, canon)
+    # Spot checks against the layout in strata_moe.h.
+    B = qre.BLOB_BYTES
+    for j in range(n):
+        c = canon[j * B:(j + 1) * B].reshape(-1, 18)
+        p = packed[j * B:(j + 1) * B]
+        for (r, kb) in ((0, 0), (129, 7), (639, 39)):
+            blk = c[r * 40 + kb]                   # gate row r, k-block kb
+            chunk = ((r // 128) * 40 + kb) * 4608
+            np.testing.assert_array_equal(p[chunk + 16 * (r % 128): chunk + 16 * (r % 128) + 16], blk[2:])
+            np.testing.assert_array_equal(p[chunk + 4096 + 4 * (r % 128): chunk + 4096 + 4 * (r % 128) + 2], blk[:2])
+            blk = c[25600 + r * 40 + kb]           # up
+            np.testing.assert_array_equal(p[chunk + 2048 + 16 * (r % 128): chunk + 2048 + 16 * (r % 128) + 16], blk[2:])
+            np.testing.assert_array_equal(p[chunk + 4096 + 4 * (r % 128) + 2: chunk + 4096 + 4 * (r % 128) + 4], blk[:2])
+        for (nr, kb) in ((0, 0), (1000, 3), (2559, 9)):
+            blk = c[51200 + nr * 10 + kb]          # down row nr, k-block kb
+            chunk = 921600 + ((nr // 128) * 10 + kb) * 2304
+            np.testing.assert_array_equal(p[chunk + 16 * (nr % 128): chunk + 16 * (nr % 128) + 16], blk[2:])
+            np.testing.assert_array_equal(p[chunk + 2048 + 2 * (nr % 128): chunk + 2048 + 2 * (nr % 128) + 2], blk[:2])
+
+
+def test_pack_rejects_overlap_and_null(lib):
+    buf = np.zeros(2 * qre.BLOB_BYTES, dtype=np.uint8)
+    with pytest.raises(qre.StrataError):
+        qre.strata_pack_q2_0(buf, buf[1000:], 1)
+    assert lib.strata_pack_q2_0(None, buf.ctypes.data, 1) == -1
+    assert lib.strata_unpack_q2_0(buf.ctypes.data, None, 1) == -1
+
+
+def _rc(fn, *args):
+    return fn(*args)
+
+
+def test_host_argument_checks(lib):
+    """Every rejected call returns before touching the device (no GPU here)."""
+    A = 1 << 20  # fake, 256-aligned addresses: never dereferenced because the checks fail first
+    ws_big = qre.strata_moe_workspace_bytes(16)
+    # T out of range / null pointers / bad E
+    assert lib.strata_moe_route(A, -1, A, None, 512, A, A, None, A, ws_big, None) == -1
+    assert lib.strata_moe_route(A, 8193, A, None, 512, A, A, None, A, ws_big, None) == -1
+    assert lib.strata_moe_route(None, 4, A, None, 512, A, A, None, A, ws_big, None) == -1
+    assert lib.strata_moe_route(A, 4, A, None, 500, A, A, None, A, ws_big, None) == -1
+    assert lib.strata_moe_route(A, 4, A, None, 1024, A, A, None, A, ws_big, None) == -1
+    # misaligned x / ws
+    assert lib.strata_moe_route(A + 4, 4, A, None, 512, A, A, None, A, ws_big, None) == -2
+    assert lib.strata_moe_route(A, 4, A, None, 512, A, A, None, A + 16, ws_big, None) == -2
+    # workspace too small
+    assert lib.strata_moe_route(A, 16, A, None, 512, A, A, None, A, 4096, None) == -6
+    # experts struct checks
+    ex = qre.experts(A, 512, 1)
+    bad_off = qre.experts(A, 512, 3)
+    bad_stride = qre.experts(A, 512, 1, qre.BLOB_BYTES + 16)
+    bad_e = qre.experts(A, 100, 1)
+    bad_align = qre.experts(A + 128, 512, 1)
+    for e, want in ((bad_off, -1), (bad_stride, -2), (bad_e, -1), (bad_align, -2)):
+        assert lib.strata_moe_layer(ctypes.byref(e), A, None, A, 4, 0, A, None, None, A, ws_big, None) == want
+    assert lib.strata_moe_layer(ctypes.byref(ex), A, None, A, 4, 2, A, None, None, A, ws_big, None) == -1
+    assert lib.strata_moe_layer(None, A, None, A, 4, 0, A, None, None, A, ws_big, None) == -1
+    assert lib.strata_moe_combine(None, A, 4, None, A, None) == -1
+    assert lib.strata_moe_combine(A, A, 4, None, A + 8, None) == -2
+    assert lib.strata_moe_group(A, 4, 512, None, A, A, A, A, ws_big, None) == -1
+    assert lib.strata_moe_experts(ctypes.byref(ex), A, 9000, A, A, A, A, A, A, ws_big, None) == -1
+    assert lib.strata_moe_stack(None, A, None, 2, A, 4, None, None, A, ws_big, None) == -1
+    assert lib.strata_pack_q2_0_device(A, qre.BLOB_BYTES, A + 16, qre.BLOB_BYTES, 1, None) == -2
+    assert lib.strata_moe_workspace_init(A + 8, 4096, None) == -2
+    assert lib.strata_moe_workspace_init(A, 100, None) == -6
+    # empty calls are valid and enqueue nothing
+    assert lib.strata_moe_route(A, 0, A, None, 512, A, A, None, A, ws_big, None) == 0
+    assert lib.strata_moe_layer(ctypes.byref(ex), A, None, A, 0, 0, A, None, None, A, ws_big, None) == 0
+    assert lib.strata_moe_combine(A, A, 0, None, A, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(qre, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(qre, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        qre.lib()

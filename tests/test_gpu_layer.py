@@ -1,0 +1,115 @@
+"""GPU parity of strata_moe_layer (steps 1-5 through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import quantized_routed_expert_top10_gb300 as qre
+from gpu_common import (DEV, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
+                        workspace)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def layer0():
+    """Seed-0 layer-0 experts packed on the device, and the host blob cache for the oracle."""
+    blobs = device_packed_layer(0, 0)
+    yield blobs, BlobCache(0)
+    del blobs
+    torch.cuda.empty_cache()
+
+
+def parity(layer0, x, wr, bias, flags=0, q2_offset=1):
+    blobs, cache = layer0
+    out, ids, w = run_layer(blobs, wr, bias, x, flags, q2_offset)
+    ref_r = oracle.route(x, wr, bias, residual=bool(flags))
+    ties = check_routing(ids, ref_r["ids"], ref_r["logits"])
+    ref = oracle.moe_layer(x, wr, bias, cache.layer_list(0, ids), q2_offset=q2_offset, residual=bool(flags),
+                           ids_in=ids)
+    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=2e-6)
+    if flags:
+        check_close(out - x, ref["out"] - x.astype(np.float64), "moe part of residual layer")
+    else:
+        check_close(out, ref["out"], "layer output")
+    return ties
+
+
+@pytest.mark.parametrize("q2_offset", [1, 2])
+def test_config0_decode_one_token(layer0, q2_offset):
+    parity(layer0, gen.activations_fast(0, 1), gen.router_weights(0, 0), None, q2_offset=q2_offset)
+
+
+def test_config1_verify_window(layer0):
+    parity(layer0, gen.verify_window(0, 4), gen.router_weights(0, 0), None)
+
+
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 37, 300])
+def test_ragged_token_counts_with_zipf_bias(layer0, T):
+    parity(layer0, gen.activations_fast(11, T), gen.router_weights(0, 0), gen.zipf_bias(0, 0))
+
+
+@pytest.mark.parametrize("T", [1, 3, 20])
+def test_residual_rmsnorm_layer(layer0, T):
+    x = 3.0 * gen.activations_fast(5, T)
+    parity(layer0, x.astype(np.float32), gen.router_weights(0, 0), gen.zipf_bias(0, 0), flags=1)
+
+
+def test_every_token_on_the_same_ten_experts(layer0):
+    """Degenerate routing: 64 tokens all pick the same ten experts (groups of 64, several tiles)."""
+    bias = np.zeros(512, dtype=np.float32)
+    hot = [5, 17, 99, 130, 255, 256, 300, 411, 500, 511]
+    bias[hot] = 50.0
+    blobs, cache = layer0
+    x = gen.activations_fast(2, 64)
+    wr = gen.router_weights(0, 0)
+    out, ids, w = run_layer(blobs, wr, bias, x)
+    assert np.all(np.sort(ids, axis=1) == np.array(hot))
+    parity(layer0, x, wr, bias)
+
+
+@pytest.mark.parametrize("T", [1, 20])
+def test_equal_logits_pick_lowest_ids(layer0, T):
+    blobs, cache = layer0
+    wr = np.zeros((512, 2560), dtype=np.uint16)
+    x = gen.activations_fast(4, T)
+    out, ids, w = run_layer(blobs, wr, None, x)
+    assert np.all(ids == np.arange(10)) and np.all(w == np.float32(0.1))
+    ref = oracle.moe_layer(x, wr, None, cache.layer_list(0, ids), ids_in=ids)
+    check_close(out, ref["out"], "equal-logit layer")
+
+
+def test_empty_call_is_a_no_op(layer0):
+    blobs, _ = layer0
+    ws = workspace(1)
+    out = torch.full((1, qre.H), 7.0, device=DEV)
+    x = torch.zeros(1, qre.H, device=DEV)
+    wr = torch.zeros(512, qre.H, dtype=torch.int16, device=DEV)
+    qre.strata_moe_layer(qre.experts(blobs), wr, None, x, 0, 0, out, None, None, ws)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+def test_out_may_alias_x(layer0):
+    blobs, cache = layer0
+    T = 4
+    x = gen.activations_fast(9, T)
+    wr = gen.router_weights(0, 0)
+    ref_out, _, _ = run_layer(blobs, wr, None, x, flags=1)
+    xd = to_dev(x)
+    ws = workspace(T)
+    qre.strata_moe_layer(qre.experts(blobs), to_dev(wr), None, xd, T, 1, xd, None, None, ws)
+    assert qre.strata_poll_status(ws) == 0
+    np.testing.assert_array_equal(xd.cpu().numpy(), ref_out)
+
+
+def test_repeat_calls_are_deterministic(layer0):
+    blobs, _ = layer0
+    x = gen.activations_fast(6, 300)
+    wr = gen.router_weights(0, 0)
+    bias = gen.zipf_bias(0, 0)
+    a = run_layer(blobs, wr, bias, x)
+    b = run_layer(blobs, wr, bias, x)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
