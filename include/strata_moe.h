@@ -109,6 +109,27 @@ strata_status strata_moe_group(const int32_t* ids, int32_t T, int32_t n_expert, 
                                int32_t* pair, int32_t* active, int32_t* n_active, void* ws,
                                size_t ws_bytes, void* stream);
 
+/* Step 3 without a caller workspace (this entry point has no counterpart on the pages).
+ * Some callers cannot call cudaMalloc at all: code running inside an engine whose device memory
+ * belongs to its own pool or to another runtime, or a process that must not grow its device
+ * footprint after start-up.  This call takes the same inputs and writes the same outputs as
+ * strata_moe_group (bit for bit), but its scratch -- the per-chunk expert histograms and the tile
+ * list -- is a fixed array of STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES (256 KiB) in the library's own
+ * device memory, so it allocates nothing and takes no ws.
+ *   - The array is sized for the largest T the ABI allows; T outside [0, STRATA_MOE_T_MAX] returns
+ *     STRATA_E_INVAL.
+ *   - Every GPU that loads the library holds the array until the process exits.  The first call on
+ *     a device looks up the array's device address (with that device current) and caches it, so
+ *     make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (every word a call reads
+ *     it first writes, so nothing has to be cleared): calls whose GPU work overlaps -- other streams,
+ *     other host threads -- race on it; order them.
+ *   - There is no device status word: an id outside [0, E) drops its pair, which shows as
+ *     expert_off[E] < T*10. */
+#define STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES (256 * 1024)
+strata_status strata_moe_group_noalloc(const int32_t* ids, int32_t T, int32_t n_expert, int32_t* expert_off,
+                                       int32_t* pair, int32_t* active, int32_t* n_active, void* stream);
+
 /* Step 4. For every pair p = t*10 + k listed by the grouping: parts[p][:] = expert(x[t]) with the
  * expert that owns p.  x fp32 [T][2560]; grouping arrays as strata_moe_group writes them; parts
  * fp32 [T][10][2560].  Weights are the packed blobs of ex (host pointer to the struct). */

@@ -22,6 +22,7 @@ QK = 64
 BLOB_BYTES = 1382400
 T_MAX = 8192
 RESIDUAL_RMSNORM = 1
+GROUP_NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 STATUS = {
     0: "STRATA_OK",
@@ -37,6 +38,7 @@ STATUS = {
 # Every symbol include/strata_moe.h declares.
 EXPORTS = (
     "strata_moe_workspace_bytes", "strata_moe_workspace_init", "strata_moe_route", "strata_moe_group",
+    "strata_moe_group_noalloc",
     "strata_moe_experts", "strata_moe_combine", "strata_moe_layer", "strata_moe_stack",
     "strata_pack_q2_0", "strata_unpack_q2_0", "strata_pack_q2_0_device", "strata_poll_status",
     "strata_clear_status", "strata_status_str",
@@ -73,6 +75,7 @@ def lib():
             "strata_moe_workspace_init": (ctypes.c_int, [_vp, _sz, _vp]),
             "strata_moe_route": (ctypes.c_int, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
             "strata_moe_group": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+            "strata_moe_group_noalloc": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
             "strata_moe_experts": (ctypes.c_int, [ctypes.POINTER(strata_experts_t), _vp, _i32, _vp, _vp, _vp,
                                                   _vp, _vp, _vp, _sz, _vp]),
             "strata_moe_combine": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp]),
@@ -150,6 +153,12 @@ def strata_moe_route(x, T, w_router, bias, n_expert, ids, weights, logits, ws, w
 def strata_moe_group(ids, T, n_expert, expert_off, pair, active, n_active, ws, ws_bytes=None, stream=None):
     _check("strata_moe_group", lib().strata_moe_group(_p(ids), T, n_expert, _p(expert_off), _p(pair), _p(active),
                                                       _p(n_active), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def strata_moe_group_noalloc(ids, T, n_expert, expert_off, pair, active, n_active, stream=None):
+    """Grouping with the library's own fixed device scratch: for callers that cannot allocate."""
+    _check("strata_moe_group_noalloc", lib().strata_moe_group_noalloc(_p(ids), T, n_expert, _p(expert_off), _p(pair),
+                                                                      _p(active), _p(n_active), _s(stream)))
 
 
 def strata_moe_experts(ex, x, T, expert_off, pair, active, n_active, parts, ws, ws_bytes=None, stream=None):

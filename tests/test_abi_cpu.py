@@ -31,7 +31,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     assert sorted(names) == sorted(qre.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -124,6 +124,11 @@ def test_host_argument_checks(lib):
     assert lib.strata_moe_group(A, 4, 512, None, A, A, A, A, ws_big, None) == -1
     assert lib.strata_moe_experts(ctypes.byref(ex), A, 9000, A, A, A, A, A, A, ws_big, None) == -1
     assert lib.strata_moe_stack(None, A, None, 2, A, 4, None, None, A, ws_big, None) == -1
+    assert lib.strata_moe_group_noalloc(A, -1, 512, A, A, A, A, None) == -1
+    assert lib.strata_moe_group_noalloc(A, 8193, 512, A, A, A, A, None) == -1
+    assert lib.strata_moe_group_noalloc(A, 4, 512, A + 2, A, A, A, None) == -2
+    assert lib.strata_moe_group_noalloc(A, 4, 512, None, A, A, A, None) == -1
+    assert lib.strata_moe_group_noalloc(A, 0, 512, A, A, A, A, None) == 0
     assert lib.strata_pack_q2_0_device(A, qre.BLOB_BYTES, A + 16, qre.BLOB_BYTES, 1, None) == -2
     assert lib.strata_moe_workspace_init(A + 8, 4096, None) == -2
     assert lib.strata_moe_workspace_init(A, 100, None) == -6
