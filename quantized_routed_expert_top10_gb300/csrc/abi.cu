@@ -84,6 +84,10 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
   int32_t* ids_d = ids ? ids : (int32_t*)(w + L.ids);
   float* wts_d = weights ? weights : (float*)(w + L.weights);
   const int norm = (flags & STRATA_MOE_RESIDUAL_RMSNORM) ? 1 : 0;
+  if (T <= DECODE_T_MAX) {
+    STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, out, ids_d, wts_d, L, w, s));
+    return STRATA_OK;
+  }
   STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
   float* parts = (float*)(w + L.parts);
   STRATA_CUDA(launch_experts_gemv(*ex, T, (const int32_t*)(w + L.pair), L, w, parts, s));

@@ -59,10 +59,23 @@ struct __align__(16) Tile {
 // Workspace layout for a call with T tokens (byte offsets, each 256-aligned).  The first
 // WS_HEADER bytes (status word and counters) are the same for every T and are zeroed once by
 // strata_moe_workspace_init; kernels that use a counter reset it before they finish.
-constexpr size_t WS_HEADER = 4096;
+constexpr size_t WS_HEADER = 12288;
 constexpr size_t WS_STATUS = 0;     // int32 status word
 constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
 constexpr size_t WS_CNT_GU = 256;   // int32 [max_tiles(DECODE_T_MAX)][RT_GU] split counters
+// Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): grid barrier, exit
+// counter, per (expert slot, gate/up row tile) split counters, per expert slot h-ready counters,
+// per down row tile counters.
+constexpr size_t WS_SYNC = 4096;
+constexpr int WS_SYNC_BAR = 0;
+constexpr int WS_SYNC_EXIT = 1;
+constexpr int WS_SYNC_CNT_GU = 16;
+constexpr int WS_SYNC_HREADY = WS_SYNC_CNT_GU + DECODE_T_MAX * K * RT_GU;
+constexpr int WS_SYNC_CNT_DN = WS_SYNC_HREADY + DECODE_T_MAX * K;
+constexpr int WS_SYNC_REL = ((WS_SYNC_CNT_DN + RT_D + 31) / 32) * 32;  // barrier release flags, one per 128-B line
+constexpr int WS_NREP = 16;                          // replicas of data every CTA reads at once
+constexpr int WS_SYNC_WORDS = WS_SYNC_REL + 32 * WS_NREP;
+static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sync words must fit the header");
 
 struct WsLayout {
   size_t status, cnt_route, cnt_gu;
@@ -70,6 +83,8 @@ struct WsLayout {
   size_t ids;         // int32 [T][K]
   size_t weights;     // fp32 [T][K]
   size_t xn;          // fp32 [T][H] normalised input (residual layers, T > DECODE_T_MAX)
+  size_t sumsq;       // fp32 [WS_NREP][T][KB_GU] per-block sums of squares, replicated (one-kernel decode layer)
+  size_t dots_rep;    // fp32 [WS_NREP][T][EMAX] replicated router dot products (one-kernel decode layer)
   size_t expert_off;  // int32 [EMAX + 1]
   size_t pair;        // int32 [T*K]
   size_t active;      // int32 [EMAX]
@@ -110,6 +125,8 @@ inline WsLayout ws_layout(int T) {
   L.ids = take(sizeof(int32_t) * (size_t)P);
   L.weights = take(sizeof(float) * (size_t)P);
   L.xn = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);
+  L.sumsq = take(sizeof(float) * (size_t)WS_NREP * T * KB_GU);
+  L.dots_rep = take(sizeof(float) * (size_t)WS_NREP * (T < DECODE_T_MAX ? T : DECODE_T_MAX) * EMAX);
   L.expert_off = take(sizeof(int32_t) * (EMAX + 1));
   L.pair = take(sizeof(int32_t) * (size_t)P);
   L.active = take(sizeof(int32_t) * EMAX);
@@ -244,6 +261,9 @@ cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t
                                 char* ws, float* parts, cudaStream_t s);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
+cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
+                                const float* x, int T, int residual, float* out, int32_t* ids, float* weights,
+                                const WsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_pack_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed,
                                int64_t dst_stride, int64_t n_blobs, cudaStream_t s);
 }  // namespace strata

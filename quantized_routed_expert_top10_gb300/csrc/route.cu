@@ -5,126 +5,26 @@
 // descending argsort, gathers the first 10 and renormalises with ggml's lower clamp.
 // momoyeyu.github.io "ai-infra-strata", section "提示词处理": tokens are gathered per expert so a
 // single read of an expert's weights serves every token routed to it.
-#include "common.cuh"
+#include "device_common.cuh"
 
 namespace strata {
 namespace {
 
-constexpr float kRenormFloor = 6.103515625e-05f;  // 2^-14
-
-// ---------------------------------------------------------------------------------------------
-// top-k of one token's logits by one warp: softmax over E (E % 32 == 0, E <= 512), the K
-// largest probabilities in descending order (lower id first on equal values), renormalised.
-// ---------------------------------------------------------------------------------------------
+// top-k of one token's logits (global memory written by other CTAs or kernels) by one warp.
 __device__ void top_k_warp(const float* logits, int E, int32_t* ids, float* weights) {
+  int id;
+  float w;
+  top_k_warp_fn([&](int e) { return __ldcg(logits + e); }, E, &id, &w);
   const int lane = threadIdx.x & 31;
-  const int per = E >> 5;
-  float l[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) l[j] = (j < per) ? __ldcg(logits + lane + 32 * j) : -INFINITY;
-  float m = l[0];
-#pragma unroll
-  for (int j = 1; j < 16; ++j) m = fmaxf(m, l[j]);
-  m = warp_max(m);
-  float p[16];
-  float z = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    p[j] = (j < per) ? expf(l[j] - m) : 0.f;
-    z += p[j];
-  }
-  z = warp_sum(z);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) p[j] = (j < per) ? p[j] / z : -1.f;
-  uint32_t taken = 0;
-  float sel_p[K];
-  int sel_id[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    float bv = -2.f;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (!((taken >> j) & 1u) && p[j] > bv) {  // ids grow with j: first max is the lowest id
-        bv = p[j];
-        bid = lane + 32 * j;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    sel_p[k] = bv;
-    sel_id[k] = bid;
-  }
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < K; ++k) s += sel_p[k];
-  const float denom = fmaxf(s, kRenormFloor);
   if (lane < K) {
-    float pk = sel_p[0];
-    int ik = sel_id[0];
-#pragma unroll
-    for (int k = 1; k < K; ++k)
-      if (lane == k) { pk = sel_p[k]; ik = sel_id[k]; }
-    ids[lane] = ik;
-    weights[lane] = pk / denom;
+    ids[lane] = id;
+    weights[lane] = w;
   }
 }
 
 // ---------------------------------------------------------------------------------------------
 // Grouping: counting sort of pair numbers p = t*K + k by expert (stable), active experts, tiles.
 // ---------------------------------------------------------------------------------------------
-
-// Exclusive scan of cnt[0..E) in shared memory by a whole CTA of 128..1024 threads; returns the
-// total; out may alias cnt.  scratch: >= 32 ints.
-__device__ int cta_exclusive_scan(const int* cnt, int* out, int E, int* scratch) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int per = (E + nt - 1) / nt;
-  const int b0 = tid * per;
-  int local = 0;
-  for (int i = 0; i < per; ++i)
-    if (b0 + i < E) local += cnt[b0 + i];
-  // warp-level inclusive scan of the per-thread sums
-  const int lane = tid & 31, warp = tid >> 5;
-  int v = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) scratch[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = nt >> 5;
-    int w = (lane < nw) ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += n;
-    }
-    if (lane < nw) scratch[lane] = w;  // inclusive over warps
-  }
-  __syncthreads();
-  const int total = scratch[(nt >> 5) - 1];
-  int run = v - local + (warp ? scratch[warp - 1] : 0);
-  __syncthreads();
-  for (int i = 0; i < per; ++i) {
-    if (b0 + i < E) {
-      const int c = cnt[b0 + i];
-      out[b0 + i] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
-  return total;
-}
 
 // From per-expert counts (shared) build expert_off, active, n_active and the tile list.
 // Whole CTA; cnt is shared [E]; sh_off, sh_tile shared [E]; scratch shared [>= 32].
@@ -164,27 +64,6 @@ __device__ void finish_grouping(const int* cnt, int E, int* sh_off, int* sh_tile
   if (tid == 0) {
     n_active_tiles[0] = na;
     n_active_tiles[1] = ntiles < max_tiles ? ntiles : max_tiles;
-  }
-}
-
-// Stable scatter of pairs [p0, p1) by one warp: fill[e] (shared) holds the next slot of expert e.
-__device__ void stable_scatter_warp(const int32_t* ids, int p0, int p1, int E, int* fill, int32_t* pair) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int base = p0; base < p1; base += 32) {
-    const int p = base + lane;
-    int e = (p < p1) ? ids[p] : -1;
-    if (e >= E || e < 0) e = -1;
-    const uint32_t same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & lt);
-    int pos = 0;
-    if (e >= 0) pos = fill[e] + rank;
-    __syncwarp();
-    if (e >= 0) {
-      pair[pos] = p;
-      if ((same >> lane) == 1u) fill[e] += __popc(same);  // highest lane of the group
-    }
-    __syncwarp();
   }
 }
 

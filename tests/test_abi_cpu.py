@@ -47,7 +47,7 @@ def test_workspace_sizes(lib):
     assert qre.strata_moe_workspace_bytes(-1) == 0
     assert qre.strata_moe_workspace_bytes(8193) == 0
     sizes = [qre.strata_moe_workspace_bytes(t) for t in (0, 1, 4, 8, 9, 2048, 8192)]
-    assert sizes[0] == 4096
+    assert sizes[0] == 12288
     assert all(b > a for a, b in zip(sizes, sizes[1:]))
     assert all(s % 256 == 0 for s in sizes)
 
