@@ -60,11 +60,10 @@ strata_status route_and_group(const float* x, int T, int norm, const uint16_t* w
     xin = (const float*)(ws + L.xn);
   }
   float* logits = logits_user ? logits_user : (float*)(ws + L.logits);
-  STRATA_CUDA(launch_router_logits(xin, T, w_router, bias, E, logits, s));
+  STRATA_CUDA(launch_router_tc(xin, T, w_router, bias, E, logits, (int*)(ws + L.status), s));
   STRATA_CUDA(launch_top_k(logits, T, E, ids, weights, s));
   STRATA_CUDA(launch_group(ids, T, E, (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair),
                            (int32_t*)(ws + L.active), nullptr, L, ws, s));
-  STRATA_CUDA(launch_quantise_x(xin, T, q2_offset, (QBlock*)(ws + L.qx), s));
   return STRATA_OK;
 }
 
@@ -90,7 +89,11 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
   }
   STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
   float* parts = (float*)(w + L.parts);
-  STRATA_CUDA(launch_experts_gemv(*ex, T, (const int32_t*)(w + L.pair), L, w, parts, s));
+  const float* xin = norm ? (const float*)(w + L.xn) : x;
+  STRATA_CUDA(launch_experts_tc(*ex, xin, T, (const int32_t*)(w + L.expert_off), (const int32_t*)(w + L.pair),
+                                (const int32_t*)(w + L.active), (const int32_t*)(w + L.n_active), parts,
+                                (uint8_t*)(w + L.xg), (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta),
+                                (int*)(w + L.status), s));
   STRATA_CUDA(launch_combine(parts, wts_d, T, norm ? x : nullptr, out, s));
   return STRATA_OK;
 }
@@ -130,7 +133,7 @@ strata_status strata_moe_route(const float* x, int32_t T, const uint16_t* w_rout
     return STRATA_OK;
   }
   float* lg = logits ? logits : (float*)(w + L.logits);
-  STRATA_CUDA(launch_router_logits(x, T, w_router, bias, n_expert, lg, s));
+  STRATA_CUDA(launch_router_tc(x, T, w_router, bias, n_expert, lg, (int*)(w + L.status), s));
   STRATA_CUDA(launch_top_k(lg, T, n_expert, ids, weights, s));
   return STRATA_OK;
 }
@@ -163,6 +166,11 @@ strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int
   const WsLayout L = ws_layout(T);
   char* w = (char*)ws;
   cudaStream_t s = (cudaStream_t)stream;
+  if (T > DECODE_T_MAX) {
+    STRATA_CUDA(launch_experts_tc(*ex, x, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
+                                  (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
+    return STRATA_OK;
+  }
   STRATA_CUDA(launch_build_tiles(expert_off, active, n_active, ex->n_expert, T, L, w, s));
   STRATA_CUDA(launch_quantise_x(x, T, ex->q2_offset, (QBlock*)(w + L.qx), s));
   STRATA_CUDA(launch_experts_gemv(*ex, T, pair, L, w, parts, s));

@@ -95,6 +95,9 @@ struct WsLayout {
   size_t partial;     // fp32 [max_tiles][RT_GU][S_SPLIT][NT][RT][2] (decode split-K partials)
   size_t hq;          // QBlock [T*K][KB_D]
   size_t parts;       // fp32 [T*K][H]
+  size_t xg;          // tensor-core path (T > DECODE_T_MAX): gathered fp16 tokens [KB_GU][rows][128 B]
+  size_t hg;          //                                      fp16 h [KB_D][rows][128 B]
+  size_t tcmeta;      //                                      expert ranges, tiles, counts
   size_t total;
   int max_tiles;
   int n_chunks;
@@ -109,6 +112,12 @@ inline int max_tiles_for(int T) {
   const int P = T * K;
   return P / NT + (P < EMAX ? P : EMAX);
 }
+
+// Sizes of the tensor-core path's buffers (experts_tc.cu).
+int64_t tc_rows_cap(int T);
+size_t tc_xg_bytes(int T);
+size_t tc_hg_bytes(int T);
+size_t tc_meta_bytes(int T);
 
 inline WsLayout ws_layout(int T) {
   WsLayout L{};
@@ -139,6 +148,9 @@ inline WsLayout ws_layout(int T) {
   L.partial = take(sizeof(float) * (size_t)max_tiles_for(Td) * RT_GU * S_SPLIT * NT * RT * 2);
   L.hq = take(sizeof(QBlock) * (size_t)P * KB_D);
   L.parts = take(sizeof(float) * (size_t)P * H);
+  L.xg = take(T > DECODE_T_MAX ? tc_xg_bytes(T) : 0);
+  L.hg = take(T > DECODE_T_MAX ? tc_hg_bytes(T) : 0);
+  L.tcmeta = take(T > DECODE_T_MAX ? tc_meta_bytes(T) : 0);
   L.total = T > 0 ? o : WS_HEADER;
   return L;
 }
@@ -249,8 +261,8 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
                                 const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
                                 float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s);
-cudaError_t launch_router_logits(const float* x, int T, const uint16_t* w_router, const float* bias,
-                                 int E, float* logits, cudaStream_t s);
+cudaError_t launch_router_tc(const float* x, int T, const uint16_t* w_router, const float* bias, int E,
+                             float* logits, int* status, cudaStream_t s);
 cudaError_t launch_top_k(const float* logits, int T, int E, int32_t* ids, float* weights, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair,
                          int32_t* active, int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s);
@@ -259,6 +271,9 @@ cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active,
 cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s);
 cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t* pair, const WsLayout& L,
                                 char* ws, float* parts, cudaStream_t s);
+cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, int T, const int32_t* expert_off,
+                              const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
+                              uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,

@@ -249,19 +249,14 @@ cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t
   QBlock* hq = (QBlock*)(ws + L.hq);
   int* status = (int*)(ws + L.status);
   const int max_tiles = L.max_tiles;
-  if (T <= DECODE_T_MAX) {
-    constexpr int S = S_SPLIT;
-    const size_t smem = NSTAGE * GU_CHUNK + sizeof(QBlock) * (KB_GU / S) * NT;
-    cudaFuncSetAttribute(gateup_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gateup_kernel<S><<<max_tiles * RT_GU * S, 128, smem, s>>>(blobs, ex.blob_stride, tiles, nat, pair, qx,
-                                                             (float*)(ws + L.partial), (int*)(ws + L.cnt_gu),
-                                                             hq, ex.q2_offset, status);
-  } else {
-    const size_t smem = NSTAGE * GU_CHUNK + sizeof(QBlock) * KB_GU * NT;
-    cudaFuncSetAttribute(gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gateup_kernel<1><<<max_tiles * RT_GU, 128, smem, s>>>(blobs, ex.blob_stride, tiles, nat, pair, qx, nullptr,
-                                                         (int*)(ws + L.cnt_gu), hq, ex.q2_offset, status);
-  }
+  // decode-sized calls only (T <= DECODE_T_MAX); larger calls take the tensor-core path
+  (void)T;
+  constexpr int S = S_SPLIT;
+  const size_t smem = NSTAGE * GU_CHUNK + sizeof(QBlock) * (KB_GU / S) * NT;
+  cudaFuncSetAttribute(gateup_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  gateup_kernel<S><<<max_tiles * RT_GU * S, 128, smem, s>>>(blobs, ex.blob_stride, tiles, nat, pair, qx,
+                                                           (float*)(ws + L.partial), (int*)(ws + L.cnt_gu), hq,
+                                                           ex.q2_offset, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   down_kernel<<<max_tiles * RT_D, 128, 0, s>>>(blobs, ex.blob_stride, tiles, nat, pair, hq, parts, status);

@@ -206,53 +206,6 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   for (int h = threadIdx.x; h < H; h += 256) xn[(size_t)t * H + h] = xr[h] * inv;
 }
 
-// logits[t][e] = sum_h x[t][h] * W[e][h] + bias[e], fp32 FFMA GEMM: 64 tokens x 64 experts per
-// CTA, 256 threads with 4 x 4 outputs each, k-steps of 32.
-__global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restrict__ x, int T,
-                                                          const uint16_t* __restrict__ wr,
-                                                          const float* __restrict__ bias, int E,
-                                                          float* __restrict__ logits, int ld_logits) {
-  __shared__ float sx[32][64 + 4];
-  __shared__ float sw[32][64 + 4];
-  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
-  const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;  // outputs rows t0 + ty*4 .., cols e0 + tx*4 ..
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += 32) {
-    // load 64 x 32 of x and of W (transposed into [k][row])
-    for (int i = tid; i < 64 * 32; i += 256) {
-      const int r = i >> 5, k = i & 31;
-      const int t = t0 + r;
-      sx[k][r] = (t < T) ? x[(size_t)t * H + k0 + k] : 0.f;
-      const int e = e0 + r;
-      sw[k][r] = (e < E) ? __uint_as_float((uint32_t)wr[(size_t)e * H + k0 + k] << 16) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&sx[k][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&sw[k][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) logits[(size_t)t * ld_logits + e] = acc[i][j] + (bias ? bias[e] : 0.f);
-    }
-  }
-}
-
 __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ logits, int ld, int T, int E,
                                                     int32_t* __restrict__ ids, float* __restrict__ weights) {
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -386,13 +339,6 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
 
 cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s) {
   rmsnorm_kernel<<<T, 256, 0, s>>>(x, xn);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_router_logits(const float* x, int T, const uint16_t* w_router, const float* bias, int E,
-                                 float* logits, cudaStream_t s) {
-  dim3 grid((T + 63) / 64, (E + 63) / 64);
-  router_gemm_kernel<<<grid, 256, 0, s>>>(x, T, w_router, bias, E, logits, E);
   return cudaGetLastError();
 }
 

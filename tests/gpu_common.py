@@ -18,6 +18,13 @@ import quantized_routed_expert_top10_gb300 as qre
 
 TIE = 1e-4
 REL_TOL = 2e-3
+# Renormalised routing weights: the prefill router runs on the tensor cores (bf16 hi/lo split of x,
+# fp32 accumulation in the tensor core's datapath), whose logits differ from the fp64 oracle by ~1e-5
+# -- ten times inside the 1e-4 tie band -- so weights agree to ~5e-6; the decode GEMV path is closer.
+W_TOL = 1e-5
+# Router logits of the prefill path: the tensor core's accumulation over the 2,560-term dot products
+# leaves up to ~3e-5 (measured), below the 1e-4 band that decides the routing.
+LOGIT_TOL = 5e-5
 DEV = torch.device("cuda:0")
 B = qre.BLOB_BYTES
 

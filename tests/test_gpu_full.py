@@ -13,7 +13,7 @@ import torch
 import gen
 import oracle
 import quantized_routed_expert_top10_gb300 as qre
-from gpu_common import (DEV, B, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
+from gpu_common import (W_TOL, DEV, B, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
                         workspace)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -93,7 +93,7 @@ def test_config3_prefill_2048(arena):
     cache = BlobCache(0)
     ref = oracle.moe_layer(x[sample], wr, bias, cache.layer_list(0, ids[sample]), ids_in=ids[sample])
     check_close(out[sample], ref["out"], "config 3 sampled outputs")
-    np.testing.assert_allclose(w[sample], ref["w"], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(w[sample], ref["w"], rtol=0, atol=W_TOL)
 
 
 def test_config4_prefill_8192_stack_sampled(arena):

@@ -6,7 +6,7 @@ import torch
 import gen
 import oracle
 import quantized_routed_expert_top10_gb300 as qre
-from gpu_common import (DEV, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
+from gpu_common import (W_TOL, DEV, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
                         workspace)
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +28,7 @@ def parity(layer0, x, wr, bias, flags=0, q2_offset=1):
     ties = check_routing(ids, ref_r["ids"], ref_r["logits"])
     ref = oracle.moe_layer(x, wr, bias, cache.layer_list(0, ids), q2_offset=q2_offset, residual=bool(flags),
                            ids_in=ids)
-    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=W_TOL)
     if flags:
         check_close(out - x, ref["out"] - x.astype(np.float64), "moe part of residual layer")
     else:

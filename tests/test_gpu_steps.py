@@ -7,7 +7,7 @@ import torch
 import gen
 import oracle
 import quantized_routed_expert_top10_gb300 as qre
-from gpu_common import (DEV, B, BlobCache, check_close, check_routing, device_canonical, device_packed_layer,
+from gpu_common import (W_TOL, LOGIT_TOL, DEV, B, BlobCache, check_close, check_routing, device_canonical, device_packed_layer,
                         host_packed, to_dev, workspace)
 
 pytestmark = pytest.mark.gpu
@@ -40,11 +40,12 @@ def test_route_step(T):
     qre.strata_moe_route(to_dev(x), T, to_dev(wr), None if bias is None else to_dev(bias), 512, ids, w, logits, ws)
     assert qre.strata_poll_status(ws) == 0
     ref = oracle.route(x, wr, bias)
-    np.testing.assert_allclose(logits.cpu().numpy(), ref["logits"], rtol=0, atol=2e-5)
+    # decode GEMV: fp32 FFMA; prefill: tensor-core GEMM with bf16 hi/lo parts of x (see gpu_common)
+    np.testing.assert_allclose(logits.cpu().numpy(), ref["logits"], rtol=0, atol=2e-5 if T <= 8 else LOGIT_TOL)
     ids_h = ids.cpu().numpy()
     check_routing(ids_h, ref["ids"], ref["logits"])
     wref = np.stack([oracle.weights_for_ids(ref["logits"][t], ids_h[t]) for t in range(T)])
-    np.testing.assert_allclose(w.cpu().numpy(), wref, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(w.cpu().numpy(), wref, rtol=0, atol=W_TOL)
 
 
 @pytest.mark.parametrize("E", [32, 256])
