@@ -143,23 +143,48 @@ def setup_device(cfg_id, seed, dev):
     return cfg, arena, wr, bias, exs, x_host
 
 
-def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws):
+def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws):
     """One pass of the whole hot path over the batch (x_in is never modified)."""
     T, L = cfg["T"], cfg["L"]
     if L == 1:
         qre.strata_moe_layer(exs[0], wr[0], None if bias is None else bias[0], x_in, T, 0, out, ids, None, ws)
         return out
     x_work.copy_(x_in)
-    qre.strata_moe_stack(exs, wr, bias, L, x_work, T, None, None, ws)
+    qre.strata_moe_stack(exs, wr, bias, L, x_work, T, ids_all, None, ws)
     return x_work
 
 
-def launches_per_step(T, L):
-    # T <= 8: one kernel per layer (decode_layer_kernel); else rmsnorm (stacks) + router GEMM + top-k +
-    # 3 grouping kernels + quantise + gate/up + down + combine.
-    if T <= 8:
-        return L
-    return (8 + (1 if L > 1 else 0)) * L
+# Kernels timed with the library's own event hooks inside the timed region: the whole decode layer for
+# T <= 8; for prefill every kernel of the step (the dominant one is picked by total time).
+PREFILL_KERNELS = ("RMSNORM", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN", "GROUP_SCATTER", "TC_PREPARE",
+                   "TC_GATHER", "TC_GATEUP", "TC_DOWN", "COMBINE")
+FLOPS_PER_PAIR = {"TC_GATEUP": 2 * 2 * 2560 * 640, "TC_DOWN": 2 * 640 * 2560}
+CSRC = os.path.join(ROOT, "quantized_routed_expert_top10_gb300", "csrc")
+KERNEL_SOURCES = {
+    "DECODE_LAYER": ("decode_fused.cu", "common.cuh", "device_common.cuh"),
+    "TC_GATEUP": ("experts_tc.cu", "tc_common.cuh", "common.cuh", "device_common.cuh"),
+    "TC_DOWN": ("experts_tc.cu", "tc_common.cuh", "common.cuh", "device_common.cuh"),
+}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture of the
+# workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
+# sources at capture time: once a source changes the figure no longer describes the kernel (null).
+NCU_TRAFFIC = {}
+
+
+def source_digest(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, ()):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None or rec[1] != source_digest(kernel):
+        return None
+    return rec[0]
 
 
 def measure_gb300(args, rank, world, local_rank):
@@ -180,6 +205,7 @@ def measure_gb300(args, rank, world, local_rank):
     x_work = torch.empty_like(x_in)
     out = torch.empty_like(x_in)
     ids = torch.empty(T, 10, dtype=torch.int32, device=dev)
+    ids_all = torch.empty(L, T, 10, dtype=torch.int32, device=dev) if L > 1 else None
     ws_bytes = qre.strata_moe_workspace_bytes(T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     qre.strata_moe_workspace_init(ws)
@@ -188,7 +214,7 @@ def measure_gb300(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     for _ in range(W):
-        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws)
+        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
     torch.cuda.synchronize()
     st = qre.strata_poll_status(ws)
     if st != 0:
@@ -196,6 +222,20 @@ def measure_gb300(args, rank, world, local_rank):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # Dominant-kernel timing inside the timed region: T <= 8 and one layer -> the step is exactly one
+    # launch of the decode layer kernel (its events are the step's); T <= 8 stacks -> one layer per
+    # step, rotating over the layers (every launch would add event records between the 48 launches);
+    # prefill -> every launch of the two tensor-core expert kernels.
+    timed = () if T <= 8 and L == 1 else ("DECODE_LAYER",) if T <= 8 else ("TC_GATEUP", "TC_DOWN")
+    per_step = 1 if T <= 8 else L
+    kev = {}
+    for k in timed:
+        kev[k] = ([torch.cuda.Event(enable_timing=True) for _ in range(K * per_step)],
+                  [torch.cuda.Event(enable_timing=True) for _ in range(K * per_step)])
+        for e in kev[k][0] + kev[k][1]:
+            e.record(stream)  # creates the CUDA event behind the torch object
+    torch.cuda.synchronize()
+    armed = {}
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -203,14 +243,28 @@ def measure_gb300(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.25)
     wall0 = time.perf_counter()
+    launches0 = qre.strata_moe_launch_count()
     for i in range(K):
         if need_flush:
             flush.fill_(i & 0xFF)
+        for k in timed:
+            if T <= 8:  # layer i % L of this step
+                armed[k] = qre.strata_moe_profile_arm(k, kev[k][0][i:i + 1], kev[k][1][i:i + 1], skip=i % L)
+            elif i == 0:
+                armed[k] = qre.strata_moe_profile_arm(k, *kev[k])
         starts[i].record(stream)
-        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ws)
+        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    n_launches = qre.strata_moe_launch_count() - launches0
+    kernel_ms = {}
+    for k in timed:
+        kernel_ms[k] = [a.elapsed_time(b) for a, b in zip(*kev[k])]
+        qre.strata_moe_profile_arm(k, [], [])
+    del armed
+    if T <= 8 and L == 1:
+        kernel_ms["DECODE_LAYER"] = step_ms_list(starts, ends)
     if wall < 1.0:
         time.sleep(0.3)
     clk = clocks.stop()
@@ -225,14 +279,14 @@ def measure_gb300(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
     ids_h = ids.cpu().numpy()
+    ids_all_h = ids_all.cpu().numpy() if L > 1 else None
     value = world * T * K / (total_ms / 1e3)
 
     # ---- dominant kernel ----
-    if T <= 8 and L == 1:
-        # the step is one launch of decode_layer_kernel: its duration is the step's event time
-        roof = layer_kernel_roofline(step_ms, len(np.unique(ids_h)))
-    else:
-        roof = expert_roofline(qre, cfg, exs, x_in, ids, ws, stream, flush if need_flush else None, T, dev)
+    roof = kernel_roofline(cfg, kernel_ms, K, ids_all_h if L > 1 else ids_h[None])
+    if T > 8:
+        roof["kernel_ms_per_step"] = step_breakdown(qre, run_step, (qre, cfg, exs, wr, bias, x_in, x_work, out, ids,
+                                                                   ids_all, ws), stream, L)
 
     # ---- end to end through the public API with host buffers ----
     e2e = measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush if need_flush else None, dev,
@@ -249,77 +303,115 @@ def measure_gb300(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "q2_0 weights x int16-split activations (dp4a), fp32 accumulate",
+        "dtype": path_dtype(T),
         "data": "synthetic (seeded Philox4x32-10 inputs; random Q2_0 experts; no trained weights)",
-        "config": {
-            "workload": cfg["name"],
-            "tokens": T,
-            "layers": L,
-            "experts": E,
-            "top_k": 10,
-            "hidden": 2560,
-            "ffn": 640,
-            "q2_offset": 1,
-            "seed": args.seed,
-            "l2": "256 MB buffer written between timed steps (flush excluded)" if need_flush
-            else "working set larger than L2 (no flush)",
-            "distinct_experts_last_step": int(len(np.unique(ids_h))) if L == 1 else None,
-            "parallelism": f"replicas x{world}",
-        },
+        "config": workload_config(cfg, args.seed, world, need_flush,
+                                  int(len(np.unique(ids_h))) if L == 1 else None),
         "roofline": roof,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(T, L) * K,
+        "gpu_launches": n_launches,
     }
     return result, cfg, ids_h
 
 
-def layer_kernel_roofline(step_ms, D):
-    """decode_layer_kernel: algorithmic bytes = router rows (E x H bf16) + D distinct experts x blob."""
-    hbm, _, _, how = load_peaks()
-    avg_ms = float(np.mean(step_ms))
-    bytes_alg = ROUTER_BYTES + D * BLOB
-    achieved = bytes_alg / (avg_ms / 1e3) / 1e9
-    return {"kernel": "decode_layer_kernel (router + top-10 + grouping + Q2_0 experts + combine)",
-            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": None, "bytes_per_launch": bytes_alg, "distinct_experts": D, "avg_launch_ms": avg_ms,
-            "peak_source": f"{how} (MEASURED_PEAKS.json hbm_gbs)" if how == "measured" else "fallback 6.8 TB/s"}
+def step_ms_list(starts, ends):
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
-def expert_roofline(qre, cfg, exs, x_in, ids, ws, stream, flush, T, dev):
-    """Average duration of strata_moe_experts (the Q2_0 gate/up and down kernels plus the tile builder
-    and activation quantiser) against its algorithmic bytes: distinct experts x 1,382,400 B."""
+def step_breakdown(qre, fn, args, stream, L, steps=2):
+    """Per-kernel device time of a step (ms), from a separate untimed pass with every prefill kernel's
+    launches bracketed by events (the extra event records are kept out of the timed region)."""
     import torch
-    if cfg["L"] != 1:
+    evs, armed = {}, {}
+    for k in PREFILL_KERNELS:
+        evs[k] = ([torch.cuda.Event(enable_timing=True) for _ in range(steps * L)],
+                  [torch.cuda.Event(enable_timing=True) for _ in range(steps * L)])
+        for e in evs[k][0] + evs[k][1]:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for k in PREFILL_KERNELS:
+        armed[k] = qre.strata_moe_profile_arm(k, *evs[k])
+    for _ in range(steps):
+        fn(*args)
+    torch.cuda.synchronize()
+    out = {}
+    for k in PREFILL_KERNELS:
+        n = qre.strata_moe_profile_recorded(k)
+        if n:
+            out[k] = round(sum(a.elapsed_time(b) for a, b in zip(evs[k][0][:n], evs[k][1][:n])) / steps, 5)
+        qre.strata_moe_profile_arm(k, [], [])
+    del armed
+    return dict(sorted(out.items(), key=lambda kv: -kv[1]))
+
+
+def path_dtype(T):
+    """Arithmetic of the path: decode = dp4a on 2-bit codes x int16-split activations (int32 partial
+    sums, fp32 accumulation); prefill = fp16 x fp16 tensor-core products with fp32 accumulation."""
+    return "s8 dp4a (q2 x int16-split x), fp32 acc" if T <= 8 else "f16 tcgen05, fp32 acc"
+
+
+def workload_config(cfg, seed, world, need_flush, distinct):
+    return {
+        "workload": cfg["name"],
+        "tokens": cfg["T"],
+        "layers": cfg["L"],
+        "experts": E,
+        "top_k": 10,
+        "hidden": 2560,
+        "ffn": 640,
+        "q2_offset": 1,
+        "seed": seed,
+        "l2": "256 MB buffer written between timed steps (flush excluded)" if need_flush
+        else "working set larger than L2 (no flush)",
+        "distinct_experts_last_step": distinct,
+        "parallelism": f"replicas x{world}",
+    }
+
+
+def kernel_roofline(cfg, kernel_ms, K, ids_layers):
+    """Roofline of the dominant kernel from the per-launch event times taken in the timed region.
+
+    decode layer (T <= 8): HBM-bound; algorithmic bytes per launch = router rows (512 x 2560 bf16) +
+      D distinct experts x 1,382,400 B, D from that layer's ids.
+    prefill (T > 8): tensor-bound; algorithmic flops per launch = T*10 pairs x 6,553,600 (gate/up:
+      two 640 x 2560 products) or x 3,276,800 (down: 2560 x 640).  fp16 operands run at the bf16 rate,
+      so the peak is the measured bf16 figure: burst for a single layer, sustained for 48-layer stacks.
+    """
+    hbm, tc_burst, tc_sust, how = load_peaks()
+    T, L = cfg["T"], cfg["L"]
+    totals = {k: float(np.sum(v)) for k, v in kernel_ms.items() if v}
+    if not totals:
         return None
-    hbm, _, _, how = load_peaks()
-    off = torch.empty(513, dtype=torch.int32, device=dev)
-    pair = torch.empty(T * 10, dtype=torch.int32, device=dev)
-    active = torch.empty(512, dtype=torch.int32, device=dev)
-    na = torch.empty(1, dtype=torch.int32, device=dev)
-    parts = torch.empty(T * 10 * 2560, dtype=torch.float32, device=dev)
-    qre.strata_moe_group(ids, T, 512, off, pair, active, na, ws)
-    torch.cuda.synchronize()
-    D = int(na.item())
-    n = 200 if T <= 8 else 20
-    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    for i in range(3):
-        qre.strata_moe_experts(exs[0], x_in, T, off, pair, active, na, parts, ws)
-    for i in range(n):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
-        s_ev[i].record(stream)
-        qre.strata_moe_experts(exs[0], x_in, T, off, pair, active, na, parts, ws)
-        e_ev[i].record(stream)
-    torch.cuda.synchronize()
-    avg_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]))
-    bytes_alg = D * BLOB
-    achieved = bytes_alg / (avg_ms / 1e3) / 1e9
-    return {"kernel": "strata_moe_experts (q2 gate/up + down)", "bound": "hbm", "achieved": achieved,
-            "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
-            "bytes_per_launch": bytes_alg, "distinct_experts": D, "avg_launch_ms": avg_ms,
-            "peak_source": f"{how} (MEASURED_PEAKS.json hbm_gbs)" if how == "measured" else "fallback 6.8 TB/s"}
+    dom = max(totals, key=totals.get)
+    ms = kernel_ms[dom]
+    avg_ms = float(np.mean(ms))
+    src = f"{how} (MEASURED_PEAKS.json)" if how == "measured" else "fallback"
+    if dom == "DECODE_LAYER":
+        d = [len(np.unique(ids_layers[l])) for l in range(ids_layers.shape[0])]
+        per_launch = ROUTER_BYTES + float(np.mean(d)) * BLOB
+        achieved = per_launch / (avg_ms / 1e3) / 1e9
+        return {"kernel": "decode_layer_kernel (router + top-10 + grouping + Q2_0 experts + combine)",
+                "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "frac_of": f"hbm_gbs, {src}", "traffic": ncu_traffic(cfg["name"], dom),
+                "algorithmic_bytes_per_launch": per_launch, "distinct_experts_per_layer": float(np.mean(d)),
+                "avg_launch_ms": avg_ms, "launches_timed": len(ms),
+                "timing": "step events (one launch per step)" if L == 1 else
+                "library event hooks around one layer per step (layer = step % 48)"}
+    peak = tc_burst if L == 1 else tc_sust
+    flops = T * 10 * FLOPS_PER_PAIR[dom]
+    achieved = flops / (avg_ms / 1e3) / 1e12
+    other = "TC_DOWN" if dom == "TC_GATEUP" else "TC_GATEUP"
+    o_ms = float(np.mean(kernel_ms[other])) if kernel_ms.get(other) else None
+    return {"kernel": f"tc_expert_kernel ({'gate/up + SwiGLU' if dom == 'TC_GATEUP' else 'down'}, tcgen05 fp16)",
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "frac_of": f"{'bf16_tflops' if L == 1 else 'bf16_tflops_sustained'}, {src}",
+            "traffic": ncu_traffic(cfg["name"], dom), "algorithmic_flops_per_launch": flops,
+            "avg_launch_ms": avg_ms, "launches_timed": len(ms),
+            "other_expert_kernel": None if o_ms is None else {
+                "kernel": other, "avg_launch_ms": o_ms,
+                "achieved_tflops": T * 10 * FLOPS_PER_PAIR[other] / (o_ms / 1e3) / 1e12},
+            "timing": "library event hooks around every launch of the two expert kernels"}
 
 
 def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, world):
@@ -405,7 +497,8 @@ def reference_arm(args, rank):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
             "steps": K, "warmup": W, "ms_per_step": 1e3 * float(np.mean(step_s)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["name"]}, "cpu_baseline": cpu,
+            "config": workload_config(cfg, args.seed, 1, cfg_id in (0, 1), None),
+            "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

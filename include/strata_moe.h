@@ -179,6 +179,47 @@ strata_status strata_clear_status(void* ws, void* stream);
 /* Static string naming a status code. */
 const char* strata_status_str(strata_status s);
 
+/* ---- Diagnostics: launch accounting and kernel timing -------------------------------------------
+ * Not part of the method: these let a caller measure the library's kernels with its own CUDA events.
+ * Kernel ids (every kernel the library launches): */
+#define STRATA_KERNEL_DECODE_LAYER 0   /* whole layer for T <= 8, one cooperative launch */
+#define STRATA_KERNEL_ROUTE_DECODE 1   /* router GEMV + top-10 + grouping, T <= 8 (strata_moe_route) */
+#define STRATA_KERNEL_RMSNORM 2
+#define STRATA_KERNEL_ROUTER_TC 3      /* router GEMM on the tensor cores, T > 8 */
+#define STRATA_KERNEL_TOP_K 4
+#define STRATA_KERNEL_GROUP_HIST 5
+#define STRATA_KERNEL_GROUP_SCAN 6
+#define STRATA_KERNEL_GROUP_SCATTER 7
+#define STRATA_KERNEL_BUILD_TILES 8
+#define STRATA_KERNEL_QUANTISE_X 9
+#define STRATA_KERNEL_GEMV_GATEUP 10   /* Q2_0 gate/up + SwiGLU GEMV, T <= 8 (strata_moe_experts) */
+#define STRATA_KERNEL_GEMV_DOWN 11
+#define STRATA_KERNEL_TC_PREPARE 12    /* tile list of the tensor-core expert path, T > 8 */
+#define STRATA_KERNEL_TC_GATHER 13     /* fp16 token gather per expert */
+#define STRATA_KERNEL_TC_GATEUP 14     /* Q2_0 gate/up + SwiGLU grouped GEMM (tcgen05) */
+#define STRATA_KERNEL_TC_DOWN 15       /* Q2_0 down grouped GEMM (tcgen05) */
+#define STRATA_KERNEL_COMBINE 16
+#define STRATA_KERNEL_PACK 17
+#define STRATA_KERNEL_COUNT 18
+
+/* Number of kernels this process has launched through the library so far (all threads). */
+uint64_t strata_moe_launch_count(void);
+
+/* Arm event timing of one kernel for the calling host thread: of the launches of kernel `kernel` made
+ * from this thread after this call, the first `skip` are not recorded and the next n record
+ * start_events[i] on the launch's stream just before launch i and stop_events[i] just after it
+ * (cudaEventRecord; i = 0 .. n-1), so cudaEventElapsedTime(start_events[i], stop_events[i]) is that
+ * launch's duration on the device.  The arrays are host arrays of cudaEvent_t handles owned by the
+ * caller; the library keeps the two array pointers (not copies) until it is re-armed or disarmed, so
+ * they must stay valid until then.  n == 0 disarms.  Not meant for stream capture (event records in a
+ * captured stream are ordering nodes, not timestamps).  Returns STRATA_E_INVAL for a bad kernel id,
+ * skip < 0, n < 0, or NULL arrays with n > 0. */
+strata_status strata_moe_profile_arm(int32_t kernel, int32_t skip, void* const* start_events, void* const* stop_events,
+                                     int32_t n);
+
+/* How many launches of `kernel` were recorded since it was last armed (calling thread); -1 for a bad id. */
+int32_t strata_moe_profile_recorded(int32_t kernel);
+
 #ifdef __cplusplus
 }
 #endif

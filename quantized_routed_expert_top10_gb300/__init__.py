@@ -41,7 +41,8 @@ EXPORTS = (
     "strata_moe_group_noalloc",
     "strata_moe_experts", "strata_moe_combine", "strata_moe_layer", "strata_moe_stack",
     "strata_pack_q2_0", "strata_unpack_q2_0", "strata_pack_q2_0_device", "strata_poll_status",
-    "strata_clear_status", "strata_status_str",
+    "strata_clear_status", "strata_status_str", "strata_moe_launch_count", "strata_moe_profile_arm",
+    "strata_moe_profile_recorded",
 )
 
 
@@ -89,6 +90,9 @@ def lib():
             "strata_poll_status": (ctypes.c_int, [_vp, _vp]),
             "strata_clear_status": (ctypes.c_int, [_vp, _vp]),
             "strata_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+            "strata_moe_launch_count": (ctypes.c_uint64, []),
+            "strata_moe_profile_arm": (ctypes.c_int, [_i32, _i32, _vp, _vp, _i32]),
+            "strata_moe_profile_recorded": (_i32, [_i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -208,3 +212,41 @@ def strata_clear_status(ws, stream=None):
 
 def strata_status_str(status: int) -> str:
     return lib().strata_status_str(status).decode()
+
+
+# kernel ids of strata_moe_profile_arm (STRATA_KERNEL_* of the header)
+KERNELS = ("DECODE_LAYER", "ROUTE_DECODE", "RMSNORM", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN",
+           "GROUP_SCATTER", "BUILD_TILES", "QUANTISE_X", "GEMV_GATEUP", "GEMV_DOWN", "TC_PREPARE", "TC_GATHER",
+           "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK")
+KERNEL_ID = {name: i for i, name in enumerate(KERNELS)}
+
+
+def strata_moe_launch_count() -> int:
+    return int(lib().strata_moe_launch_count())
+
+
+def strata_moe_profile_arm(kernel, start_events, stop_events, skip=0):
+    """Arm event timing of `kernel` (name or id) for this thread with lists of torch.cuda.Event (or raw
+    cudaEvent_t handles), after `skip` unrecorded launches; returns the ctypes arrays, which the caller
+    must keep alive while armed.  Empty lists disarm."""
+    kid = KERNEL_ID[kernel] if isinstance(kernel, str) else int(kernel)
+    n = len(start_events)
+    if len(stop_events) != n:
+        raise ValueError("start and stop event lists differ in length")
+
+    def handle(ev):
+        h = ev if isinstance(ev, int) else ev.cuda_event
+        if not h:
+            raise ValueError("event has no CUDA handle yet (torch creates it on its first record())")
+        return h
+
+    arr_t = ctypes.c_void_p * max(n, 1)
+    a = arr_t(*[handle(e) for e in start_events])
+    b = arr_t(*[handle(e) for e in stop_events])
+    _check("strata_moe_profile_arm", lib().strata_moe_profile_arm(kid, skip, a if n else None, b if n else None, n))
+    return a, b
+
+
+def strata_moe_profile_recorded(kernel) -> int:
+    kid = KERNEL_ID[kernel] if isinstance(kernel, str) else int(kernel)
+    return int(lib().strata_moe_profile_recorded(kid))

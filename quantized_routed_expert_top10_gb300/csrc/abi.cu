@@ -54,14 +54,14 @@ strata_status route_and_group(const float* x, int T, int norm, const uint16_t* w
     STRATA_CUDA(launch_route_decode(x, T, norm, w_router, bias, E, q2_offset, ids, weights, logits_user, L, ws, s));
     return STRATA_OK;
   }
-  const float* xin = x;
+  const float* inv = nullptr;
   if (norm) {
-    STRATA_CUDA(launch_rmsnorm(x, T, (float*)(ws + L.xn), s));
-    xin = (const float*)(ws + L.xn);
+    STRATA_CUDA(launch_inv_rms(x, T, (float*)(ws + L.inv_rms), s));
+    inv = (const float*)(ws + L.inv_rms);
   }
-  float* logits = logits_user ? logits_user : (float*)(ws + L.logits);
-  STRATA_CUDA(launch_router_tc(xin, T, w_router, bias, E, logits, (int*)(ws + L.status), s));
-  STRATA_CUDA(launch_top_k(logits, T, E, ids, weights, s));
+  float* lparts = (float*)(ws + L.logits);
+  STRATA_CUDA(launch_router_tc(x, inv, T, w_router, E, lparts, (int*)(ws + L.status), s));
+  STRATA_CUDA(launch_top_k(lparts, T, E, bias, logits_user, ids, weights, s));
   STRATA_CUDA(launch_group(ids, T, E, (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair),
                            (int32_t*)(ws + L.active), nullptr, L, ws, s));
   return STRATA_OK;
@@ -89,8 +89,8 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
   }
   STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
   float* parts = (float*)(w + L.parts);
-  const float* xin = norm ? (const float*)(w + L.xn) : x;
-  STRATA_CUDA(launch_experts_tc(*ex, xin, T, (const int32_t*)(w + L.expert_off), (const int32_t*)(w + L.pair),
+  const float* inv = norm ? (const float*)(w + L.inv_rms) : nullptr;
+  STRATA_CUDA(launch_experts_tc(*ex, x, inv, T, (const int32_t*)(w + L.expert_off), (const int32_t*)(w + L.pair),
                                 (const int32_t*)(w + L.active), (const int32_t*)(w + L.n_active), parts,
                                 (uint8_t*)(w + L.xg), (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta),
                                 (int*)(w + L.status), s));
@@ -132,9 +132,9 @@ strata_status strata_moe_route(const float* x, int32_t T, const uint16_t* w_rout
     STRATA_CUDA(launch_route_decode(x, T, 0, w_router, bias, n_expert, 1, ids, weights, logits, L, w, s));
     return STRATA_OK;
   }
-  float* lg = logits ? logits : (float*)(w + L.logits);
-  STRATA_CUDA(launch_router_tc(x, T, w_router, bias, n_expert, lg, (int*)(w + L.status), s));
-  STRATA_CUDA(launch_top_k(lg, T, n_expert, ids, weights, s));
+  float* lparts = (float*)(w + L.logits);
+  STRATA_CUDA(launch_router_tc(x, nullptr, T, w_router, n_expert, lparts, (int*)(w + L.status), s));
+  STRATA_CUDA(launch_top_k(lparts, T, n_expert, bias, logits, ids, weights, s));
   return STRATA_OK;
 }
 
@@ -167,7 +167,7 @@ strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int
   char* w = (char*)ws;
   cudaStream_t s = (cudaStream_t)stream;
   if (T > DECODE_T_MAX) {
-    STRATA_CUDA(launch_experts_tc(*ex, x, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
+    STRATA_CUDA(launch_experts_tc(*ex, x, nullptr, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
                                   (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
     return STRATA_OK;
   }

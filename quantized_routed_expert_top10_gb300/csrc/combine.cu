@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual, float* out,
                            cudaStream_t s) {
   const int64_t n4 = (int64_t)T * (H / 4);
-  combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(parts, weights, T, residual, out);
+  STRATA_LAUNCH(KID_COMBINE, s,
+                combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(parts, weights, T, residual, out));
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ constexpr int64_t BLOB = STRATA_MOE_BLOB_BYTES;
 // S_SPLIT ways when the call is small (decode), so enough CTAs stream the weights.
 constexpr int NT = 8;
 constexpr int S_SPLIT = 4;
+constexpr int ROUTER_KSPLIT = 4;  // prefill router: splits of the 2,560-term contraction over CTAs
 constexpr int DECODE_T_MAX = 8;  // T <= this: fused single-kernel routing (router + top-10 + grouping)
 
 // Device status bits (ws word 0).
@@ -79,10 +80,11 @@ static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sy
 
 struct WsLayout {
   size_t status, cnt_route, cnt_gu;
-  size_t logits;      // fp32 [T][EMAX]
+  size_t logits;      // fp32 [ROUTER_KSPLIT][T][EMAX] partial router logits (T > DECODE_T_MAX: one slice per
+                      // split of the contraction; the decode path uses slice 0 as [T][EMAX] logits)
   size_t ids;         // int32 [T][K]
   size_t weights;     // fp32 [T][K]
-  size_t xn;          // fp32 [T][H] normalised input (residual layers, T > DECODE_T_MAX)
+  size_t inv_rms;     // fp32 [T] 1/rms of each token (residual layers, T > DECODE_T_MAX)
   size_t sumsq;       // fp32 [WS_NREP][T][KB_GU] per-block sums of squares, replicated (one-kernel decode layer)
   size_t dots_rep;    // fp32 [WS_NREP][T][EMAX] replicated router dot products (one-kernel decode layer)
   size_t expert_off;  // int32 [EMAX + 1]
@@ -130,10 +132,10 @@ inline WsLayout ws_layout(int T) {
   L.cnt_gu = WS_CNT_GU;
   size_t o = WS_HEADER;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
-  L.logits = take(sizeof(float) * (size_t)T * EMAX);
+  L.logits = take(sizeof(float) * (size_t)ROUTER_KSPLIT * T * EMAX);
   L.ids = take(sizeof(int32_t) * (size_t)P);
   L.weights = take(sizeof(float) * (size_t)P);
-  L.xn = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);
+  L.inv_rms = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T : 0);
   L.sumsq = take(sizeof(float) * (size_t)WS_NREP * T * KB_GU);
   L.dots_rep = take(sizeof(float) * (size_t)WS_NREP * (T < DECODE_T_MAX ? T : DECODE_T_MAX) * EMAX);
   L.expert_off = take(sizeof(int32_t) * (EMAX + 1));
@@ -257,13 +259,30 @@ __device__ __forceinline__ int dot64(const Masked& c, const uint32_t* hi, const 
 
 // Launchers implemented in the .cu files (all enqueue on `stream`, return cudaGetLastError()).
 namespace strata {
+// Launch accounting (instrument.cu): every launch is bracketed by kernel_begin / kernel_end, which count
+// it and record the caller's armed timing events around it.  Ids equal the ABI's STRATA_KERNEL_*.
+enum KernelId : int {
+  KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_RMSNORM, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
+  KID_GROUP_SCATTER, KID_BUILD_TILES, KID_QUANTISE_X, KID_GEMV_GATEUP, KID_GEMV_DOWN, KID_TC_PREPARE,
+  KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_COUNT
+};
+void kernel_begin(int kid, cudaStream_t s);
+void kernel_end(int kid, cudaStream_t s);
+#define STRATA_LAUNCH(kid, s, ...) \
+  do {                             \
+    kernel_begin((kid), (s));      \
+    __VA_ARGS__;                   \
+    kernel_end((kid), (s));        \
+  } while (0)
+
 cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
                                 const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
                                 float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);
-cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s);
-cudaError_t launch_router_tc(const float* x, int T, const uint16_t* w_router, const float* bias, int E,
-                             float* logits, int* status, cudaStream_t s);
-cudaError_t launch_top_k(const float* logits, int T, int E, int32_t* ids, float* weights, cudaStream_t s);
+cudaError_t launch_inv_rms(const float* x, int T, float* inv_rms, cudaStream_t s);
+cudaError_t launch_router_tc(const float* x, const float* inv_rms, int T, const uint16_t* w_router, int E,
+                             float* parts, int* status, cudaStream_t s);
+cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, float* logits_out, int32_t* ids,
+                         float* weights, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair,
                          int32_t* active, int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
@@ -271,8 +290,9 @@ cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active,
 cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s);
 cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t* pair, const WsLayout& L,
                                 char* ws, float* parts, cudaStream_t s);
-cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, int T, const int32_t* expert_off,
-                              const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
+cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
+                              const int32_t* expert_off, const int32_t* pair, const int32_t* active,
+                              const int32_t* n_active, float* parts,
                               uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);

@@ -463,7 +463,9 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
     if (dev >= 0 && dev < 64) g_info[dev].grid[vi] = grid;
   }
   void* args[] = {(void*)&prm};
-  return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(DF_THREADS), args, smem, s);
+  STRATA_LAUNCH(KID_DECODE_LAYER, s,
+                err = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(DF_THREADS), args, smem, s));
+  return err;
 }
 
 }  // namespace

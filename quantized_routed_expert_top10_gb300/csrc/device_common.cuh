@@ -221,10 +221,11 @@ __device__ __forceinline__ int cta_exclusive_scan(const int* cnt, int* out, int 
   return total;
 }
 
-// Stable scatter of pairs [p0, p1) by one warp: fill[e] (shared) holds the next slot of expert e.
-// ids may be in shared or global memory; ids outside [0, E) are skipped.
+// Stable scatter of pairs [p0, p1) by one warp: fill[e] (shared) holds the next slot of expert e, which
+// receives pair number pair_base + p.  ids may be in shared or global memory; ids outside [0, E) are
+// skipped.
 __device__ __forceinline__ void stable_scatter_warp(const int32_t* ids, int p0, int p1, int E, int* fill,
-                                                    int32_t* pair) {
+                                                    int32_t* pair, int pair_base) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   for (int base = p0; base < p1; base += 32) {
@@ -237,7 +238,7 @@ __device__ __forceinline__ void stable_scatter_warp(const int32_t* ids, int p0, 
     if (e >= 0) pos = fill[e] + rank;
     __syncwarp();
     if (e >= 0) {
-      pair[pos] = p;
+      pair[pos] = pair_base + p;
       if ((same >> lane) == 1u) fill[e] += __popc(same);  // highest lane of the group
     }
     __syncwarp();

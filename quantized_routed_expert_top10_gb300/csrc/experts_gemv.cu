@@ -254,12 +254,14 @@ cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t
   constexpr int S = S_SPLIT;
   const size_t smem = NSTAGE * GU_CHUNK + sizeof(QBlock) * (KB_GU / S) * NT;
   cudaFuncSetAttribute(gateup_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  gateup_kernel<S><<<max_tiles * RT_GU * S, 128, smem, s>>>(blobs, ex.blob_stride, tiles, nat, pair, qx,
-                                                           (float*)(ws + L.partial), (int*)(ws + L.cnt_gu), hq,
-                                                           ex.q2_offset, status);
+  STRATA_LAUNCH(KID_GEMV_GATEUP, s,
+                gateup_kernel<S><<<max_tiles * RT_GU * S, 128, smem, s>>>(
+                    blobs, ex.blob_stride, tiles, nat, pair, qx, (float*)(ws + L.partial), (int*)(ws + L.cnt_gu), hq,
+                    ex.q2_offset, status));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  down_kernel<<<max_tiles * RT_D, 128, 0, s>>>(blobs, ex.blob_stride, tiles, nat, pair, hq, parts, status);
+  STRATA_LAUNCH(KID_GEMV_DOWN, s,
+                down_kernel<<<max_tiles * RT_D, 128, 0, s>>>(blobs, ex.blob_stride, tiles, nat, pair, hq, parts, status));
   return cudaGetLastError();
 }
 

@@ -8,13 +8,20 @@
 // Per expert e with n_e tokens (its slots in the grouping), two grouped GEMMs with the weights as the
 // M = 128 operand ("swap AB") and the expert's tokens as N (up to 128 per tile):
 //   gate/up:  [g; u] (2 x 128 rows x N) = [G_rt; U_rt] (128 x 2560) * X_e^T, h = silu(g) * u -> Hg (fp16)
-//   down:     y (128 rows x N) = D_rt (128 x 640) * H_e^T -> parts[pair][row] (fp32)
-// Warp roles in each persistent CTA (one per SM): warp 0 streams the Q2_0 code chunks and the token
-// tile of each 64-wide k-block with cp.async.bulk; warps 4.. dequantise the codes straight into the
-// 128B-swizzled K-major shared-memory layout (fp16: (c + 1024) built by one LOP3 per pair, minus
-// (1024 + q2_offset), times d -- all exact); warp 1 issues tcgen05.mma (fp16 x fp16 -> fp32 in TMEM)
-// and commits to the stage's "empty" mbarrier; after the last k-block the same dequant warps read the
-// accumulators with tcgen05.ld for the epilogue.  Every wait is bounded (STRATA_E_TIMEOUT).
+//   down:     [y_2rp; y_2rp+1] (2 x 128 rows x N) = [D_2rp; D_2rp+1] (128 x 640 each) * H_e^T
+//             -> parts[pair][row] (fp32); two row tiles per item so each token tile is read half as often
+// Warp roles in each persistent CTA (one per SM; work items = (tile, 128-row tile of the weights)):
+//   warp 0      streams the token tile and the Q2_0 code chunk of each 64-wide k-block with
+//               cp.async.bulk into a 6-stage ring;
+//   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
+//               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
+//               exact) in a 2-stage ring of weight tiles;
+//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into one of two TMEM accumulator buffers and
+//               commits to the stages' "empty" mbarriers;
+//   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
+//               epilogue while the next item accumulates into the other buffer;
+//   warp 2      owns the TMEM allocation.
+// Every wait is bounded (STRATA_E_TIMEOUT).
 //
 // In-block order: the dequantiser emits the 64 weights of a block in the order pi (per 16 weights:
 // 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15), which is what one LOP3 per half2 produces from the packed
@@ -26,14 +33,10 @@ namespace strata {
 namespace {
 
 constexpr int TCN = 128;        // max tokens per tile (MMA N)
-constexpr int TC_NS = 4;        // ring stages
-constexpr int GU_THREADS = 384; // warp 0 producer, warp 1 MMA, warps 4..11 dequant/epilogue
-constexpr int DN_THREADS = 384;
 constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 64 fp16
 constexpr uint32_t B_TILE = TCN * 128;      // up to 128 token rows x 64 fp16
 
-// position s (0..15) of the emitted order -> weight index within the 16; and its inverse
-__host__ __device__ __forceinline__ int pi16(int s) { return ((s >> 1) & 3) + 4 * ((s >> 3) & 1) + 8 * (s & 1); }
+// Position in the emitted order (0..15) of weight j of a 16-group: the order is 0,8,1,9,..,7,15.
 __host__ __device__ __forceinline__ int pi16_inv(int j) { return 2 * (j & 3) + 8 * ((j >> 2) & 1) + ((j >> 3) & 1); }
 
 struct TcExpert { int32_t e, q0, n, q0pad; };    // grouping slots [q0, q0+n), padded rows from q0pad
@@ -76,114 +79,147 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
 }
 
 // ---------------------------------------------------------------------------------------------
-// Xg[kb][row][128 B]: row = padded slot; fp16 x of the slot's token in pi order, swizzled by row % 8.
+// Xg[kb][row][128 B]: row = padded slot; fp16 x of the slot's token (times its 1/rms for residual
+// layers) in pi order, swizzled by row % 8; rows past an expert's tokens are zero.  One warp per
+// padded row (the expert found by binary search over the experts' first rows, staged in shared
+// memory); lane = (k-block within a group of 4, 16-byte chunk), so a warp reads 1 KB of x contiguously.
+// Chunk c of a 64-block holds weights {0,8,1,9,2,10,3,11} (c even) or {4,12,5,13,6,14,7,15} (c odd)
+// of the block's 16-group c / 2: two float4 loads.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_gather_kernel(const float* __restrict__ x, const int32_t* __restrict__ pair,
-                                                        const TcExpert* __restrict__ exps,
-                                                        const int32_t* __restrict__ counts, uint8_t* __restrict__ xg,
-                                                        int64_t rows_cap) {
-  const int kb = blockIdx.y;
-  const int na = counts[0];
-  for (int i = blockIdx.x; i < na; i += gridDim.x) {
-    const TcExpert ex = exps[i];
-    const int npad = (ex.n + 7) / 8 * 8;
-    for (int idx = threadIdx.x; idx < npad * 8; idx += blockDim.x) {
-      const int s = idx >> 3, c = idx & 7;
+constexpr int GATHER_THREADS = 256;
+constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over rows; 4 CTAs per SM of a 152-SM GB300
+__global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const float* __restrict__ x,
+                                                                   const float* __restrict__ inv_rms,
+                                                                   const int32_t* __restrict__ pair,
+                                                                   const TcExpert* __restrict__ exps,
+                                                                   const int32_t* __restrict__ counts,
+                                                                   uint8_t* __restrict__ xg, int64_t rows_cap) {
+  __shared__ int s_row0[EMAX];
+  const int na = counts[0], ppad = counts[2];
+  for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_row0[i] = exps[i].q0pad;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (GATHER_THREADS / 32);
+  for (int r = blockIdx.x * (GATHER_THREADS / 32) + (threadIdx.x >> 5); r < ppad && r < rows_cap; r += warps) {
+    int lo = 0, hi = na - 1;  // last expert whose first row is <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_row0[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const TcExpert ex = exps[lo];
+    const int s = r - ex.q0pad;
+    const int t = (s < ex.n) ? pair[ex.q0 + s] / K : -1;
+    const float sc = (t >= 0 && inv_rms) ? __ldg(inv_rms + t) : 1.f;
+    const int c = lane & 7, odd = c & 1;
+#pragma unroll 2
+    for (int kb = lane >> 3; kb < KB_GU; kb += 4) {
       uint4 out = make_uint4(0, 0, 0, 0);
-      if (s < ex.n) {
-        const int t = pair[ex.q0 + s] / K;
-        const float* src = x + (size_t)t * H + kb * QK + 16 * (c >> 1);
-        __half hv[8];
-#pragma unroll
-        for (int e8 = 0; e8 < 8; ++e8) hv[e8] = __float2half_rn(src[pi16(8 * (c & 1) + e8)]);
-        out = *reinterpret_cast<uint4*>(hv);
+      if (t >= 0) {
+        const float* src = x + (size_t)t * H + kb * QK + 16 * (c >> 1) + 4 * odd;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(src + 8));
+        const __half2 h0 = __floats2half2_rn(a.x * sc, b.x * sc), h1 = __floats2half2_rn(a.y * sc, b.y * sc);
+        const __half2 h2 = __floats2half2_rn(a.z * sc, b.z * sc), h3 = __floats2half2_rn(a.w * sc, b.w * sc);
+        out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                         *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
       }
-      const int64_t row = ex.q0pad + s;
-      if (row < rows_cap)
-        *reinterpret_cast<uint4*>(xg + ((int64_t)kb * rows_cap + row) * 128 + ((c ^ (row & 7)) << 4)) = out;
+      *reinterpret_cast<uint4*>(xg + ((int64_t)kb * rows_cap + r) * 128 + ((c ^ (r & 7)) << 4)) = out;
     }
   }
 }
 
-// Dequantise one 16-byte Q2_0 code row (64 weights, scale d) into 8 swizzled 16-byte chunks of row r.
-// Chunks [c0, c0 + nc) only.
-__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r, int c0,
-                                            int nc) {
-  const __half2 magic_off = __half2half2(__float2half_rn(1024.f + (float)q2_offset));
+// Dequantise one 16-byte Q2_0 code row (64 weights, scale d) into the 8 swizzled 16-byte chunks of
+// row r of a K-major tile.  Chunk c holds code bytes (c & 1) and 2 + (c & 1) of word c / 2, i.e.
+// weights 4(c&1) .. +3 and 8 + 4(c&1) .. +3 of the 16-group c / 2; its half2 number m holds field m
+// (bits 2m, 2m + 1) of both bytes.  OR-ing the field into the mantissa of M_m = 2^(10 - 2m), whose
+// last-place unit sits at bit 2m, gives M_m + code in one LOP3; subtracting M_m + q2_offset and
+// multiplying by d are exact.
+__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r) {
   const __half2 d2 = __half2half2(d);
   const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  __half2 sub[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) sub[m] = __half2half2(__float2half_rn((float)((1024 >> (2 * m)) + q2_offset)));
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    if (c < c0 || c >= c0 + nc) continue;
-    const uint32_t word = w[c >> 1];
-    const int base = (c & 1) ? 8 : 0;  // chunk 2q: pairs m = 0..3 (shift 2m); chunk 2q+1: shift 8 + 2m
+    const uint32_t word = (c & 1) ? (w[c >> 1] >> 8) : w[c >> 1];
     uint32_t out[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const uint32_t bits = ((word >> (base + 2 * m)) & 0x00030003u) | 0x64006400u;  // half2(1024 + c)
+      const uint32_t magic = (uint32_t)((25 - 2 * m) << 10) * 0x00010001u;  // half2(2^(10 - 2m))
+      const uint32_t bits = (word & (0x00030003u << (2 * m))) | magic;       // half2(M_m + code)
       __half2 h = *reinterpret_cast<const __half2*>(&bits);
-      h = __hmul2(__hsub2(h, magic_off), d2);                                         // (c - off) * d, exact
+      h = __hmul2(__hsub2(h, sub[m]), d2);                                   // (code - q2_offset) * d
       out[m] = *reinterpret_cast<uint32_t*>(&h);
     }
     *reinterpret_cast<uint4*>(tile + tc::swz_off(r, c)) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
-struct TcGuParams {
+struct TcParams {
   const uint8_t* blobs;
   int64_t stride;
   int q2_offset;
   const TcTile* tiles;
   const int32_t* counts;
-  const uint8_t* xg;
-  uint8_t* hg;
+  const uint8_t* act;   // gate/up: Xg; down: Hg
+  uint8_t* hg;          // gate/up output
   int64_t rows_cap;
+  const int32_t* pair;  // down: slot -> pair
+  float* parts;         // down output
   int* status;
 };
 
-struct TcDnParams {
-  const uint8_t* blobs;
-  int64_t stride;
-  int q2_offset;
-  const TcTile* tiles;
-  const int32_t* counts;
-  const uint8_t* hg;
-  int64_t rows_cap;
-  const int32_t* pair;
-  float* parts;
-  int* status;
+// Kernel geometry.  Warp 0: bulk-copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
+// dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each);
+// warps 12..15: epilogue (one TMEM lane = one weight row per thread).
+// gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
+// down (GU = false): item = (tile, pair of row tiles 2rp, 2rp + 1 of down): both share the token tile.
+// TMEM accumulator buffer b (of 2): matrix j in columns [b*256 + j*128, +128).
+constexpr int TC_THREADS = 512;
+constexpr int NS_TMA = 6;  // stages of (token tile, code chunks)
+constexpr int NS_A = 2;    // stages of dequantised weight tiles
+template <bool GU>
+struct TcGeo {
+  static constexpr int NMAT = 2;
+  static constexpr int KBN = GU ? KB_GU : KB_D;          // k-blocks per item
+  static constexpr int RTN = GU ? RT_GU : RT_D / 2;      // items per token tile
+  static constexpr int CODE = GU ? GU_CHUNK : 2 * D_CHUNK; // code bytes per k-block
+  static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
+  static constexpr uint32_t A_STAGE = NMAT * A_TILE;
+  static constexpr uint32_t TMEM_BUF = NMAT * TCN;     // accumulator columns per buffer
+  static constexpr uint32_t TMEM_COLS = 2 * TMEM_BUF;  // double buffered
+  static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
 };
 
-// Shared-memory plan of one stage (1024-aligned pieces): A tile(s), B tile, code chunk.
-template <int NA, int CODE>
-struct StagePlan {
-  static constexpr uint32_t A_OFF = 0;
-  static constexpr uint32_t B_OFF = NA * A_TILE;
-  static constexpr uint32_t C_OFF = B_OFF + B_TILE;
-  static constexpr uint32_t BYTES = (C_OFF + CODE + 1023) / 1024 * 1024;
-};
-using GuPlan = StagePlan<2, GU_CHUNK>;
-using DnPlan = StagePlan<1, D_CHUNK>;
-
-// ---------------------------------------------------------------------------------------------
-// gate/up + SwiGLU.  Work item = (tile, row tile rt); TMEM: gate columns [0, 128), up [128, 256).
-// ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(GU_THREADS, 1) gu_tc_kernel(const TcGuParams p) {
+template <bool GU>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams p) {
+  using G = TcGeo<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full_tma[TC_NS], full_a[TC_NS], empty[TC_NS], tmem_full, tmem_empty, mma_done;
+  uint8_t* tma_ring = smem;
+  uint8_t* a_ring = smem + (size_t)NS_TMA * G::TMA_STAGE;
+  __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
+  __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
+  __shared__ int s_fail_flag;
+  volatile int& s_fail = s_fail_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp == 2) tc::tmem_alloc(&tmem_base, 256);
+  if (warp == 2) tc::tmem_alloc(&tmem_base, G::TMEM_COLS);
   if (tid == 0) {
-    for (int s = 0; s < TC_NS; ++s) {
+    for (int s = 0; s < NS_TMA; ++s) {
       mbar_init(&full_tma[s], 1);
-      mbar_init(&full_a[s], 8);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty_tma[s], 1);
     }
-    mbar_init(&tmem_full, 1);
-    mbar_init(&tmem_empty, 8);
+    for (int s = 0; s < NS_A; ++s) {
+      mbar_init(&full_a[s], 8);
+      mbar_init(&empty_a[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4);
+    }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
     s_fail = 0;
@@ -192,261 +228,172 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gu_tc_kernel(const TcGuParams p
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int n_items = p.counts[1] * RT_GU;
+  const int n_items = p.counts[1] * G::RTN;
   int* status = p.status;
 
   if (warp == 0) {
-    // ---------------- producer ----------------
+    // ---------------- producer: token tile + code chunk per k-block ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int it = 0;
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
-        const TcTile tl = p.tiles[item / RT_GU];
-        const int rt = item % RT_GU;
+        const TcTile tl = p.tiles[item / G::RTN];
+        const int rt = item % G::RTN;
         const int nrows = (tl.n + 15) / 16 * 16;
-        const uint8_t* codes = p.blobs + (int64_t)tl.e * p.stride + (int64_t)rt * KB_GU * GU_CHUNK;
-        for (int kb = 0; kb < KB_GU; ++kb, ++it) {
-          const int s = it % TC_NS;
-          if (it >= TC_NS && !mbar_wait(&empty[s], (uint32_t)((it / TC_NS - 1) & 1), status)) { s_fail = 1; break; }
-          uint8_t* st = smem + s * GuPlan::BYTES;
-          mbar_expect_tx(&full_tma[s], GU_CHUNK + nrows * 128);
-          bulk_g2s_stream(st + GuPlan::C_OFF, codes + (int64_t)kb * GU_CHUNK, GU_CHUNK, &full_tma[s], pol);
-          bulk_g2s(st + GuPlan::B_OFF, p.xg + ((int64_t)kb * p.rows_cap + tl.q0pad) * 128, nrows * 128, &full_tma[s]);
+        const uint8_t* blob = p.blobs + (int64_t)tl.e * p.stride;
+        for (int kb = 0; kb < G::KBN; ++kb, ++it) {
+          const int s = it % NS_TMA;
+          if (it >= NS_TMA && !mbar_wait(&empty_tma[s], (uint32_t)((it / NS_TMA - 1) & 1), status)) {
+            s_fail = 1;
+            break;
+          }
+          uint8_t* st = tma_ring + (size_t)s * G::TMA_STAGE;
+          mbar_expect_tx(&full_tma[s], G::CODE + nrows * 128);
+          bulk_g2s(st, p.act + ((int64_t)kb * p.rows_cap + tl.q0pad) * 128, nrows * 128, &full_tma[s]);
+          if (GU) {
+            bulk_g2s_stream(st + B_TILE, blob + ((int64_t)rt * KB_GU + kb) * GU_CHUNK, GU_CHUNK, &full_tma[s], pol);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              bulk_g2s_stream(st + B_TILE + h * D_CHUNK, blob + D_REGION + ((int64_t)(2 * rt + h) * KB_D + kb) * D_CHUNK,
+                              D_CHUNK, &full_tma[s], pol);
+          }
         }
       }
-      // copies still in flight (only after a failed wait): let them land before the CTA leaves
-      for (int back = 1; back <= TC_NS && back <= it; ++back)
-        mbar_wait(&full_tma[(it - back) % TC_NS], (uint32_t)(((it - back) / TC_NS) & 1), status);
+      for (int back = 1; back <= NS_TMA && back <= it; ++back)  // copies still in flight after a failure
+        mbar_wait(&full_tma[(it - back) % NS_TMA], (uint32_t)(((it - back) / NS_TMA) & 1), status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       int it = 0, ti = 0;
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x, ++ti) {
-        const TcTile tl = p.tiles[item / RT_GU];
+        const TcTile tl = p.tiles[item / G::RTN];
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
-        if (ti > 0 && !mbar_wait(&tmem_empty, (uint32_t)((ti - 1) & 1), status)) { s_fail = 1; break; }
+        const int b = ti & 1;
+        if (ti >= 2 && !mbar_wait(&tmem_empty[b], (uint32_t)(((ti >> 1) - 1) & 1), status)) {
+          s_fail = 1;
+          break;
+        }
         tc::fence_after_sync();
-        for (int kb = 0; kb < KB_GU; ++kb, ++it) {
-          const int s = it % TC_NS;
-          const uint32_t par = (uint32_t)((it / TC_NS) & 1);
-          if (!mbar_wait(&full_tma[s], par, status) || !mbar_wait(&full_a[s], par, status)) { s_fail = 1; break; }
-          tc::fence_after_sync();
-          uint8_t* st = smem + s * GuPlan::BYTES;
-          const uint64_t ag = tc::smem_desc_sw128(smem_u32(st + GuPlan::A_OFF));
-          const uint64_t au = tc::smem_desc_sw128(smem_u32(st + GuPlan::A_OFF + A_TILE));
-          const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + GuPlan::B_OFF));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            tc::mma_f16(tmem, ag + 2 * kk, bd + 2 * kk, idesc, acc);
-            tc::mma_f16(tmem + 128, au + 2 * kk, bd + 2 * kk, idesc, acc);
+        const uint32_t acc = tmem + b * G::TMEM_BUF;
+        for (int kb = 0; kb < G::KBN; ++kb, ++it) {
+          const int s = it % NS_TMA, sa = it % NS_A;
+          if (!mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status) ||
+              !mbar_wait(&full_a[sa], (uint32_t)((it / NS_A) & 1), status)) {
+            s_fail = 1;
+            break;
           }
-          tc::mma_commit(&empty[s]);
+          tc::fence_after_sync();
+          const uint64_t bd = tc::smem_desc_sw128(smem_u32(tma_ring + (size_t)s * G::TMA_STAGE));
+          const uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
+#pragma unroll
+          for (int mat = 0; mat < G::NMAT; ++mat) {
+            const uint64_t ad = tc::smem_desc_sw128(smem_u32(ast + mat * A_TILE));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_f16(acc + mat * TCN, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&empty_tma[s]);
+          tc::mma_commit(&empty_a[sa]);
         }
         if (s_fail) break;
-        tc::mma_commit(&tmem_full);
+        tc::mma_commit(&tmem_full[b]);
       }
-      // every MMA this thread issued has finished before TMEM is released
-      tc::mma_commit(&mma_done);
+      tc::mma_commit(&mma_done);  // every MMA this thread issued has finished before TMEM is released
       mbar_wait(&mma_done, 0u, status);
     }
-  } else if (warp >= 4) {
-    // ---------------- dequant + epilogue (256 threads: row, matrix) ----------------
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------- dequantisers ----------------
     const int dt = tid - 128;
-    const int row = dt & 127, mat = dt >> 7;
-    const int ew = warp - 4;               // epilogue warp 0..7; TMEM lane quadrant = warp % 4
-    const int erow = 32 * (warp & 3) + lane;
-    const int ehalf = ew >> 2;
-    int it = 0, ti = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ti) {
-      const TcTile tl = p.tiles[item / RT_GU];
-      const int rt = item % RT_GU;
-      const int nrows = (tl.n + 15) / 16 * 16;
-      bool ok = true;
-      for (int kb = 0; kb < KB_GU; ++kb, ++it) {
-        const int s = it % TC_NS;
-        uint8_t* st = smem + s * GuPlan::BYTES;
-        if (it >= TC_NS) ok = ok && mbar_wait(&empty[s], (uint32_t)((it / TC_NS - 1) & 1), status);
-        ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / TC_NS) & 1), status);
+    const int row = dt & 127, sub = dt >> 7;  // matrix of the item
+    int it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (int kb = 0; kb < G::KBN; ++kb, ++it) {
+        const int s = it % NS_TMA, sa = it % NS_A;
+        if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], (uint32_t)((it / NS_A - 1) & 1), status);
+        ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status);
         if (ok) {
-          const uint4 cw = *reinterpret_cast<const uint4*>(st + GuPlan::C_OFF + (mat ? 2048 : 0) + 16 * row);
-          const __half d = *reinterpret_cast<const __half*>(st + GuPlan::C_OFF + 4096 + 4 * row + 2 * mat);
-          dequant_row(cw, d, p.q2_offset, st + GuPlan::A_OFF + mat * A_TILE, row, 0, 8);
+          const uint8_t* code = tma_ring + (size_t)s * G::TMA_STAGE + B_TILE;
+          uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
+          // gate/up chunk: gate codes, up codes, {gate d, up d} per row; down: two plain chunks
+          const uint8_t* cb = code + (GU ? 0 : sub * D_CHUNK);
+          const uint4 cw = *reinterpret_cast<const uint4*>(cb + (GU ? sub * 2048 : 0) + 16 * row);
+          const __half d = *reinterpret_cast<const __half*>(cb + (GU ? 4096 + 4 * row + 2 * sub : 2048 + 2 * row));
+          dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full_a[s]);
+        if (lane == 0) tc::mbar_arrive(&full_a[sa]);
       }
-      // epilogue: h = silu(g) * u for this CTA's 128 rows and the tile's tokens
-      ok = ok && mbar_wait(&tmem_full, (uint32_t)(ti & 1), status);
+    }
+  } else if (warp >= 12) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int erow = 32 * q + lane;
+    int ti = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ti) {
+      const TcTile tl = p.tiles[item / G::RTN];
+      const int rt = item % G::RTN;
+      const int nrows = (tl.n + 15) / 16 * 16;
+      const int b = ti & 1;
+      ok = ok && mbar_wait(&tmem_full[b], (uint32_t)((ti >> 1) & 1), status);
       tc::fence_after_sync();
-      const int nch = nrows / 16;
-      const int ch0 = ehalf ? (nch + 1) / 2 : 0, ch1 = ehalf ? nch : (nch + 1) / 2;
-      const int k = rt * 128 + erow;  // h index = down's contraction index
-      const int kbd = k >> 6, k64 = k & 63;
-      const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
-      for (int ch = ch0; ch < ch1; ++ch) {
-        float g[16], u[16];
-        const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
-        tc::tmem_ld16(tmem + lane_addr + 16 * ch, g);
-        tc::tmem_ld16(tmem + lane_addr + 128 + 16 * ch, u);
-        if (ok) {
+      const uint32_t acc = tmem + b * G::TMEM_BUF + ((uint32_t)(32 * q) << 16);
+      if (GU) {
+        const int k = rt * 128 + erow;  // h index = the down projection's contraction index
+        const int kbd = k >> 6, k64 = k & 63;
+        const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
+        for (int ch = 0; ch < nrows / 16; ++ch) {
+          float g[16], u[16];
+          tc::tmem_ld16(acc + 16 * ch, g);
+          tc::tmem_ld16(acc + TCN + 16 * ch, u);
+          if (ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = 16 * ch + i;
-            if (col < tl.n) {
-              const int64_t hrow = tl.q0pad + col;
-              __half* dst = reinterpret_cast<__half*>(p.hg + ((int64_t)kbd * p.rows_cap + hrow) * 128 +
-                                                      (((pos >> 3) ^ (hrow & 7)) << 4)) + (pos & 7);
-              *dst = __float2half_rn(silu_mul(g[i], u[i]));
+            for (int i = 0; i < 16; ++i) {
+              const int col = 16 * ch + i;
+              if (col < tl.n) {
+                const int64_t hrow = tl.q0pad + col;
+                __half* dst = reinterpret_cast<__half*>(p.hg + ((int64_t)kbd * p.rows_cap + hrow) * 128 +
+                                                        (((pos >> 3) ^ (hrow & 7)) << 4)) + (pos & 7);
+                *dst = __float2half_rn(silu_mul(g[i], u[i]));
+              }
+            }
+          }
+        }
+      } else {
+        const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
+        for (int ch = 0; ch < nrows / 16; ++ch) {
+          float y0[16], y1[16];
+          tc::tmem_ld16(acc + 16 * ch, y0);
+          tc::tmem_ld16(acc + TCN + 16 * ch, y1);
+          if (ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = 16 * ch + i;
+              if (col < tl.n) {
+                float* dst = p.parts + (size_t)p.pair[tl.q0 + col] * H + orow;
+                dst[0] = y0[i];
+                dst[128] = y1[i];
+              }
             }
           }
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tmem_empty);
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[b]);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 2) tc::tmem_dealloc(tmem, 256);
-  if (warp == 2) tc::tmem_relinquish();
-}
-
-// ---------------------------------------------------------------------------------------------
-// down.  Work item = (tile, row tile rtd); TMEM columns [0, 128).
-// ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(DN_THREADS, 1) down_tc_kernel(const TcDnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full_tma[TC_NS], full_a[TC_NS], empty[TC_NS], tmem_full, tmem_empty, mma_done;
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp == 2) tc::tmem_alloc(&tmem_base, 128);
-  if (tid == 0) {
-    for (int s = 0; s < TC_NS; ++s) {
-      mbar_init(&full_tma[s], 1);
-      mbar_init(&full_a[s], 8);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(&tmem_full, 1);
-    mbar_init(&tmem_empty, 8);
-    mbar_init(&mma_done, 1);
-    fence_mbar_init();
-    s_fail = 0;
+  if (warp == 2) {
+    tc::tmem_dealloc(tmem, G::TMEM_COLS);
+    tc::tmem_relinquish();
   }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  const int n_items = p.counts[1] * RT_D;
-  int* status = p.status;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int it = 0;
-      for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
-        const TcTile tl = p.tiles[item / RT_D];
-        const int rtd = item % RT_D;
-        const int nrows = (tl.n + 15) / 16 * 16;
-        const uint8_t* codes = p.blobs + (int64_t)tl.e * p.stride + D_REGION + (int64_t)rtd * KB_D * D_CHUNK;
-        for (int kb = 0; kb < KB_D; ++kb, ++it) {
-          const int s = it % TC_NS;
-          if (it >= TC_NS && !mbar_wait(&empty[s], (uint32_t)((it / TC_NS - 1) & 1), status)) { s_fail = 1; break; }
-          uint8_t* st = smem + s * DnPlan::BYTES;
-          mbar_expect_tx(&full_tma[s], D_CHUNK + nrows * 128);
-          bulk_g2s_stream(st + DnPlan::C_OFF, codes + (int64_t)kb * D_CHUNK, D_CHUNK, &full_tma[s], pol);
-          bulk_g2s(st + DnPlan::B_OFF, p.hg + ((int64_t)kb * p.rows_cap + tl.q0pad) * 128, nrows * 128, &full_tma[s]);
-        }
-      }
-      // copies still in flight (only after a failed wait): let them land before the CTA leaves
-      for (int back = 1; back <= TC_NS && back <= it; ++back)
-        mbar_wait(&full_tma[(it - back) % TC_NS], (uint32_t)(((it - back) / TC_NS) & 1), status);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      int it = 0, ti = 0;
-      for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x, ++ti) {
-        const TcTile tl = p.tiles[item / RT_D];
-        const int nrows = (tl.n + 15) / 16 * 16;
-        const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
-        if (ti > 0 && !mbar_wait(&tmem_empty, (uint32_t)((ti - 1) & 1), status)) { s_fail = 1; break; }
-        tc::fence_after_sync();
-        for (int kb = 0; kb < KB_D; ++kb, ++it) {
-          const int s = it % TC_NS;
-          const uint32_t par = (uint32_t)((it / TC_NS) & 1);
-          if (!mbar_wait(&full_tma[s], par, status) || !mbar_wait(&full_a[s], par, status)) { s_fail = 1; break; }
-          tc::fence_after_sync();
-          uint8_t* st = smem + s * DnPlan::BYTES;
-          const uint64_t ad = tc::smem_desc_sw128(smem_u32(st + DnPlan::A_OFF));
-          const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + DnPlan::B_OFF));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&empty[s]);
-        }
-        if (s_fail) break;
-        tc::mma_commit(&tmem_full);
-      }
-      // every MMA this thread issued has finished before TMEM is released
-      tc::mma_commit(&mma_done);
-      mbar_wait(&mma_done, 0u, status);
-    }
-  } else if (warp >= 4) {
-    const int dt = tid - 128;
-    const int row = dt & 127, half = dt >> 7;  // dequant: each thread writes 4 of the row's 8 chunks
-    const int ew = warp - 4;
-    const int erow = 32 * (warp & 3) + lane;
-    const int ehalf = ew >> 2;
-    int it = 0, ti = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ti) {
-      const TcTile tl = p.tiles[item / RT_D];
-      const int rtd = item % RT_D;
-      const int nrows = (tl.n + 15) / 16 * 16;
-      bool ok = true;
-      for (int kb = 0; kb < KB_D; ++kb, ++it) {
-        const int s = it % TC_NS;
-        uint8_t* st = smem + s * DnPlan::BYTES;
-        if (it >= TC_NS) ok = ok && mbar_wait(&empty[s], (uint32_t)((it / TC_NS - 1) & 1), status);
-        ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / TC_NS) & 1), status);
-        if (ok) {
-          const uint4 cw = *reinterpret_cast<const uint4*>(st + DnPlan::C_OFF + 16 * row);
-          const __half d = *reinterpret_cast<const __half*>(st + DnPlan::C_OFF + 2048 + 2 * row);
-          dequant_row(cw, d, p.q2_offset, st + DnPlan::A_OFF, row, 4 * half, 4);
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full_a[s]);
-      }
-      ok = ok && mbar_wait(&tmem_full, (uint32_t)(ti & 1), status);
-      tc::fence_after_sync();
-      const int nch = nrows / 16;
-      const int ch0 = ehalf ? (nch + 1) / 2 : 0, ch1 = ehalf ? nch : (nch + 1) / 2;
-      const int orow = rtd * 128 + erow;
-      for (int ch = ch0; ch < ch1; ++ch) {
-        float y[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * ch, y);
-        if (ok) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = 16 * ch + i;
-            if (col < tl.n) p.parts[(size_t)p.pair[tl.q0 + col] * H + orow] = y[i];
-          }
-        }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tmem_empty);
-    }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 2) tc::tmem_dealloc(tmem, 128);
-  if (warp == 2) tc::tmem_relinquish();
 }
 
 int g_sms[64];
@@ -462,7 +409,8 @@ size_t tc_meta_bytes(int T) {
   return sizeof(TcExpert) * EMAX + sizeof(TcTile) * (size_t)(T * K / TCN + EMAX) + 64;
 }
 
-cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, int T, const int32_t* expert_off,
+cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
+                              const int32_t* expert_off,
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
                               uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s) {
   const int max_tiles = T * K / TCN + EMAX;
@@ -470,8 +418,11 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, int T,
   TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * EMAX);
   int32_t* counts = reinterpret_cast<int32_t*>(meta + sizeof(TcExpert) * EMAX + sizeof(TcTile) * max_tiles);
   const int64_t rows_cap = tc_rows_cap(T);
-  tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, exps, tiles, counts, max_tiles);
-  tc_gather_kernel<<<dim3(256, KB_GU), 256, 0, s>>>(x, pair, exps, counts, xg, rows_cap);
+  STRATA_LAUNCH(KID_TC_PREPARE, s,
+                tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, exps, tiles, counts,
+                                                    max_tiles));
+  STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, exps, counts, xg,
+                                                                                   rows_cap));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   int dev = 0;
@@ -481,18 +432,19 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, int T,
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) g_sms[dev] = sms;
   }
-  TcGuParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, status};
-  const size_t gsmem = (size_t)TC_NS * GuPlan::BYTES + 1024;
-  if ((err = cudaFuncSetAttribute(gu_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem)) != cudaSuccess)
+  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, parts,
+              status};
+  if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)TcGeo<true>::SMEM)) != cudaSuccess)
     return err;
-  gu_tc_kernel<<<sms, GU_THREADS, gsmem, s>>>(gp);
+  STRATA_LAUNCH(KID_TC_GATEUP, s, tc_expert_kernel<true><<<sms, TC_THREADS, TcGeo<true>::SMEM, s>>>(gp));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  TcDnParams dp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, hg, rows_cap, pair, parts, status};
-  const size_t dsmem = (size_t)TC_NS * DnPlan::BYTES + 1024;
-  if ((err = cudaFuncSetAttribute(down_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsmem)) !=
-      cudaSuccess)
+  TcParams dp = gp;
+  dp.act = hg;
+  if ((err = cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)TcGeo<false>::SMEM)) != cudaSuccess)
     return err;
-  down_tc_kernel<<<sms, DN_THREADS, dsmem, s>>>(dp);
+  STRATA_LAUNCH(KID_TC_DOWN, s, tc_expert_kernel<false><<<sms, TC_THREADS, TcGeo<false>::SMEM, s>>>(dp));
   return cudaGetLastError();
 }
 

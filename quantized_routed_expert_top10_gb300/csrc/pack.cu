@@ -53,7 +53,9 @@ __global__ void pack_kernel(const uint8_t* __restrict__ canonical, int64_t src_s
 cudaError_t launch_pack_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed, int64_t dst_stride,
                                int64_t n_blobs, cudaStream_t s) {
   const int64_t total = n_blobs * kBlocks;
-  pack_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(canonical, src_stride, packed, dst_stride, n_blobs);
+  STRATA_LAUNCH(KID_PACK, s,
+                pack_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(canonical, src_stride, packed, dst_stride,
+                                                                           n_blobs));
   return cudaGetLastError();
 }
 

@@ -183,33 +183,58 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
   __syncthreads();
   finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
   __syncthreads();
-  if (warp == 0) stable_scatter_warp(ids, 0, P, E, s_off, pair);
+  if (warp == 0) stable_scatter_warp(ids, 0, P, E, s_off, pair, 0);
   if (tid == 0) *counter = 0;
 }
 
 // ---------------------------------------------------------------------------------------------
 // Prefill routing kernels.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, float* __restrict__ xn) {
-  __shared__ float s_red[8];
-  const int t = blockIdx.x;
-  const float* xr = x + (size_t)t * H;
+// 1/rms of each token row for the residual layers' rmsnorm: inv[t] = 1 / sqrt(mean(x[t]^2) + 1e-6).
+// One warp per row; the consumers (router GEMM, token gather) scale x by it as they read it.
+__global__ void __launch_bounds__(256) inv_rms_kernel(const float* __restrict__ x, int T, float* __restrict__ inv) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
   float ss = 0.f;
-  for (int h = threadIdx.x; h < H; h += 256) { const float v = xr[h]; ss += v * v; }
+#pragma unroll 4
+  for (int i = lane; i < H / 4; i += 32) {
+    const float4 v = __ldg(xr + i);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
   ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) tot += s_red[w];
-  const float inv = 1.f / sqrtf(tot / (float)H + 1e-6f);
-  for (int h = threadIdx.x; h < H; h += 256) xn[(size_t)t * H + h] = xr[h] * inv;
+  if (lane == 0) inv[t] = 1.f / sqrtf(ss / (float)H + 1e-6f);
 }
 
-__global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ logits, int ld, int T, int E,
+// Logits of token t = the router GEMM's ROUTER_KSPLIT partial sums added in a fixed order, plus the
+// bias; then the top-10 of the token (one warp per token).
+__global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ parts, int T, int E,
+                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids, float* __restrict__ weights) {
-  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (t < T) top_k_warp(logits + (size_t)t * ld, E, ids + t * K, weights + t * K);
+  static_assert(ROUTER_KSPLIT == 4, "the fixed summation order below assumes four slices");
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const size_t slice = (size_t)T * EMAX;
+  const float* p = parts + (size_t)t * EMAX;
+  float lg[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int e = lane + 32 * j;
+    float v = 0.f;
+    if (e < E) {
+      v = (__ldcg(p + e) + __ldcg(p + slice + e)) + (__ldcg(p + 2 * slice + e) + __ldcg(p + 3 * slice + e));
+      if (bias) v += __ldg(bias + e);
+      if (logits_out) logits_out[(size_t)t * E + e] = v;
+    }
+    lg[j] = v;
+  }
+  int id;
+  float w;
+  top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, &id, &w);
+  if (lane < K) {
+    ids[t * K + lane] = id;
+    weights[t * K + lane] = w;
+  }
 }
 
 __global__ void __launch_bounds__(256) group_hist_kernel(const int32_t* __restrict__ ids, int P, int E,
@@ -249,17 +274,20 @@ __global__ void __launch_bounds__(512) group_scan_kernel(int n_chunks, int E, in
   finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
 }
 
-// One warp per chunk: stable scatter starting from expert_off[e] + chunk base.
+// One warp per chunk: the chunk's ids staged in shared memory with independent loads, then the
+// stable scatter starting from expert_off[e] + chunk base.
 __global__ void __launch_bounds__(32) group_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                            const int32_t* __restrict__ chunk_cnt,
                                                            const int32_t* __restrict__ expert_off,
                                                            int32_t* __restrict__ pair) {
   __shared__ int fill[EMAX];
+  __shared__ int s_ids[GROUP_CHUNK];
   for (int i = threadIdx.x; i < E; i += 32)
     fill[i] = expert_off[i] + chunk_cnt[(size_t)blockIdx.x * EMAX + i];
-  __syncwarp();
   const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
-  stable_scatter_warp(ids, p0, p1, E, fill, pair);
+  for (int p = p0 + (int)threadIdx.x; p < p1; p += 32) s_ids[p - p0] = __ldg(ids + p);
+  __syncwarp();
+  stable_scatter_warp(s_ids, 0, p1 - p0, E, fill, pair, p0);
 }
 
 // Tiles from a caller-provided grouping (strata_moe_experts): one CTA.  The arrays come from the
@@ -329,21 +357,25 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
       (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair), (int32_t*)(ws + L.active),              \
       (int32_t*)(ws + L.n_active), (Tile*)(ws + L.tiles), L.max_tiles, (QBlock*)(ws + L.qx),           \
       (int*)(ws + L.cnt_route), (int*)(ws + L.status)
+  kernel_begin(KID_ROUTE_DECODE, s);
   if (T <= 1) route_decode_kernel<1><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
   else if (T <= 2) route_decode_kernel<2><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
   else if (T <= 4) route_decode_kernel<4><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
   else route_decode_kernel<8><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
+  kernel_end(KID_ROUTE_DECODE, s);
 #undef STRATA_ROUTE_ARGS
   return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm(const float* x, int T, float* xn, cudaStream_t s) {
-  rmsnorm_kernel<<<T, 256, 0, s>>>(x, xn);
+cudaError_t launch_inv_rms(const float* x, int T, float* inv_rms, cudaStream_t s) {
+  STRATA_LAUNCH(KID_RMSNORM, s, inv_rms_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, inv_rms));
   return cudaGetLastError();
 }
 
-cudaError_t launch_top_k(const float* logits, int T, int E, int32_t* ids, float* weights, cudaStream_t s) {
-  top_k_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, E, T, E, ids, weights);
+cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, float* logits_out, int32_t* ids,
+                         float* weights, cudaStream_t s) {
+  STRATA_LAUNCH(KID_TOP_K, s,
+                top_k_kernel<<<(T + 3) / 4, 128, 0, s>>>(parts, T, E, bias, logits_out, ids, weights));
   return cudaGetLastError();
 }
 
@@ -352,24 +384,29 @@ cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, 
   const int P = T * K;
   int32_t* chunk_cnt = (int32_t*)(ws + L.chunk_cnt);
   int32_t* nat = (int32_t*)(ws + L.n_active);
-  group_hist_kernel<<<L.n_chunks, 256, 0, s>>>(ids, P, E, chunk_cnt, (int*)(ws + L.status));
-  group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat, (Tile*)(ws + L.tiles),
-                                      L.max_tiles);
-  group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair);
+  STRATA_LAUNCH(KID_GROUP_HIST, s,
+                group_hist_kernel<<<L.n_chunks, 256, 0, s>>>(ids, P, E, chunk_cnt, (int*)(ws + L.status)));
+  STRATA_LAUNCH(KID_GROUP_SCAN, s,
+                group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat,
+                                                    (Tile*)(ws + L.tiles), L.max_tiles));
+  STRATA_LAUNCH(KID_GROUP_SCATTER, s,
+                group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
   if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
                                int T, const WsLayout& L, char* ws, cudaStream_t s) {
-  build_tiles_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, E, T * K, (int32_t*)(ws + L.n_active),
-                                       (Tile*)(ws + L.tiles), L.max_tiles, (int*)(ws + L.status));
+  STRATA_LAUNCH(KID_BUILD_TILES, s,
+                build_tiles_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, E, T * K,
+                                                     (int32_t*)(ws + L.n_active), (Tile*)(ws + L.tiles), L.max_tiles,
+                                                     (int*)(ws + L.status)));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s) {
   const int nblk = T * KB_GU;
-  quantise_x_kernel<<<(nblk + 3) / 4, 128, 0, s>>>(x, T, q2_offset, qx);
+  STRATA_LAUNCH(KID_QUANTISE_X, s, quantise_x_kernel<<<(nblk + 3) / 4, 128, 0, s>>>(x, T, q2_offset, qx));
   return cudaGetLastError();
 }
 

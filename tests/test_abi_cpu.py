@@ -31,7 +31,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 18
     assert sorted(names) == sorted(qre.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -143,3 +143,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qre, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         qre.lib()
+
+
+def test_profile_arm_argument_checks(lib):
+    assert lib.strata_moe_profile_arm(-1, 0, None, None, 0) == -1
+    assert lib.strata_moe_profile_arm(qre.KERNEL_ID["TC_GATEUP"], 0, None, None, 2) == -1
+    assert lib.strata_moe_profile_arm(qre.KERNEL_ID["TC_GATEUP"], -1, None, None, 0) == -1
+    assert lib.strata_moe_profile_arm(qre.KERNEL_ID["TC_GATEUP"], 0, None, None, 0) == 0
+    assert lib.strata_moe_profile_recorded(qre.KERNEL_ID["TC_GATEUP"]) == 0
+    assert lib.strata_moe_profile_recorded(len(qre.KERNELS)) == -1
+    assert lib.strata_moe_launch_count() >= 0
+
+
+def test_kernel_ids_match_header():
+    src = open(HEADER).read()
+    ids = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"#define STRATA_KERNEL_([A-Z_]+) (\d+)", src))
+    assert ids.pop("COUNT") == len(qre.KERNELS)
+    assert ids == qre.KERNEL_ID
