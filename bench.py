@@ -220,13 +220,37 @@ def measure_gb300(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
 
+    # Decode steps (T <= 8: one cooperative launch per layer) would be bound by the host's launch
+    # rate, so the step is captured once in a CUDA graph and replayed; prefill steps run eagerly.
+    graph, graph_launches, graph_note = None, None, "eager launches"
+    if T <= 8:
+        try:
+            n0 = qre.strata_moe_launch_count()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
+            graph_launches = qre.strata_moe_launch_count() - n0
+            for _ in range(W):
+                graph.replay()
+            torch.cuda.synchronize()
+            st = qre.strata_poll_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
+            graph_note = "CUDA graph replay of the step"
+        except Exception as exc:  # capture refused: fall back to eager launches, and say so
+            graph, graph_launches = None, None
+            graph_note = f"eager launches (graph capture failed: {str(exc)[:120]})"
+            torch.cuda.synchronize()
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     # Dominant-kernel timing inside the timed region: T <= 8 and one layer -> the step is exactly one
-    # launch of the decode layer kernel (its events are the step's); T <= 8 stacks -> one layer per
-    # step, rotating over the layers (every launch would add event records between the 48 launches);
-    # prefill -> every launch of the two tensor-core expert kernels.
-    timed = () if T <= 8 and L == 1 else ("DECODE_LAYER",) if T <= 8 else ("TC_GATEUP", "TC_DOWN")
+    # launch of the decode layer kernel (its events are the step's); T <= 8 stacks -> replayed as a
+    # graph: the step time over its L launches (an upper bound on the kernel's duration), or, run
+    # eagerly, library event hooks around one layer per step; prefill -> every launch of the two
+    # tensor-core expert kernels.
+    timed = () if (T <= 8 and (L == 1 or graph is not None)) else ("DECODE_LAYER",) if T <= 8 \
+        else ("TC_GATEUP", "TC_DOWN")
     per_step = 1 if T <= 8 else L
     kev = {}
     for k in timed:
@@ -253,11 +277,14 @@ def measure_gb300(args, rank, world, local_rank):
             elif i == 0:
                 armed[k] = qre.strata_moe_profile_arm(k, *kev[k])
         starts[i].record(stream)
-        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
+        if graph is not None:
+            graph.replay()
+        else:
+            run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    n_launches = qre.strata_moe_launch_count() - launches0
+    n_launches = graph_launches * K if graph is not None else qre.strata_moe_launch_count() - launches0
     kernel_ms = {}
     for k in timed:
         kernel_ms[k] = [a.elapsed_time(b) for a, b in zip(*kev[k])]
@@ -265,6 +292,8 @@ def measure_gb300(args, rank, world, local_rank):
     del armed
     if T <= 8 and L == 1:
         kernel_ms["DECODE_LAYER"] = step_ms_list(starts, ends)
+    elif T <= 8 and graph is not None:
+        kernel_ms["DECODE_LAYER"] = [m / L for m in step_ms_list(starts, ends) for _ in range(L)]
     if wall < 1.0:
         time.sleep(0.3)
     clk = clocks.stop()
@@ -283,7 +312,8 @@ def measure_gb300(args, rank, world, local_rank):
     value = world * T * K / (total_ms / 1e3)
 
     # ---- dominant kernel ----
-    roof = kernel_roofline(cfg, kernel_ms, K, ids_all_h if L > 1 else ids_h[None])
+    roof = kernel_roofline(cfg, kernel_ms, K, ids_all_h if L > 1 else ids_h[None],
+                           graph_stack=T <= 8 and L > 1 and graph is not None)
     if T > 8:
         roof["kernel_ms_per_step"] = step_breakdown(qre, run_step, (qre, cfg, exs, wr, bias, x_in, x_work, out, ids,
                                                                    ids_all, ws), stream, L)
@@ -305,8 +335,8 @@ def measure_gb300(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": path_dtype(T),
         "data": "synthetic (seeded Philox4x32-10 inputs; random Q2_0 experts; no trained weights)",
-        "config": workload_config(cfg, args.seed, world, need_flush,
-                                  int(len(np.unique(ids_h))) if L == 1 else None),
+        "config": dict(workload_config(cfg, args.seed, world, need_flush,
+                                       int(len(np.unique(ids_h))) if L == 1 else None), launch=graph_note),
         "roofline": roof,
         "clocks": clk,
         "e2e": e2e,
@@ -369,7 +399,7 @@ def workload_config(cfg, seed, world, need_flush, distinct):
     }
 
 
-def kernel_roofline(cfg, kernel_ms, K, ids_layers):
+def kernel_roofline(cfg, kernel_ms, K, ids_layers, graph_stack=False):
     """Roofline of the dominant kernel from the per-launch event times taken in the timed region.
 
     decode layer (T <= 8): HBM-bound; algorithmic bytes per launch = router rows (512 x 2560 bf16) +
@@ -397,7 +427,8 @@ def kernel_roofline(cfg, kernel_ms, K, ids_layers):
                 "algorithmic_bytes_per_launch": per_launch, "distinct_experts_per_layer": float(np.mean(d)),
                 "avg_launch_ms": avg_ms, "launches_timed": len(ms),
                 "timing": "step events (one launch per step)" if L == 1 else
-                "library event hooks around one layer per step (layer = step % 48)"}
+                "step events / 48 (graph replay of the 48 launches; includes the gaps between them)"
+                if graph_stack else "library event hooks around one layer per step (layer = step % 48)"}
     peak = tc_burst if L == 1 else tc_sust
     flops = T * 10 * FLOPS_PER_PAIR[dom]
     achieved = flops / (avg_ms / 1e3) / 1e12

@@ -32,15 +32,17 @@
  *     reusable.  Two calls that share a ws must not overlap in time (same stream, or ordered).
  *
  * Packed expert blob ("GPU layout", written by strata_pack_q2_0*; same 1,382,400 bytes as the
- * canonical blob, every chunk 256-byte aligned when the blob is):
+ * canonical blob; every piece starts on a 16-byte boundary when the blob is 256-byte aligned):
  *   canonical: gate [640][2560], up [640][2560], down [2560][640], each row-major, as Q2_0 blocks of
  *     64 consecutive weights {fp16 d, 16 code bytes}; weight i of a block in code byte i/4 at bits
  *     2*(i%4); value d * (c - q2_offset).
- *   packed gate/up region, bytes [0, 921600): for row tile rt = 0..4 (rows 128*rt ..), for k-block
- *     kb = 0..39, a 4608-byte chunk at (rt*40 + kb)*4608:
- *        [0, 2048)    gate codes of the tile's 128 rows, 16 bytes per row, row order
- *        [2048, 4096) up codes, same order
- *        [4096, 4608) per row r: {fp16 gate d, fp16 up d} at 4096 + 4*r
+ *   packed gate/up region, bytes [0, 921600): for slab s = 0..39 (rows 16*s .. 16*s + 15 of gate and
+ *     up), for k-block kb = 0..39, a 576-byte piece at (s*40 + kb)*576:
+ *        [0, 256)     gate codes of the slab's 16 rows, 16 bytes per row, row order
+ *        [256, 512)   up codes, same order
+ *        [512, 576)   per row r: {fp16 gate d, fp16 up d} at 512 + 4*r
+ *     so one slab (all 40 k-blocks, 23,040 bytes) is contiguous, and the 8 pieces of one k-block of
+ *     a 128-row tile sit 23,040 bytes apart.
  *   packed down region, bytes [921600, 1382400): for row tile rt = 0..19, kb = 0..9, a 2304-byte
  *     chunk at 921600 + (rt*10 + kb)*2304: [0, 2048) codes of 128 rows, [2048, 2304) fp16 d per row.
  *   Code bytes keep the canonical in-block order.
@@ -132,7 +134,10 @@ strata_status strata_moe_group_noalloc(const int32_t* ids, int32_t T, int32_t n_
 
 /* Step 4. For every pair p = t*10 + k listed by the grouping: parts[p][:] = expert(x[t]) with the
  * expert that owns p.  x fp32 [T][2560]; grouping arrays as strata_moe_group writes them; parts
- * fp32 [T][10][2560].  Weights are the packed blobs of ex (host pointer to the struct). */
+ * fp32 [T][10][2560].  Weights are the packed blobs of ex (host pointer to the struct).  Computed
+ * as grouped tensor-core GEMMs (x rounded to fp16, fp32 accumulation) for every T.  The grouping
+ * arrays are checked on the device: an expert id outside [0, n_expert), a slot range outside
+ * [0, T*10) or a pair number outside [0, T*10) sets STRATA_E_CORRUPT and that entry is skipped. */
 strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int32_t T,
                                  const int32_t* expert_off, const int32_t* pair, const int32_t* active,
                                  const int32_t* n_active, float* parts, void* ws, size_t ws_bytes,
@@ -190,17 +195,13 @@ const char* strata_status_str(strata_status s);
 #define STRATA_KERNEL_GROUP_HIST 5
 #define STRATA_KERNEL_GROUP_SCAN 6
 #define STRATA_KERNEL_GROUP_SCATTER 7
-#define STRATA_KERNEL_BUILD_TILES 8
-#define STRATA_KERNEL_QUANTISE_X 9
-#define STRATA_KERNEL_GEMV_GATEUP 10   /* Q2_0 gate/up + SwiGLU GEMV, T <= 8 (strata_moe_experts) */
-#define STRATA_KERNEL_GEMV_DOWN 11
-#define STRATA_KERNEL_TC_PREPARE 12    /* tile list of the tensor-core expert path, T > 8 */
-#define STRATA_KERNEL_TC_GATHER 13     /* fp16 token gather per expert */
-#define STRATA_KERNEL_TC_GATEUP 14     /* Q2_0 gate/up + SwiGLU grouped GEMM (tcgen05) */
-#define STRATA_KERNEL_TC_DOWN 15       /* Q2_0 down grouped GEMM (tcgen05) */
-#define STRATA_KERNEL_COMBINE 16
-#define STRATA_KERNEL_PACK 17
-#define STRATA_KERNEL_COUNT 18
+#define STRATA_KERNEL_TC_PREPARE 8     /* tile list of the tensor-core expert path */
+#define STRATA_KERNEL_TC_GATHER 9      /* fp16 token gather per expert */
+#define STRATA_KERNEL_TC_GATEUP 10     /* Q2_0 gate/up + SwiGLU grouped GEMM (tcgen05) */
+#define STRATA_KERNEL_TC_DOWN 11       /* Q2_0 down grouped GEMM (tcgen05) */
+#define STRATA_KERNEL_COMBINE 12
+#define STRATA_KERNEL_PACK 13
+#define STRATA_KERNEL_COUNT 14
 
 /* Number of kernels this process has launched through the library so far (all threads). */
 uint64_t strata_moe_launch_count(void);

@@ -166,14 +166,8 @@ strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int
   const WsLayout L = ws_layout(T);
   char* w = (char*)ws;
   cudaStream_t s = (cudaStream_t)stream;
-  if (T > DECODE_T_MAX) {
-    STRATA_CUDA(launch_experts_tc(*ex, x, nullptr, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
-                                  (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
-    return STRATA_OK;
-  }
-  STRATA_CUDA(launch_build_tiles(expert_off, active, n_active, ex->n_expert, T, L, w, s));
-  STRATA_CUDA(launch_quantise_x(x, T, ex->q2_offset, (QBlock*)(w + L.qx), s));
-  STRATA_CUDA(launch_experts_gemv(*ex, T, pair, L, w, parts, s));
+  STRATA_CUDA(launch_experts_tc(*ex, x, nullptr, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
+                                (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
   return STRATA_OK;
 }
 

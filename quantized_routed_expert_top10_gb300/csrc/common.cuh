@@ -19,18 +19,22 @@ constexpr int EMAX = STRATA_MOE_E_MAX;
 constexpr int TMAX = STRATA_MOE_T_MAX;
 constexpr int KB_GU = H / QK;  // 40 k-blocks along gate/up's contraction
 constexpr int KB_D = FF / QK;  // 10 k-blocks along down's contraction
-constexpr int RT = 128;        // rows per packed row tile
+constexpr int RT = 128;        // rows per row tile
 constexpr int RT_GU = FF / RT; // 5 gate/up row tiles
 constexpr int RT_D = H / RT;   // 20 down row tiles
-constexpr int GU_CHUNK = 4608; // bytes per (rt, kb) gate+up chunk
+// Packed gate/up region: slabs of 16 rows; per (slab, kb) a 576-byte piece (gate codes of the 16
+// rows, up codes, {gate d, up d} per row); a slab's 40 pieces are contiguous (23,040 bytes).
+constexpr int SLAB = 16;                  // rows per gate/up slab
+constexpr int N_SLAB = FF / SLAB;         // 40 slabs
+constexpr int SLAB_KB = 576;              // bytes per (slab, kb) piece
+constexpr int SLAB_BYTES = KB_GU * SLAB_KB;  // 23,040 bytes per slab
+constexpr int GU_CHUNK = (RT / SLAB) * SLAB_KB;  // 4,608 bytes: one kb of a 128-row tile (8 pieces)
 constexpr int D_CHUNK = 2304;  // bytes per (rt, kb) down chunk
 constexpr int64_t D_REGION = 921600;
 constexpr int64_t BLOB = STRATA_MOE_BLOB_BYTES;
 
-// GEMV expert path: up to NT tokens of one expert per tile; the gate/up contraction is split
-// S_SPLIT ways when the call is small (decode), so enough CTAs stream the weights.
+// Grouping tiles (finish_grouping): up to NT slots of one expert per tile.
 constexpr int NT = 8;
-constexpr int S_SPLIT = 4;
 constexpr int ROUTER_KSPLIT = 4;  // prefill router: splits of the 2,560-term contraction over CTAs
 constexpr int DECODE_T_MAX = 8;  // T <= this: fused single-kernel routing (router + top-10 + grouping)
 
@@ -63,15 +67,12 @@ struct __align__(16) Tile {
 constexpr size_t WS_HEADER = 12288;
 constexpr size_t WS_STATUS = 0;     // int32 status word
 constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
-constexpr size_t WS_CNT_GU = 256;   // int32 [max_tiles(DECODE_T_MAX)][RT_GU] split counters
 // Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): grid barrier, exit
-// counter, per (expert slot, gate/up row tile) split counters, per expert slot h-ready counters,
-// per down row tile counters.
+// counter, per expert slot h counters (finished gate/up slabs), per down row tile counters.
 constexpr size_t WS_SYNC = 4096;
 constexpr int WS_SYNC_BAR = 0;
 constexpr int WS_SYNC_EXIT = 1;
-constexpr int WS_SYNC_CNT_GU = 16;
-constexpr int WS_SYNC_HREADY = WS_SYNC_CNT_GU + DECODE_T_MAX * K * RT_GU;
+constexpr int WS_SYNC_HREADY = 16;
 constexpr int WS_SYNC_CNT_DN = WS_SYNC_HREADY + DECODE_T_MAX * K;
 constexpr int WS_SYNC_REL = ((WS_SYNC_CNT_DN + RT_D + 31) / 32) * 32;  // barrier release flags, one per 128-B line
 constexpr int WS_NREP = 16;                          // replicas of data every CTA reads at once
@@ -79,7 +80,7 @@ constexpr int WS_SYNC_WORDS = WS_SYNC_REL + 32 * WS_NREP;
 static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sync words must fit the header");
 
 struct WsLayout {
-  size_t status, cnt_route, cnt_gu;
+  size_t status, cnt_route;
   size_t logits;      // fp32 [ROUTER_KSPLIT][T][EMAX] partial router logits (T > DECODE_T_MAX: one slice per
                       // split of the contraction; the decode path uses slice 0 as [T][EMAX] logits)
   size_t ids;         // int32 [T][K]
@@ -93,11 +94,10 @@ struct WsLayout {
   size_t n_active;    // int32 [4]: n_active, n_tiles
   size_t tiles;       // Tile [max_tiles]
   size_t chunk_cnt;   // int32 [n_chunks][EMAX]
-  size_t qx;          // QBlock [T][KB_GU]
-  size_t partial;     // fp32 [max_tiles][RT_GU][S_SPLIT][NT][RT][2] (decode split-K partials)
-  size_t hq;          // QBlock [T*K][KB_D]
+  size_t qx;          // QBlock [T][KB_GU] quantised layer input (one-kernel decode layer)
+  size_t hf;          // fp32 [min(T, DECODE_T_MAX) * K][FF] h of each pair (one-kernel decode layer)
   size_t parts;       // fp32 [T*K][H]
-  size_t xg;          // tensor-core path (T > DECODE_T_MAX): gathered fp16 tokens [KB_GU][rows][128 B]
+  size_t xg;          // tensor-core expert path: gathered fp16 tokens [KB_GU][rows][128 B]
   size_t hg;          //                                      fp16 h [KB_D][rows][128 B]
   size_t tcmeta;      //                                      expert ranges, tiles, counts
   size_t total;
@@ -129,7 +129,6 @@ inline WsLayout ws_layout(int T) {
   if (L.n_chunks < 1) L.n_chunks = 1;
   L.status = WS_STATUS;
   L.cnt_route = WS_CNT_ROUTE;
-  L.cnt_gu = WS_CNT_GU;
   size_t o = WS_HEADER;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
   L.logits = take(sizeof(float) * (size_t)ROUTER_KSPLIT * T * EMAX);
@@ -147,18 +146,14 @@ inline WsLayout ws_layout(int T) {
   L.qx = take(sizeof(QBlock) * (size_t)T * KB_GU);
   // sized for min(T, DECODE_T_MAX) so the total grows with T (a workspace sized for T serves any T' <= T)
   const int Td = T < DECODE_T_MAX ? T : DECODE_T_MAX;
-  L.partial = take(sizeof(float) * (size_t)max_tiles_for(Td) * RT_GU * S_SPLIT * NT * RT * 2);
-  L.hq = take(sizeof(QBlock) * (size_t)P * KB_D);
+  L.hf = take(sizeof(float) * (size_t)Td * K * FF);
   L.parts = take(sizeof(float) * (size_t)P * H);
-  L.xg = take(T > DECODE_T_MAX ? tc_xg_bytes(T) : 0);
-  L.hg = take(T > DECODE_T_MAX ? tc_hg_bytes(T) : 0);
-  L.tcmeta = take(T > DECODE_T_MAX ? tc_meta_bytes(T) : 0);
+  L.xg = take(tc_xg_bytes(T));
+  L.hg = take(tc_hg_bytes(T));
+  L.tcmeta = take(tc_meta_bytes(T));
   L.total = T > 0 ? o : WS_HEADER;
   return L;
 }
-static_assert(WS_CNT_GU + sizeof(int32_t) * (size_t)(DECODE_T_MAX * K / NT + DECODE_T_MAX * K) * RT_GU <= WS_HEADER,
-              "decode split counters must fit in the workspace header");
-
 // ---------------------------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------------------------
@@ -263,8 +258,7 @@ namespace strata {
 // it and record the caller's armed timing events around it.  Ids equal the ABI's STRATA_KERNEL_*.
 enum KernelId : int {
   KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_RMSNORM, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
-  KID_GROUP_SCATTER, KID_BUILD_TILES, KID_QUANTISE_X, KID_GEMV_GATEUP, KID_GEMV_DOWN, KID_TC_PREPARE,
-  KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_COUNT
+  KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_COUNT
 };
 void kernel_begin(int kid, cudaStream_t s);
 void kernel_end(int kid, cudaStream_t s);
@@ -285,11 +279,6 @@ cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, fl
                          float* weights, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair,
                          int32_t* active, int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s);
-cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
-                               int T, const WsLayout& L, char* ws, cudaStream_t s);
-cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s);
-cudaError_t launch_experts_gemv(const strata_experts_t& ex, int T, const int32_t* pair, const WsLayout& L,
-                                char* ws, float* parts, cudaStream_t s);
 cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
                               const int32_t* expert_off, const int32_t* pair, const int32_t* active,
                               const int32_t* n_active, float* parts,

@@ -10,14 +10,17 @@
 //      into hi/lo bytes, see QBlock) and their sums of squares (for the rmsnorm of residual layers);
 //   2. one grid barrier; then every CTA redundantly computes the top-10 of all tokens and the
 //      grouping in shared memory (identical results everywhere, no second barrier);
-//   3. the expert bytes are cut into equal 23,040-byte units -- gate/up units (expert, 128-row tile,
-//      5 of the 40 k-blocks) and down units (expert, 128-row tile, all 10 k-blocks) -- dealt round
-//      robin to the CTAs, gate/up units first.  Each CTA streams its units through a ring of shared
-//      memory stages with cp.async.bulk (L2 evict-first) as soon as routing is known;
-//   4. the last of the 8 CTAs of a gate/up row tile adds the partial sums in split order, applies
-//      silu(g) * u, quantises h and bumps the expert's h counter; a down unit waits (bounded) until
-//      its expert's five row tiles of h are ready; the last down unit of each output row tile
-//      combines the ten weighted expert outputs of every token in k order (+ the residual).
+//   3. right after the barrier each CTA copies every token's quantised activations into shared
+//      memory (one bulk copy, overlapping the top-k); the expert bytes are cut into equal
+//      23,040-byte units -- gate/up units (expert, slab of 16 rows, all 40 k-blocks: contiguous in
+//      the packed blob) and down units (expert, 128-row tile, all 10 k-blocks) -- dealt round robin
+//      to the CTAs, gate/up units first.  Each CTA streams its units through a ring of shared memory
+//      stages with cp.async.bulk (L2 evict-first) as soon as routing is known;
+//   4. a gate/up unit finishes g and u of its 16 rows for the expert's tokens (8 thread groups of 5
+//      k-blocks, added in group order), writes h = silu(g) * u and bumps the expert's h counter; a
+//      down unit waits (bounded) until all 40 slabs of its expert are in, quantises h itself, and the
+//      last down unit of each output row tile combines the ten weighted expert outputs of every
+//      token in k order (+ the residual).
 // All waits are bounded by %globaltimer and record STRATA_E_TIMEOUT in the status word.  The last CTA
 // to leave resets the counters, so the workspace is ready for the next call.
 #include "device_common.cuh"
@@ -25,15 +28,21 @@
 namespace strata {
 namespace {
 
-constexpr int DF_NS = 3;                       // ring stages per CTA
 constexpr int DF_UNIT = 23040;                 // bytes per work unit
-constexpr int DF_SGU = 8;                      // gate/up k-splits
-constexpr int DF_KBU = KB_GU / DF_SGU;         // 5 k-blocks per gate/up unit
-constexpr int DF_GU = RT_GU * DF_SGU;          // 40 gate/up units per expert
+constexpr int DF_GU = N_SLAB;                  // 40 gate/up units (slabs) per expert
 constexpr int DF_DN = RT_D;                    // 20 down units per expert
 constexpr int DF_MAXD = DECODE_T_MAX * K;      // at most 80 distinct experts
 constexpr int DF_THREADS = 128;
-static_assert(DF_KBU * GU_CHUNK == DF_UNIT && KB_D * D_CHUNK == DF_UNIT, "equal unit sizes");
+constexpr int DF_KG = DF_THREADS / SLAB;       // 8 k-block groups per gate/up unit
+constexpr int DF_KBG = KB_GU / DF_KG;          // 5 k-blocks per group
+static_assert(SLAB_BYTES == DF_UNIT && KB_D * D_CHUNK == DF_UNIT, "equal unit sizes");
+// Ring stages per CTA: three, or two when eight tokens' activations take the shared memory.
+template <int TT>
+__host__ __device__ constexpr int df_stages() { return TT <= 4 ? 3 : 2; }
+template <int TT>
+constexpr size_t df_smem() {
+  return (size_t)df_stages<TT>() * DF_UNIT + sizeof(QBlock) * (size_t)(TT * KB_GU + KB_D * TT);
+}
 
 struct DecodeParams {
   const float* x;  // [T][H] layer input (may alias out)
@@ -48,8 +57,7 @@ struct DecodeParams {
   float* dots;       // ws [WS_NREP][T][EMAX] raw router dot products, replicated
   float* sumsq;      // ws [WS_NREP][T][KB_GU], replicated
   QBlock* qx;        // ws [T][KB_GU]
-  QBlock* hq;        // ws [T*K][KB_D]
-  float* partial;    // ws [RT_GU*DF_SGU][T*K][RT] float2
+  float* hf;         // ws [T*K][FF] h of each pair, in slot order
   float* parts;      // ws [T*K][H]
   int* sync;         // ws sync words (WS_SYNC)
   int* status;
@@ -65,13 +73,60 @@ __device__ __forceinline__ void unpack_words(const QBlock& a, uint32_t* hi, uint
   }
 }
 
+// ---- two or more tokens: warp-level tensor-core products (mma.sync m16n8k16, fp16 x fp16 -> fp32) ----
+// Weights are the A operand (16 rows x 16 k), the tokens (or an expert's pairs) the 8 columns of B.
+// Within a 64-block the k order is free as long as A and B agree: k-step s of thread (g, t) -- g =
+// lane / 4 owns rows g, g + 8 and column g, t = lane % 4 -- takes half2 number 2s (k = 2t, 2t + 1) and
+// 2s + 1 (k = 2t + 8, 2t + 9) of code word t of its rows, where half2 number q = 4b + m holds field m of
+// code bytes b and b + 2 (weights 16t + 4b + m and 16t + 8 + 4b + m).  Activations are stored once in
+// that order ("fragment order": per (k-block, t, column) 16 halves, pair q at halves 2q, 2q + 1), so a
+// thread's B operand for a whole k-block is two 16-byte loads.  A holds code - q2_offset exactly (the
+// LOP3 / HSUB2 construction of the tensor-core prefill path); the scale d of each (row, k-block) is
+// applied to the k-block's fp32 partial products.
+__device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The 8 half2 (code - q2_offset) of one 16-code word, in half2 order q = 4b + m.
+__device__ __forceinline__ void codes_to_half2(uint32_t word, const uint32_t* sub, uint32_t* h) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int b = q >> 2, m = q & 3;
+    const uint32_t src = b ? (word >> 8) : word;
+    const uint32_t bits = (src & (0x00030003u << (2 * m))) | ((uint32_t)((25 - 2 * m) << 10) * 0x00010001u);
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&bits), *reinterpret_cast<const __half2*>(&sub[m]));
+    h[q] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+// 16 consecutive values v[0..15] of a block (weights 16t ..) as the 8 fragment-order half2.
+__device__ __forceinline__ void to_fragment_order(const float* v, uint32_t* h) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int b = q >> 2, m = q & 3;
+    const __half2 x2 = __floats2half2_rn(v[4 * b + m], v[8 + 4 * b + m]);
+    h[q] = *reinterpret_cast<const uint32_t*>(&x2);
+  }
+}
+
 template <int TT>
 __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const DecodeParams p) {
+  constexpr bool MMA = TT >= 2;  // one token: dp4a on the codes; more: tensor-core products
+  constexpr int NS = df_stages<TT>();
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;                                            // DF_NS * DF_UNIT
-  QBlock* sq = reinterpret_cast<QBlock*>(smem + DF_NS * DF_UNIT);  // [KB_D][TT]
-  __shared__ uint64_t bars[DF_NS];
-  __shared__ int s_pending[DF_NS];
+  uint8_t* ring = smem;                                                 // NS * DF_UNIT
+  QBlock* sqx = reinterpret_cast<QBlock*>(smem + NS * DF_UNIT);         // [T][KB_GU] all tokens
+  QBlock* sq = sqx + TT * KB_GU;                                        // [KB_D][TT] h of a down unit
+  float2* red = reinterpret_cast<float2*>(sq);                          // [DF_KG][TT][SLAB] (gate/up)
+  static_assert(sizeof(float2) * DF_KG * TT * SLAB <= sizeof(QBlock) * KB_D * TT, "reduction fits");
+  __shared__ uint64_t bars[NS];
+  __shared__ uint64_t bar_qx, bar_h;
+  __shared__ int s_pending[NS];
+  __shared__ int s_qx_pending, s_h_pending;
   __shared__ float s_inv[TT];
   __shared__ int s_ids[TT * K];
   __shared__ float s_w[TT * K];
@@ -83,22 +138,24 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ float s_rpart[4][TT];
   __shared__ float s_bias[EMAX];
   __shared__ int32_t s_qtmp[4][64];
-  __shared__ float s_h[TT][RT];
   __shared__ int s_flag, s_ok, s_nact;
 
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
   int* bar = p.sync + WS_SYNC_BAR;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
-  int* cnt_gu = p.sync + WS_SYNC_CNT_GU;
-  int* h_ready = p.sync + WS_SYNC_HREADY;
+  int* h_cnt = p.sync + WS_SYNC_HREADY;
   int* cnt_dn = p.sync + WS_SYNC_CNT_DN;
 
   if (tid == 0) {
-    for (int s = 0; s < DF_NS; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bars[s], 1);
       s_pending[s] = -1;
     }
+    mbar_init(&bar_qx, 1);
+    mbar_init(&bar_h, 1);
+    s_qx_pending = 0;
+    s_h_pending = -1;
     fence_mbar_init();
     s_ok = 1;
   }
@@ -157,7 +214,14 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     if (lane == 0)
 #pragma unroll
       for (int r = 0; r < WS_NREP; ++r) p.sumsq[(size_t)r * T * KB_GU + b] = ss;
-    quantise_block_warp(v.x, v.y, p.q2_offset, p.qx + b, s_qtmp[warp]);
+    if constexpr (MMA) {  // fp16 x in fragment order: xs[kb][t4][token][16 halves]
+      const int t4 = lane >> 3, q = lane & 7, bb = q >> 2, mm = q & 3;
+      const float* src = p.x + (size_t)t * H + kb * QK + 16 * t4 + 4 * bb + mm;
+      const __half2 x2 = __floats2half2_rn(__ldg(src), __ldg(src + 8));
+      reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.qx) + ((size_t)(kb * 4 + t4) * T + t) * 32)[q] = x2;
+    } else {
+      quantise_block_warp(v.x, v.y, p.q2_offset, p.qx + b, s_qtmp[warp]);
+    }
   }
 
   // ---- grid barrier ----
@@ -170,6 +234,15 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       for (int r = 0; r < WS_NREP; ++r) st_relaxed(p.sync + WS_SYNC_REL + 32 * r, 1);
     }
     s_ok = spin_until_geq(p.sync + WS_SYNC_REL + 32 * (c % WS_NREP), 1, p.status) ? 1 : 0;
+    if (s_ok) {
+      // every token's quantised activations (written by all CTAs before the barrier) into shared
+      // memory; the async-proxy copy is ordered after the acquire by the proxy fence
+      fence_proxy_async_global();
+      const uint32_t xbytes = MMA ? (uint32_t)(KB_GU * 4 * 32 * T) : (uint32_t)(sizeof(QBlock) * T * KB_GU);
+      mbar_expect_tx(&bar_qx, xbytes);
+      bulk_g2s(sqx, p.qx, xbytes, &bar_qx);
+      s_qx_pending = 1;
+    }
   }
   __syncthreads();
 
@@ -245,70 +318,141 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     const int D = s_nact;
     const int n_gu = D * DF_GU, n_units = D * (DF_GU + DF_DN);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int u, int i) {  // thread 0 only: unit u into stage i % DF_NS
-      const int st = i % DF_NS;
+    auto issue = [&](int u, int i) {  // thread 0 only: unit u into stage i % NS
+      const int st = i % NS;
       const uint8_t* src;
       if (u < n_gu) {
-        const int j = u / DF_GU, r = u % DF_GU;
-        const int rt = r / DF_SGU, s = r % DF_SGU;
-        src = p.blobs + (int64_t)s_te[j] * p.stride + ((int64_t)rt * KB_GU + s * DF_KBU) * GU_CHUNK;
+        const int j = u / DF_GU, sl = u % DF_GU;
+        src = p.blobs + (int64_t)s_te[j] * p.stride + (int64_t)sl * SLAB_BYTES;
       } else {
         const int v = u - n_gu;
         const int j = v / DF_DN, rtd = v % DF_DN;
         src = p.blobs + (int64_t)s_te[j] * p.stride + D_REGION + (int64_t)rtd * KB_D * D_CHUNK;
       }
-      s_pending[st] = (i / DF_NS) & 1;
+      s_pending[st] = (i / NS) & 1;
       mbar_expect_tx(&bars[st], DF_UNIT);
       bulk_g2s_stream(ring + (size_t)st * DF_UNIT, src, DF_UNIT, &bars[st], pol);
     };
     if (tid == 0)
-      for (int i = 0; i < DF_NS; ++i)
+      for (int i = 0; i < NS; ++i)
         if (c + G * i < n_units) issue(c + G * i, i);
 
-    int i = 0;
+    int i = 0, n_dn = 0;
     for (int u = c; u < n_units; u += G, ++i) {
-      const int st = i % DF_NS;
-      const uint32_t par = (uint32_t)((i / DF_NS) & 1);
+      const int st = i % NS;
+      const uint32_t par = (uint32_t)((i / NS) & 1);
       const uint8_t* stage = ring + (size_t)st * DF_UNIT;
       if (u < n_gu) {
-        // -------- gate/up unit --------
-        const int j = u / DF_GU, r = u % DF_GU;
-        const int rt = r / DF_SGU, s = r % DF_SGU;
+        // -------- gate/up unit: slab sl (rows 16 sl ..) of expert slot j, all k-blocks --------
+        const int j = u / DF_GU, sl = u % DF_GU;
         const int n = s_tn[j], q0 = s_tq[j];
-        for (int idx = tid; idx < DF_KBU * TT * 9; idx += DF_THREADS) {
-          const int blk = idx / 9, part = idx % 9;
-          const int kb = blk / TT, ii = blk % TT;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (ii < n) {
-            const int t = s_pair[q0 + ii] / K;
-            v = __ldcg(reinterpret_cast<const uint4*>(p.qx + (size_t)t * KB_GU + s * DF_KBU + kb) + part);
-          }
-          reinterpret_cast<uint4*>(sq + blk)[part] = v;
-        }
-        if (!__syncthreads_and(mbar_wait(&bars[st], par, p.status) ? 1 : 0)) {
+        bool ready = mbar_wait(&bars[st], par, p.status);
+        if (s_qx_pending) ready = mbar_wait(&bar_qx, 0u, p.status) && ready;
+        if (!__syncthreads_and(ready ? 1 : 0)) {
           if (tid == 0) s_ok = 0;
           __syncthreads();
           break;
         }
-        if (tid == 0) s_pending[st] = -1;
+        if (tid == 0) {
+          s_pending[st] = -1;
+          s_qx_pending = 0;
+        }
+        if constexpr (MMA) {
+          // warp w: k-blocks [10 w, 10 w + 10) of the 16-row slab, all T tokens as columns
+          const int g = lane >> 2, t4 = lane & 3;
+          uint32_t subq[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const __half2 s2 = __half2half2(__float2half_rn((float)((1024 >> (2 * m)) + p.q2_offset)));
+            subq[m] = *reinterpret_cast<const uint32_t*>(&s2);
+          }
+          const uint8_t* xs = reinterpret_cast<const uint8_t*>(sqx);
+          float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int kk = 0; kk < KB_GU / 4; ++kk) {
+            const int kb = warp * (KB_GU / 4) + kk;
+            const uint8_t* piece = stage + kb * SLAB_KB;
+            const uint32_t wg0 = *reinterpret_cast<const uint32_t*>(piece + 16 * g + 4 * t4);
+            const uint32_t wg1 = *reinterpret_cast<const uint32_t*>(piece + 16 * (g + 8) + 4 * t4);
+            const uint32_t wu0 = *reinterpret_cast<const uint32_t*>(piece + 256 + 16 * g + 4 * t4);
+            const uint32_t wu1 = *reinterpret_cast<const uint32_t*>(piece + 256 + 16 * (g + 8) + 4 * t4);
+            const __half2 sc0 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * g);
+            const __half2 sc1 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * (g + 8));
+            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+            if (g < T) {
+              const uint4* xp = reinterpret_cast<const uint4*>(xs + ((size_t)(kb * 4 + t4) * T + g) * 32);
+              x0 = xp[0];
+              x1 = xp[1];
+            }
+            const uint32_t bq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t hg0[8], hg1[8], hu0[8], hu1[8];
+            codes_to_half2(wg0, subq, hg0);
+            codes_to_half2(wg1, subq, hg1);
+            codes_to_half2(wu0, subq, hu0);
+            codes_to_half2(wu1, subq, hu1);
+            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const uint32_t a_g[4] = {hg0[2 * s], hg1[2 * s], hg0[2 * s + 1], hg1[2 * s + 1]};
+              const uint32_t a_u[4] = {hu0[2 * s], hu1[2 * s], hu0[2 * s + 1], hu1[2 * s + 1]};
+              mma_16816(cg, a_g, bq[2 * s], bq[2 * s + 1]);
+              mma_16816(cu, a_u, bq[2 * s], bq[2 * s + 1]);
+            }
+            const float dg0 = __low2float(sc0), du0 = __high2float(sc0);
+            const float dg1 = __low2float(sc1), du1 = __high2float(sc1);
+            ag[0] = fmaf(dg0, cg[0], ag[0]); ag[1] = fmaf(dg0, cg[1], ag[1]);
+            ag[2] = fmaf(dg1, cg[2], ag[2]); ag[3] = fmaf(dg1, cg[3], ag[3]);
+            au[0] = fmaf(du0, cu[0], au[0]); au[1] = fmaf(du0, cu[1], au[1]);
+            au[2] = fmaf(du1, cu[2], au[2]); au[3] = fmaf(du1, cu[3], au[3]);
+          }
+          // red[warp][mat][row][column]: the four warps' k ranges, added below in warp order
+          float* rf = reinterpret_cast<float*>(red);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = g + 8 * (e >> 1), col = 2 * t4 + (e & 1);
+            if (col < TT) {
+              rf[((warp * 2 + 0) * SLAB + row) * TT + col] = ag[e];
+              rf[((warp * 2 + 1) * SLAB + row) * TT + col] = au[e];
+            }
+          }
+          __syncthreads();
+          if (tid < SLAB * n) {
+            const int r2 = tid % SLAB, ii = tid / SLAB;
+            const int tk = s_pair[q0 + ii] / K;
+            float gg = 0.f, uu = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              gg += rf[((w * 2 + 0) * SLAB + r2) * TT + tk];
+              uu += rf[((w * 2 + 1) * SLAB + r2) * TT + tk];
+            }
+            const float inv = s_inv[tk];
+            p.hf[(size_t)(q0 + ii) * FF + sl * SLAB + r2] = silu_mul(gg * inv, uu * inv);
+          }
+        } else {
+        const int r = tid % SLAB, grp = tid / SLAB;  // row of the slab, group of DF_KBG k-blocks
+        int tok[TT];
         float tinv[TT];
 #pragma unroll
-        for (int ii = 0; ii < TT; ++ii) tinv[ii] = (ii < n) ? s_inv[s_pair[q0 + ii] / K] : 0.f;
+        for (int ii = 0; ii < TT; ++ii) {
+          tok[ii] = (ii < n) ? s_pair[q0 + ii] / K : 0;
+          tinv[ii] = (ii < n) ? s_inv[tok[ii]] : 0.f;
+        }
         float accg[TT], accu[TT];
 #pragma unroll
         for (int ii = 0; ii < TT; ++ii) { accg[ii] = 0.f; accu[ii] = 0.f; }
 #pragma unroll 1
-        for (int kb = 0; kb < DF_KBU; ++kb) {
-          const uint8_t* chunk = stage + kb * GU_CHUNK;
-          const uint4 gc = *reinterpret_cast<const uint4*>(chunk + 16 * tid);
-          const uint4 uc = *reinterpret_cast<const uint4*>(chunk + 2048 + 16 * tid);
-          const __half2 sc = *reinterpret_cast<const __half2*>(chunk + 4096 + 4 * tid);
+        for (int kk = 0; kk < DF_KBG; ++kk) {
+          const int kb = grp * DF_KBG + kk;
+          const uint8_t* piece = stage + kb * SLAB_KB;
+          const uint4 gc = *reinterpret_cast<const uint4*>(piece + 16 * r);
+          const uint4 uc = *reinterpret_cast<const uint4*>(piece + 256 + 16 * r);
+          const __half2 sc = *reinterpret_cast<const __half2*>(piece + 512 + 4 * r);
           const float dg = __low2float(sc), du = __high2float(sc);
           const Masked gm = mask_codes(gc), um = mask_codes(uc);
 #pragma unroll
           for (int ii = 0; ii < TT; ++ii) {
             if (ii < n) {
-              const QBlock& a = sq[kb * TT + ii];
+              const QBlock& a = sqx[tok[ii] * KB_GU + kb];
               uint32_t hi[16], lo[16];
               unpack_words(a, hi, lo);
               const float f = a.s64 * tinv[ii];
@@ -319,53 +463,75 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             }
           }
         }
-        float2* part = reinterpret_cast<float2*>(p.partial);
 #pragma unroll
         for (int ii = 0; ii < TT; ++ii)
-          if (ii < n) part[((size_t)(rt * DF_SGU + s) * P + q0 + ii) * RT + tid] = make_float2(accg[ii], accu[ii]);
+          if (ii < n) red[(grp * TT + ii) * SLAB + r] = make_float2(accg[ii], accu[ii]);
+        __syncthreads();
+        if (tid < SLAB * n) {  // (row, token): the 8 groups added in group order
+          const int r2 = tid % SLAB, ii = tid / SLAB;
+          float g = 0.f, uu = 0.f;
+#pragma unroll
+          for (int q = 0; q < DF_KG; ++q) {
+            const float2 v = red[(q * TT + ii) * SLAB + r2];
+            g += v.x;
+            uu += v.y;
+          }
+          p.hf[(size_t)(q0 + ii) * FF + sl * SLAB + r2] = silu_mul(g, uu);
+        }
+        }
         __threadfence();
         __syncthreads();
-        if (tid == 0) s_flag = (atomicAdd(&cnt_gu[j * RT_GU + rt], 1) == DF_SGU - 1) ? 1 : 0;
-        __syncthreads();
-        if (s_flag) {
-          __threadfence();
-#pragma unroll
-          for (int ii = 0; ii < TT; ++ii) {
-            if (ii < n) {
-              float g = 0.f, uu = 0.f;
-              for (int ss = 0; ss < DF_SGU; ++ss) {
-                const float2 v = __ldcg(part + ((size_t)(rt * DF_SGU + ss) * P + q0 + ii) * RT + tid);
-                g += v.x;
-                uu += v.y;
-              }
-              s_h[ii][tid] = silu_mul(g, uu);
-            }
-          }
-          if (tid == 0) cnt_gu[j * RT_GU + rt] = 0;
-          __syncthreads();
-          for (int item = warp; item < 2 * n; item += 4) {
-            const int ii = item >> 1, b = item & 1;
-            quantise_block_warp(s_h[ii][64 * b + 2 * lane], s_h[ii][64 * b + 2 * lane + 1], p.q2_offset,
-                                p.hq + (size_t)(q0 + ii) * KB_D + 2 * rt + b, s_qtmp[warp]);
-          }
-          __threadfence();
-          __syncthreads();
-          if (tid == 0) atomicAdd(&h_ready[j], 1);
-        }
+        if (tid == 0) atomicAdd(&h_cnt[j], 1);
       } else {
-        // -------- down unit --------
+        // -------- down unit: row tile rtd of expert slot j --------
         const int v = u - n_gu;
         const int j = v / DF_DN, rtd = v % DF_DN;
         const int n = s_tn[j], q0 = s_tq[j];
-        if (tid == 0) s_flag = spin_until_geq(&h_ready[j], RT_GU, p.status) ? 1 : 0;
+        // h of the expert's n tokens (contiguous rows of hf) into shared memory with one bulk copy,
+        // once all 40 slabs are in; the token activations' space is free (no gate/up unit follows)
+        float* sh = reinterpret_cast<float*>(sqx);
+        static_assert(sizeof(float) * TT * FF <= sizeof(QBlock) * TT * KB_GU, "h fits the activation space");
+        if (tid == 0) {
+          bool okh = spin_until_geq(&h_cnt[j], DF_GU, p.status);
+          if (s_qx_pending) okh = mbar_wait(&bar_qx, 0u, p.status) && okh;  // (only if no gate/up unit ran)
+          s_qx_pending = 0;
+          if (okh) {
+            fence_proxy_async_global();
+            mbar_expect_tx(&bar_h, (uint32_t)(sizeof(float) * n * FF));
+            bulk_g2s(sh, p.hf + (size_t)q0 * FF, (uint32_t)(sizeof(float) * n * FF), &bar_h);
+            s_h_pending = n_dn & 1;
+          }
+          s_flag = okh ? 1 : 0;
+        }
         __syncthreads();
         if (!s_flag) { if (tid == 0) s_ok = 0; __syncthreads(); break; }
-        for (int idx = tid; idx < KB_D * TT * 9; idx += DF_THREADS) {
-          const int blk = idx / 9, part = idx % 9;
-          const int kb = blk / TT, ii = blk % TT;
-          uint4 w4 = make_uint4(0, 0, 0, 0);
-          if (ii < n) w4 = __ldcg(reinterpret_cast<const uint4*>(p.hq + (size_t)(q0 + ii) * KB_D + kb) + part);
-          reinterpret_cast<uint4*>(sq + blk)[part] = w4;
+        const bool hok = mbar_wait(&bar_h, (uint32_t)(n_dn & 1), p.status);
+        ++n_dn;
+        if (!__syncthreads_and(hok ? 1 : 0)) { if (tid == 0) s_ok = 0; __syncthreads(); break; }
+        if (tid == 0) s_h_pending = -1;
+        if constexpr (MMA) {  // h in fp16 fragment order: hx[kb][t4][slot][16 halves]
+          uint8_t* hx = reinterpret_cast<uint8_t*>(sq);
+          for (int idx = tid; idx < n * KB_D * 4; idx += DF_THREADS) {
+            const int t4 = idx % 4, kb = (idx / 4) % KB_D, ii = idx / (4 * KB_D);
+            const float4* v4 = reinterpret_cast<const float4*>(sh + ii * FF + kb * QK + 16 * t4);
+            float f[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 a = v4[q];
+              f[4 * q] = a.x; f[4 * q + 1] = a.y; f[4 * q + 2] = a.z; f[4 * q + 3] = a.w;
+            }
+            uint32_t hq[8];
+            to_fragment_order(f, hq);
+            uint4* dst = reinterpret_cast<uint4*>(hx + ((size_t)(kb * 4 + t4) * n + ii) * 32);
+            dst[0] = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+            dst[1] = make_uint4(hq[4], hq[5], hq[6], hq[7]);
+          }
+        } else {
+          for (int item = warp; item < n * KB_D; item += DF_THREADS / 32) {  // quantise h, one warp per block
+            const int ii = item / KB_D, kb = item % KB_D;
+            const float2 hv = reinterpret_cast<const float2*>(sh + ii * FF + kb * QK)[lane];
+            quantise_block_warp(hv.x, hv.y, p.q2_offset, sq + kb * TT + ii, s_qtmp[warp]);
+          }
         }
         if (!__syncthreads_and(mbar_wait(&bars[st], par, p.status) ? 1 : 0)) {
           if (tid == 0) s_ok = 0;
@@ -373,6 +539,55 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           break;
         }
         if (tid == 0) s_pending[st] = -1;
+        if constexpr (MMA) {
+          // warp w: rows 32 w .. 32 w + 31 of the tile (two 16-row groups), all 10 k-blocks; columns =
+          // the expert's pairs
+          const int g = lane >> 2, t4 = lane & 3;
+          uint32_t subq[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const __half2 s2 = __half2half2(__float2half_rn((float)((1024 >> (2 * m)) + p.q2_offset)));
+            subq[m] = *reinterpret_cast<const uint32_t*>(&s2);
+          }
+          const uint8_t* hx = reinterpret_cast<const uint8_t*>(sq);
+          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+          for (int kb = 0; kb < KB_D; ++kb) {
+            const uint8_t* chunk = stage + kb * D_CHUNK;
+            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+            if (g < n) {
+              const uint4* xp = reinterpret_cast<const uint4*>(hx + ((size_t)(kb * 4 + t4) * n + g) * 32);
+              x0 = xp[0];
+              x1 = xp[1];
+            }
+            const uint32_t bq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int rg = 0; rg < 2; ++rg) {
+              const int R0 = 32 * warp + 16 * rg + g, R1 = R0 + 8;
+              uint32_t h0[8], h1[8];
+              codes_to_half2(*reinterpret_cast<const uint32_t*>(chunk + 16 * R0 + 4 * t4), subq, h0);
+              codes_to_half2(*reinterpret_cast<const uint32_t*>(chunk + 16 * R1 + 4 * t4), subq, h1);
+              const float d0 = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * R0));
+              const float d1 = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * R1));
+              float cc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint32_t a[4] = {h0[2 * s], h1[2 * s], h0[2 * s + 1], h1[2 * s + 1]};
+                mma_16816(cc, a, bq[2 * s], bq[2 * s + 1]);
+              }
+              acc[rg][0] = fmaf(d0, cc[0], acc[rg][0]); acc[rg][1] = fmaf(d0, cc[1], acc[rg][1]);
+              acc[rg][2] = fmaf(d1, cc[2], acc[rg][2]); acc[rg][3] = fmaf(d1, cc[3], acc[rg][3]);
+            }
+          }
+#pragma unroll
+          for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 2 * t4 + (e & 1);
+              const int row = rtd * RT + 32 * warp + 16 * rg + g + 8 * (e >> 1);
+              if (col < n) p.parts[(size_t)s_pair[q0 + col] * H + row] = acc[rg][e];
+            }
+        } else {
         float acc[TT];
 #pragma unroll
         for (int ii = 0; ii < TT; ++ii) acc[ii] = 0.f;
@@ -397,31 +612,43 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 #pragma unroll
         for (int ii = 0; ii < TT; ++ii)
           if (ii < n) p.parts[(size_t)s_pair[q0 + ii] * H + row] = acc[ii];
+        }
+        const int row = rtd * RT + tid;  // combine: one output row per thread
         __threadfence();
         __syncthreads();
         if (tid == 0) s_flag = (atomicAdd(&cnt_dn[rtd], 1) == D - 1) ? 1 : 0;
         __syncthreads();
         if (s_flag) {
           __threadfence();
-          for (int t = 0; t < T; ++t) {
-            float a = 0.f;
+          float pv[TT * K], xv[TT];  // every load first, then the k-ordered sums
 #pragma unroll
-            for (int k = 0; k < K; ++k) a = fmaf(s_w[t * K + k], __ldcg(p.parts + (size_t)(t * K + k) * H + row), a);
-            p.out[(size_t)t * H + row] = p.residual ? p.x[(size_t)t * H + row] + a : a;
+          for (int q = 0; q < TT * K; ++q) pv[q] = (q < T * K) ? __ldcg(p.parts + (size_t)q * H + row) : 0.f;
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt) xv[tt] = (tt < T && p.residual) ? p.x[(size_t)tt * H + row] : 0.f;
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt) {
+            if (tt < T) {
+              float a = 0.f;
+#pragma unroll
+              for (int k = 0; k < K; ++k) a = fmaf(s_w[tt * K + k], pv[tt * K + k], a);
+              p.out[(size_t)tt * H + row] = p.residual ? xv[tt] + a : a;
+            }
           }
           if (tid == 0) cnt_dn[rtd] = 0;
         }
       }
-      __syncthreads();  // everyone is done with this stage and with sq
-      if (tid == 0 && u + G * DF_NS < n_units) issue(u + G * DF_NS, i + DF_NS);
+      __syncthreads();  // everyone is done with this stage and with sq / red
+      if (tid == 0 && u + G * NS < n_units) issue(u + G * NS, i + NS);
     }
   }
 
   // ---- leave: drain copies still in flight (only after a failed wait), last CTA resets counters ----
   __syncthreads();
   if (tid == 0) {
-    for (int st = 0; st < DF_NS; ++st)
+    for (int st = 0; st < NS; ++st)
       if (s_pending[st] >= 0) mbar_wait(&bars[st], (uint32_t)s_pending[st], p.status);
+    if (s_qx_pending) mbar_wait(&bar_qx, 0u, p.status);
+    if (s_h_pending >= 0) mbar_wait(&bar_h, (uint32_t)s_h_pending, p.status);
     __threadfence();
     s_flag = (atomicAdd(exit_cnt, 1) == G - 1) ? 1 : 0;
   }
@@ -445,15 +672,16 @@ DeviceLaunchInfo g_info[64];
 
 template <int TT>
 cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
-  const size_t smem = (size_t)DF_NS * DF_UNIT + sizeof(QBlock) * KB_D * TT;
+  const size_t smem = df_smem<TT>();
   auto kern = decode_layer_kernel<TT>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  cudaError_t err;
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   const int vi = TT == 1 ? 0 : TT == 2 ? 1 : TT == 4 ? 2 : 3;
   int grid = (dev >= 0 && dev < 64) ? g_info[dev].grid[vi] : 0;
-  if (grid == 0) {
+  if (grid == 0) {  // first launch on this device: shared-memory opt-in and the co-resident grid
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return err;
     int sms = 0, per_sm = 0;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DF_THREADS, smem)) != cudaSuccess)
@@ -489,8 +717,7 @@ cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_ro
   prm.dots = (float*)(ws + L.dots_rep);
   prm.sumsq = (float*)(ws + L.sumsq);
   prm.qx = (QBlock*)(ws + L.qx);
-  prm.hq = (QBlock*)(ws + L.hq);
-  prm.partial = (float*)(ws + L.partial);
+  prm.hf = (float*)(ws + L.hf);
   prm.parts = (float*)(ws + L.parts);
   prm.sync = (int*)(ws + WS_SYNC);
   prm.status = (int*)(ws + L.status);

@@ -67,6 +67,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   return true;
 }
 
+// Orders this thread's earlier (generic-proxy) view of global memory before its later async-proxy
+// accesses (cp.async.bulk reads of data that other threads wrote and released).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void st_relaxed(int* p, int v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -43,21 +43,30 @@ struct TcExpert { int32_t e, q0, n, q0pad; };    // grouping slots [q0, q0+n), p
 struct TcTile { int32_t e, q0, n, q0pad; };      // <= 128 tokens of one expert
 
 // ---------------------------------------------------------------------------------------------
-// Tile lists: experts' padded row ranges (multiples of 8) and tiles of at most 128 tokens.
+// Tile lists: experts' padded row ranges (multiples of 8) and tiles of at most 128 tokens.  An expert
+// entry outside [0, E) or a slot range outside [0, P) sets ST_CORRUPT and contributes no tile.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restrict__ expert_off,
                                                          const int32_t* __restrict__ active,
-                                                         const int32_t* __restrict__ n_active, int E,
+                                                         const int32_t* __restrict__ n_active, int E, int P,
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
-                                                         int32_t* __restrict__ counts, int max_tiles) {
+                                                         int32_t* __restrict__ counts, int max_tiles,
+                                                         int* __restrict__ status) {
   __shared__ int s_pad[EMAX], s_nt[EMAX], s_scratch[32];
   const int i = threadIdx.x;
-  const int na = min(*n_active, E);
+  const int na = max(0, min(*n_active, E));
   int e = 0, q0 = 0, n = 0;
-  if (i < na) {
+  if (i < na) {  // the grouping may come from the caller: a bad entry is reported and skipped
     e = active[i];
-    q0 = expert_off[e];
-    n = expert_off[e + 1] - q0;
+    if (e >= 0 && e < E) {
+      q0 = expert_off[e];
+      n = expert_off[e + 1] - q0;
+    }
+    if (e < 0 || e >= E || q0 < 0 || n < 0 || q0 + n > P) {
+      set_status(status, ST_CORRUPT);
+      q0 = 0;
+      n = 0;
+    }
   }
   s_pad[i] = (i < na) ? (n + 7) / 8 * 8 : 0;
   s_nt[i] = (i < na) ? (n + TCN - 1) / TCN : 0;
@@ -90,10 +99,11 @@ constexpr int GATHER_THREADS = 256;
 constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over rows; 4 CTAs per SM of a 152-SM GB300
 __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const float* __restrict__ x,
                                                                    const float* __restrict__ inv_rms,
-                                                                   const int32_t* __restrict__ pair,
+                                                                   const int32_t* __restrict__ pair, int P,
                                                                    const TcExpert* __restrict__ exps,
                                                                    const int32_t* __restrict__ counts,
-                                                                   uint8_t* __restrict__ xg, int64_t rows_cap) {
+                                                                   uint8_t* __restrict__ xg, int64_t rows_cap,
+                                                                   int* __restrict__ status) {
   __shared__ int s_row0[EMAX];
   const int na = counts[0], ppad = counts[2];
   for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_row0[i] = exps[i].q0pad;
@@ -109,7 +119,12 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const float* 
     }
     const TcExpert ex = exps[lo];
     const int s = r - ex.q0pad;
-    const int t = (s < ex.n) ? pair[ex.q0 + s] / K : -1;
+    int t = -1;
+    if (s < ex.n) {
+      const int pr = pair[ex.q0 + s];
+      if (pr >= 0 && pr < P) t = pr / K;
+      else if (lane == 0) set_status(status, ST_CORRUPT);  // a caller's bad pair: zero row, no write
+    }
     const float sc = (t >= 0 && inv_rms) ? __ldg(inv_rms + t) : 1.f;
     const int c = lane & 7, odd = c & 1;
 #pragma unroll 2
@@ -167,6 +182,7 @@ struct TcParams {
   uint8_t* hg;          // gate/up output
   int64_t rows_cap;
   const int32_t* pair;  // down: slot -> pair
+  int P;                // pairs (T * K)
   float* parts;         // down output
   int* status;
 };
@@ -251,7 +267,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
           mbar_expect_tx(&full_tma[s], G::CODE + nrows * 128);
           bulk_g2s(st, p.act + ((int64_t)kb * p.rows_cap + tl.q0pad) * 128, nrows * 128, &full_tma[s]);
           if (GU) {
-            bulk_g2s_stream(st + B_TILE, blob + ((int64_t)rt * KB_GU + kb) * GU_CHUNK, GU_CHUNK, &full_tma[s], pol);
+#pragma unroll
+            for (int sl = 0; sl < RT / SLAB; ++sl)  // the tile's 8 slabs: one 576-byte piece each
+              bulk_g2s_stream(st + B_TILE + sl * SLAB_KB,
+                              blob + ((int64_t)(rt * (RT / SLAB) + sl) * KB_GU + kb) * SLAB_KB, SLAB_KB,
+                              &full_tma[s], pol);
           } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -318,10 +338,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         if (ok) {
           const uint8_t* code = tma_ring + (size_t)s * G::TMA_STAGE + B_TILE;
           uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
-          // gate/up chunk: gate codes, up codes, {gate d, up d} per row; down: two plain chunks
-          const uint8_t* cb = code + (GU ? 0 : sub * D_CHUNK);
-          const uint4 cw = *reinterpret_cast<const uint4*>(cb + (GU ? sub * 2048 : 0) + 16 * row);
-          const __half d = *reinterpret_cast<const __half*>(cb + (GU ? 4096 + 4 * row + 2 * sub : 2048 + 2 * row));
+          // gate/up: 8 slab pieces {gate codes, up codes, {gate d, up d} per row}; down: two chunks
+          uint4 cw;
+          __half d;
+          if (GU) {
+            const uint8_t* pc = code + (row / SLAB) * SLAB_KB;
+            const int rr = row % SLAB;
+            cw = *reinterpret_cast<const uint4*>(pc + sub * 256 + 16 * rr);
+            d = *reinterpret_cast<const __half*>(pc + 512 + 4 * rr + 2 * sub);
+          } else {
+            const uint8_t* cb = code + sub * D_CHUNK;
+            cw = *reinterpret_cast<const uint4*>(cb + 16 * row);
+            d = *reinterpret_cast<const __half*>(cb + 2048 + 2 * row);
+          }
           dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
         }
         tc::fence_proxy_async_smem();
@@ -374,8 +403,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = 16 * ch + i;
-              if (col < tl.n) {
-                float* dst = p.parts + (size_t)p.pair[tl.q0 + col] * H + orow;
+              const int pr = col < tl.n ? p.pair[tl.q0 + col] : -1;
+              if (pr >= 0 && pr < p.P) {
+                float* dst = p.parts + (size_t)pr * H + orow;
                 dst[0] = y0[i];
                 dst[128] = y1[i];
               }
@@ -419,10 +449,10 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
   int32_t* counts = reinterpret_cast<int32_t*>(meta + sizeof(TcExpert) * EMAX + sizeof(TcTile) * max_tiles);
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
-                tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, exps, tiles, counts,
-                                                    max_tiles));
-  STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, exps, counts, xg,
-                                                                                   rows_cap));
+                tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
+                                                    counts, max_tiles, status));
+  STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, T * K, exps, counts, xg,
+                                                                                   rows_cap, status));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   int dev = 0;
@@ -432,8 +462,8 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) g_sms[dev] = sms;
   }
-  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, parts,
-              status};
+  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, T * K,
+              parts, status};
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<true>::SMEM)) != cudaSuccess)
     return err;

@@ -14,8 +14,6 @@ static_assert(KID_DECODE_LAYER == STRATA_KERNEL_DECODE_LAYER && KID_ROUTE_DECODE
                   KID_RMSNORM == STRATA_KERNEL_RMSNORM && KID_ROUTER_TC == STRATA_KERNEL_ROUTER_TC &&
                   KID_TOP_K == STRATA_KERNEL_TOP_K && KID_GROUP_HIST == STRATA_KERNEL_GROUP_HIST &&
                   KID_GROUP_SCAN == STRATA_KERNEL_GROUP_SCAN && KID_GROUP_SCATTER == STRATA_KERNEL_GROUP_SCATTER &&
-                  KID_BUILD_TILES == STRATA_KERNEL_BUILD_TILES && KID_QUANTISE_X == STRATA_KERNEL_QUANTISE_X &&
-                  KID_GEMV_GATEUP == STRATA_KERNEL_GEMV_GATEUP && KID_GEMV_DOWN == STRATA_KERNEL_GEMV_DOWN &&
                   KID_TC_PREPARE == STRATA_KERNEL_TC_PREPARE && KID_TC_GATHER == STRATA_KERNEL_TC_GATHER &&
                   KID_TC_GATEUP == STRATA_KERNEL_TC_GATEUP && KID_TC_DOWN == STRATA_KERNEL_TC_DOWN &&
                   KID_COMBINE == STRATA_KERNEL_COMBINE && KID_PACK == STRATA_KERNEL_PACK &&

@@ -19,9 +19,9 @@ __host__ __device__ inline void packed_offsets(int b, int64_t* codes_off, int64_
     const int up = b >= kBlocksPerMat;
     const int bb = up ? b - kBlocksPerMat : b;
     const int r = bb / KB_GU, kb = bb % KB_GU;
-    const int64_t chunk = ((int64_t)(r / RT) * KB_GU + kb) * GU_CHUNK;
-    *codes_off = chunk + (up ? 2048 : 0) + 16 * (r % RT);
-    *scale_off = chunk + 4096 + 4 * (r % RT) + (up ? 2 : 0);
+    const int64_t piece = ((int64_t)(r / SLAB) * KB_GU + kb) * SLAB_KB;
+    *codes_off = piece + (up ? 256 : 0) + 16 * (r % SLAB);
+    *scale_off = piece + 512 + 4 * (r % SLAB) + (up ? 2 : 0);
   } else {
     const int bb = b - 2 * kBlocksPerMat;
     const int n = bb / KB_D, kb = bb % KB_D;

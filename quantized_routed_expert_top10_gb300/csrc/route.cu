@@ -290,62 +290,6 @@ __global__ void __launch_bounds__(32) group_scatter_kernel(const int32_t* __rest
   stable_scatter_warp(s_ids, 0, p1 - p0, E, fill, pair, p0);
 }
 
-// Tiles from a caller-provided grouping (strata_moe_experts): one CTA.  The arrays come from the
-// caller, so every expert id and slot range is checked; a bad entry sets ST_CORRUPT and is skipped.
-__global__ void __launch_bounds__(512) build_tiles_kernel(const int32_t* __restrict__ expert_off,
-                                                          const int32_t* __restrict__ active,
-                                                          const int32_t* __restrict__ n_active_in, int E, int P,
-                                                          int32_t* __restrict__ n_active_tiles,
-                                                          Tile* __restrict__ tiles, int max_tiles, int* status) {
-  __shared__ int s_nt[EMAX], s_scratch[32];
-  const int na = max(0, min(*n_active_in, E));
-  const int i = threadIdx.x;
-  int c = 0, e = 0, q0 = 0;
-  if (i < na) {
-    e = active[i];
-    if (e < 0 || e >= E) {
-      set_status(status, ST_CORRUPT);
-    } else {
-      q0 = expert_off[e];
-      c = expert_off[e + 1] - q0;
-      if (q0 < 0 || c < 0 || q0 + c > P) {
-        set_status(status, ST_CORRUPT);
-        c = 0;
-      }
-    }
-  }
-  s_nt[i] = (c + NT - 1) / NT;
-  __syncthreads();
-  const int ntiles = cta_exclusive_scan(s_nt, s_nt, EMAX, s_scratch);
-  const int nt = (c + NT - 1) / NT;
-  for (int j = 0; j < nt; ++j) {
-    const int idx = s_nt[i] + j;
-    if (idx < max_tiles) {
-      Tile tl;
-      tl.e = e;
-      tl.q0 = q0 + j * NT;
-      tl.n = min(NT, c - j * NT);
-      tl.pad = 0;
-      tiles[idx] = tl;
-    }
-  }
-  if (i == 0) {
-    n_active_tiles[0] = na;
-    n_active_tiles[1] = ntiles < max_tiles ? ntiles : max_tiles;
-  }
-}
-
-__global__ void __launch_bounds__(128) quantise_x_kernel(const float* __restrict__ x, int T, int q2_offset,
-                                                         QBlock* __restrict__ qx) {
-  __shared__ int32_t tmp[4][64];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 4 + warp;
-  if (b >= T * KB_GU) return;
-  const int t = b / KB_GU, kb = b % KB_GU;
-  const float2 v = *reinterpret_cast<const float2*>(x + (size_t)t * H + kb * QK + 2 * lane);
-  quantise_block_warp(v.x, v.y, q2_offset, qx + b, tmp[warp]);
-}
-
 }  // namespace
 
 cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
@@ -392,21 +336,6 @@ cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, 
   STRATA_LAUNCH(KID_GROUP_SCATTER, s,
                 group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
   if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_build_tiles(const int32_t* expert_off, const int32_t* active, const int32_t* n_active, int E,
-                               int T, const WsLayout& L, char* ws, cudaStream_t s) {
-  STRATA_LAUNCH(KID_BUILD_TILES, s,
-                build_tiles_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, E, T * K,
-                                                     (int32_t*)(ws + L.n_active), (Tile*)(ws + L.tiles), L.max_tiles,
-                                                     (int*)(ws + L.status)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quantise_x(const float* x, int T, int q2_offset, QBlock* qx, cudaStream_t s) {
-  const int nblk = T * KB_GU;
-  STRATA_LAUNCH(KID_QUANTISE_X, s, quantise_x_kernel<<<(nblk + 3) / 4, 128, 0, s>>>(x, T, q2_offset, qx));
   return cudaGetLastError();
 }
 

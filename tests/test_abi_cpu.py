@@ -69,12 +69,13 @@ def test_pack_round_trip_and_documented_layout(lib):
         p = packed[j * B:(j + 1) * B]
         for (r, kb) in ((0, 0), (129, 7), (639, 39)):
             blk = c[r * 40 + kb]                   # gate row r, k-block kb
-            chunk = ((r // 128) * 40 + kb) * 4608
-            np.testing.assert_array_equal(p[chunk + 16 * (r % 128): chunk + 16 * (r % 128) + 16], blk[2:])
-            np.testing.assert_array_equal(p[chunk + 4096 + 4 * (r % 128): chunk + 4096 + 4 * (r % 128) + 2], blk[:2])
+            piece = ((r // 16) * 40 + kb) * 576
+            rr = r % 16
+            np.testing.assert_array_equal(p[piece + 16 * rr: piece + 16 * rr + 16], blk[2:])
+            np.testing.assert_array_equal(p[piece + 512 + 4 * rr: piece + 512 + 4 * rr + 2], blk[:2])
             blk = c[25600 + r * 40 + kb]           # up
-            np.testing.assert_array_equal(p[chunk + 2048 + 16 * (r % 128): chunk + 2048 + 16 * (r % 128) + 16], blk[2:])
-            np.testing.assert_array_equal(p[chunk + 4096 + 4 * (r % 128) + 2: chunk + 4096 + 4 * (r % 128) + 4], blk[:2])
+            np.testing.assert_array_equal(p[piece + 256 + 16 * rr: piece + 256 + 16 * rr + 16], blk[2:])
+            np.testing.assert_array_equal(p[piece + 512 + 4 * rr + 2: piece + 512 + 4 * rr + 4], blk[:2])
         for (nr, kb) in ((0, 0), (1000, 3), (2559, 9)):
             blk = c[51200 + nr * 10 + kb]          # down row nr, k-block kb
             chunk = 921600 + ((nr // 128) * 10 + kb) * 2304
