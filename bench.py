@@ -156,7 +156,7 @@ def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws):
 
 # Kernels timed with the library's own event hooks inside the timed region: the whole decode layer for
 # T <= 8; for prefill every kernel of the step (the dominant one is picked by total time).
-PREFILL_KERNELS = ("RMSNORM", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN", "GROUP_SCATTER", "TC_PREPARE",
+PREFILL_KERNELS = ("ROUTER_PREP", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN", "GROUP_SCATTER", "TC_PREPARE",
                    "TC_GATHER", "TC_GATEUP", "TC_DOWN", "COMBINE")
 FLOPS_PER_PAIR = {"TC_GATEUP": 2 * 2 * 2560 * 640, "TC_DOWN": 2 * 640 * 2560}
 CSRC = os.path.join(ROOT, "quantized_routed_expert_top10_gb300", "csrc")

@@ -189,7 +189,7 @@ const char* strata_status_str(strata_status s);
  * Kernel ids (every kernel the library launches): */
 #define STRATA_KERNEL_DECODE_LAYER 0   /* whole layer for T <= 8, one cooperative launch */
 #define STRATA_KERNEL_ROUTE_DECODE 1   /* router GEMV + top-10 + grouping, T <= 8 (strata_moe_route) */
-#define STRATA_KERNEL_RMSNORM 2
+#define STRATA_KERNEL_ROUTER_PREP 2    /* bf16 hi/lo copies of x for the router GEMM (and 1/rms), T > 8 */
 #define STRATA_KERNEL_ROUTER_TC 3      /* router GEMM on the tensor cores, T > 8 */
 #define STRATA_KERNEL_TOP_K 4
 #define STRATA_KERNEL_GROUP_HIST 5

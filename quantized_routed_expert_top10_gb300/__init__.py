@@ -215,7 +215,7 @@ def strata_status_str(status: int) -> str:
 
 
 # kernel ids of strata_moe_profile_arm (STRATA_KERNEL_* of the header)
-KERNELS = ("DECODE_LAYER", "ROUTE_DECODE", "RMSNORM", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN",
+KERNELS = ("DECODE_LAYER", "ROUTE_DECODE", "ROUTER_PREP", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN",
            "GROUP_SCATTER", "TC_PREPARE", "TC_GATHER",
            "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK")
 KERNEL_ID = {name: i for i, name in enumerate(KERNELS)}

@@ -54,13 +54,9 @@ strata_status route_and_group(const float* x, int T, int norm, const uint16_t* w
     STRATA_CUDA(launch_route_decode(x, T, norm, w_router, bias, E, q2_offset, ids, weights, logits_user, L, ws, s));
     return STRATA_OK;
   }
-  const float* inv = nullptr;
-  if (norm) {
-    STRATA_CUDA(launch_inv_rms(x, T, (float*)(ws + L.inv_rms), s));
-    inv = (const float*)(ws + L.inv_rms);
-  }
   float* lparts = (float*)(ws + L.logits);
-  STRATA_CUDA(launch_router_tc(x, inv, T, w_router, E, lparts, (int*)(ws + L.status), s));
+  STRATA_CUDA(launch_router_tc(x, norm ? (float*)(ws + L.inv_rms) : nullptr, T, w_router, E, ws + L.xbf, lparts,
+                               (int*)(ws + L.status), s));
   STRATA_CUDA(launch_top_k(lparts, T, E, bias, logits_user, ids, weights, s));
   STRATA_CUDA(launch_group(ids, T, E, (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair),
                            (int32_t*)(ws + L.active), nullptr, L, ws, s));
@@ -133,7 +129,7 @@ strata_status strata_moe_route(const float* x, int32_t T, const uint16_t* w_rout
     return STRATA_OK;
   }
   float* lparts = (float*)(w + L.logits);
-  STRATA_CUDA(launch_router_tc(x, nullptr, T, w_router, n_expert, lparts, (int*)(w + L.status), s));
+  STRATA_CUDA(launch_router_tc(x, nullptr, T, w_router, n_expert, w + L.xbf, lparts, (int*)(w + L.status), s));
   STRATA_CUDA(launch_top_k(lparts, T, n_expert, bias, logits, ids, weights, s));
   return STRATA_OK;
 }

@@ -35,7 +35,7 @@ constexpr int64_t BLOB = STRATA_MOE_BLOB_BYTES;
 
 // Grouping tiles (finish_grouping): up to NT slots of one expert per tile.
 constexpr int NT = 8;
-constexpr int ROUTER_KSPLIT = 4;  // prefill router: splits of the 2,560-term contraction over CTAs
+constexpr int ROUTER_KSPLIT = 2;  // prefill router: splits of the 2,560-term contraction over CTAs
 constexpr int DECODE_T_MAX = 8;  // T <= this: fused single-kernel routing (router + top-10 + grouping)
 
 // Device status bits (ws word 0).
@@ -86,6 +86,7 @@ struct WsLayout {
   size_t ids;         // int32 [T][K]
   size_t weights;     // fp32 [T][K]
   size_t inv_rms;     // fp32 [T] 1/rms of each token (residual layers, T > DECODE_T_MAX)
+  size_t xbf;         // bf16 [2][T][H] router operand: x_hi, x_lo (T > DECODE_T_MAX)
   size_t sumsq;       // fp32 [WS_NREP][T][KB_GU] per-block sums of squares, replicated (one-kernel decode layer)
   size_t dots_rep;    // fp32 [WS_NREP][T][EMAX] replicated router dot products (one-kernel decode layer)
   size_t expert_off;  // int32 [EMAX + 1]
@@ -135,6 +136,7 @@ inline WsLayout ws_layout(int T) {
   L.ids = take(sizeof(int32_t) * (size_t)P);
   L.weights = take(sizeof(float) * (size_t)P);
   L.inv_rms = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T : 0);
+  L.xbf = take(T > DECODE_T_MAX ? sizeof(uint16_t) * 2 * (size_t)T * H : 0);
   L.sumsq = take(sizeof(float) * (size_t)WS_NREP * T * KB_GU);
   L.dots_rep = take(sizeof(float) * (size_t)WS_NREP * (T < DECODE_T_MAX ? T : DECODE_T_MAX) * EMAX);
   L.expert_off = take(sizeof(int32_t) * (EMAX + 1));
@@ -257,7 +259,7 @@ namespace strata {
 // Launch accounting (instrument.cu): every launch is bracketed by kernel_begin / kernel_end, which count
 // it and record the caller's armed timing events around it.  Ids equal the ABI's STRATA_KERNEL_*.
 enum KernelId : int {
-  KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_RMSNORM, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
+  KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_ROUTER_PREP, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
   KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_COUNT
 };
 void kernel_begin(int kid, cudaStream_t s);
@@ -272,8 +274,9 @@ void kernel_end(int kid, cudaStream_t s);
 cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
                                 const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
                                 float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);
-cudaError_t launch_inv_rms(const float* x, int T, float* inv_rms, cudaStream_t s);
-cudaError_t launch_router_tc(const float* x, const float* inv_rms, int T, const uint16_t* w_router, int E,
+// Router logits of a prefill chunk: bf16 hi/lo copies of x (times 1/rms, written to inv_rms, when it is
+// non-null) in xbf, then the tensor-core GEMM into the partial-logit slices.
+cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16_t* w_router, int E, void* xbf,
                              float* parts, int* status, cudaStream_t s);
 cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, float* logits_out, int32_t* ids,
                          float* weights, cudaStream_t s);

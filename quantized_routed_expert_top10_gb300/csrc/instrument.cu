@@ -11,7 +11,7 @@ namespace strata {
 namespace {
 
 static_assert(KID_DECODE_LAYER == STRATA_KERNEL_DECODE_LAYER && KID_ROUTE_DECODE == STRATA_KERNEL_ROUTE_DECODE &&
-                  KID_RMSNORM == STRATA_KERNEL_RMSNORM && KID_ROUTER_TC == STRATA_KERNEL_ROUTER_TC &&
+                  KID_ROUTER_PREP == STRATA_KERNEL_ROUTER_PREP && KID_ROUTER_TC == STRATA_KERNEL_ROUTER_TC &&
                   KID_TOP_K == STRATA_KERNEL_TOP_K && KID_GROUP_HIST == STRATA_KERNEL_GROUP_HIST &&
                   KID_GROUP_SCAN == STRATA_KERNEL_GROUP_SCAN && KID_GROUP_SCATTER == STRATA_KERNEL_GROUP_SCATTER &&
                   KID_TC_PREPARE == STRATA_KERNEL_TC_PREPARE && KID_TC_GATHER == STRATA_KERNEL_TC_GATHER &&

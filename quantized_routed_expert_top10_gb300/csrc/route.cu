@@ -190,28 +190,12 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
 // ---------------------------------------------------------------------------------------------
 // Prefill routing kernels.
 // ---------------------------------------------------------------------------------------------
-// 1/rms of each token row for the residual layers' rmsnorm: inv[t] = 1 / sqrt(mean(x[t]^2) + 1e-6).
-// One warp per row; the consumers (router GEMM, token gather) scale x by it as they read it.
-__global__ void __launch_bounds__(256) inv_rms_kernel(const float* __restrict__ x, int T, float* __restrict__ inv) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
-  float ss = 0.f;
-#pragma unroll 4
-  for (int i = lane; i < H / 4; i += 32) {
-    const float4 v = __ldg(xr + i);
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  }
-  ss = warp_sum(ss);
-  if (lane == 0) inv[t] = 1.f / sqrtf(ss / (float)H + 1e-6f);
-}
-
 // Logits of token t = the router GEMM's ROUTER_KSPLIT partial sums added in a fixed order, plus the
 // bias; then the top-10 of the token (one warp per token).
 __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ parts, int T, int E,
                                                     const float* __restrict__ bias, float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids, float* __restrict__ weights) {
-  static_assert(ROUTER_KSPLIT == 4, "the fixed summation order below assumes four slices");
+  static_assert(ROUTER_KSPLIT == 2, "the fixed summation order below assumes two slices");
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const size_t slice = (size_t)T * EMAX;
@@ -222,7 +206,7 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
     const int e = lane + 32 * j;
     float v = 0.f;
     if (e < E) {
-      v = (__ldcg(p + e) + __ldcg(p + slice + e)) + (__ldcg(p + 2 * slice + e) + __ldcg(p + 3 * slice + e));
+      v = __ldcg(p + e) + __ldcg(p + slice + e);
       if (bias) v += __ldg(bias + e);
       if (logits_out) logits_out[(size_t)t * E + e] = v;
     }
@@ -308,11 +292,6 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
   else route_decode_kernel<8><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
   kernel_end(KID_ROUTE_DECODE, s);
 #undef STRATA_ROUTE_ARGS
-  return cudaGetLastError();
-}
-
-cudaError_t launch_inv_rms(const float* x, int T, float* inv_rms, cudaStream_t s) {
-  STRATA_LAUNCH(KID_RMSNORM, s, inv_rms_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, inv_rms));
   return cudaGetLastError();
 }
 

@@ -4,18 +4,20 @@
 // with a BF16 projection to 512 expert logits.  For a chunk of T tokens this is the GEMM
 //   logits[T][E] = X[T][2560] * Wr[E][2560]^T (+ bias),
 // run with the router rows (bf16, exact) as A (M = 128 experts) and the tokens as B (N = 128), so
-// the accumulator's TMEM lanes are experts and the epilogue's stores are coalesced along experts.  The fp32 activations (times the
-// token's 1/rms for residual layers) are split into bf16 x_hi = bf16(x) and x_lo = bf16(x - x_hi);
-// both products accumulate into the same fp32 TMEM accumulator, so each term carries x to about 16
-// significant bits (relative error ~2^-17).
-// The contraction is split four ways over CTAs (ROUTER_KSPLIT; 640 columns each) and, inside a CTA,
-// in two halves accumulated in separate TMEM columns; the CTA writes the sum of its two halves to
-// its own slice of the partial-logit buffer and the top-k kernel adds the four slices in a fixed
-// order (and the bias), so results do not depend on scheduling.  Short accumulation chains keep the
-// tensor core's accumulation error (~1e-5 on a logit) far below the 1e-4 band within which tied
-// logits may order either way.
-// CTA tile: 128 tokens x 128 experts x 640 columns, 64-wide k-blocks double-buffered in
-// 128B-swizzled shared memory, two CTAs per SM.
+// the accumulator's TMEM lanes are experts and the epilogue's stores are coalesced along experts.
+// A prep pass writes x (times the token's 1/rms for residual layers) as two bf16 matrices,
+// x_hi = bf16(x) and x_lo = bf16(x - x_hi); both products accumulate into the same fp32 TMEM
+// accumulator, so each term carries x to about 16 significant bits (relative error ~2^-17).
+// The contraction is split two ways over CTAs (ROUTER_KSPLIT; 1,280 columns each) and, inside a
+// CTA, in two halves accumulated in separate TMEM columns; a CTA writes the sum of its halves to its
+// slice of the partial-logit buffer and the top-k kernel adds the slices in a fixed order (and the
+// bias), so results do not depend on scheduling.  Short accumulation chains keep the tensor core's
+// accumulation error (~1e-5 on a logit) far below the 1e-4 band within which tied logits may order
+// either way.
+// Pipeline: one thread streams the three 128 x 64 operand tiles of each k-block with TMA (tensor
+// maps, 128-byte swizzle) into a 4-stage ring, one thread issues the MMAs, four warps drain TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "tc_common.cuh"
@@ -25,8 +27,9 @@ namespace {
 
 constexpr int RT_T = 128;  // tokens per tile (MMA N)
 constexpr int RT_E = 128;  // experts per tile (MMA M)
-constexpr int RT_THREADS = 256;
-constexpr uint32_t RT_TILE = 128 * 128;  // 128 rows x 64 bf16
+constexpr int RT_THREADS = 128;
+constexpr int RT_NS = 4;   // ring stages
+constexpr uint32_t RT_TILE = 128 * 128;     // 128 rows x 64 bf16
 constexpr uint32_t RT_STAGE = 3 * RT_TILE;  // x_hi, x_lo, router rows
 constexpr int RT_KBS = KB_GU / ROUTER_KSPLIT;  // k-blocks per CTA
 static_assert(KB_GU % ROUTER_KSPLIT == 0 && RT_KBS % 2 == 0, "even split of the contraction");
@@ -35,21 +38,68 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__global__ void __launch_bounds__(RT_THREADS, 2) router_tc_kernel(const float* __restrict__ x,
-                                                                  const float* __restrict__ inv_rms, int T,
-                                                                  const uint16_t* __restrict__ wr, int E,
-                                                                  float* __restrict__ parts, int* status) {
+// 2-D tiled TMA load of box {64 elements, 128 rows} at (k0, row0), completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int k0, int row0, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k0), "r"(row0), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// x (fp32 [T][H]) -> x_hi, x_lo (bf16 [T][H]), times 1/rms(x[t]) when inv_rms is non-null (which then
+// also receives the factors).  One warp per token row.
+__global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ x, int T,
+                                                          __nv_bfloat16* __restrict__ xh,
+                                                          __nv_bfloat16* __restrict__ xl,
+                                                          float* __restrict__ inv_rms) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
+  constexpr int PER = H / 4 / 32;  // 20 float4 per lane
+  float4 v[PER];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    v[i] = __ldg(xr + lane + 32 * i);
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  }
+  float sc = 1.f;
+  if (inv_rms) {
+    ss = warp_sum(ss);
+    sc = 1.f / sqrtf(ss / (float)H + 1e-6f);
+    if (lane == 0) inv_rms[t] = sc;
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float f[4] = {v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc};
+    __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hi[q] = __float2bfloat16_rn(f[q]);
+      lo[q] = __float2bfloat16_rn(f[q] - __bfloat162float(hi[q]));  // the difference is exact in fp32
+    }
+    const size_t o = (size_t)t * H + 4 * (lane + 32 * i);
+    *reinterpret_cast<uint2*>(xh + o) = *reinterpret_cast<const uint2*>(hi);
+    *reinterpret_cast<uint2*>(xl + o) = *reinterpret_cast<const uint2*>(lo);
+  }
+}
+
+__global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_constant__ CUtensorMap map_xh,
+                                                                  const __grid_constant__ CUtensorMap map_xl,
+                                                                  const __grid_constant__ CUtensorMap map_wr, int T,
+                                                                  int E, float* __restrict__ parts, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[2], empty[2], done;
+  __shared__ uint64_t full[RT_NS], empty[RT_NS], done;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
   const int kb0 = blockIdx.z * RT_KBS;
-  if (warp == 1) tc::tmem_alloc(&tmem_base, 256);
+  if (warp == 2) tc::tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&full[s], 8);
+    for (int s = 0; s < RT_NS; ++s) {
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -59,111 +109,129 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_tc_kernel(const float* _
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t idesc = idesc_bf16_f32(RT_E, RT_T);
-  const int r = tid >> 1, c0 = 4 * (tid & 1);  // loader: row r, chunks c0 .. c0 + 3
-  const float scale = (inv_rms && t0 + r < T) ? __ldg(inv_rms + t0 + r) : 1.f;
   bool ok = true;
-  for (int kbl = 0; kbl < RT_KBS; ++kbl) {
-    const int kb = kb0 + kbl;
-    const int s = kbl & 1;
-    uint8_t* st = smem + s * RT_STAGE;
-    if (kbl >= 2) ok = ok && mbar_wait(&empty[s], (uint32_t)((kbl / 2 - 1) & 1), status);
-    if (ok) {
-      // token row r as bf16 hi and lo parts (MMA operand B)
-      const int t = t0 + r;
-#pragma unroll
-      for (int c = c0; c < c0 + 4; ++c) {
-        float v[8];
-        if (t < T) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H + kb * QK + 8 * c));
-          const float4 b = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H + kb * QK + 8 * c + 4));
-          v[0] = a.x * scale; v[1] = a.y * scale; v[2] = a.z * scale; v[3] = a.w * scale;
-          v[4] = b.x * scale; v[5] = b.y * scale; v[6] = b.z * scale; v[7] = b.w * scale;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        }
-        __nv_bfloat16 hi[8], lo[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          hi[i] = __float2bfloat16_rn(v[i]);
-          lo[i] = __float2bfloat16_rn(v[i] - __bfloat162float(hi[i]));  // the difference is exact in fp32
-        }
-        *reinterpret_cast<uint4*>(st + tc::swz_off(r, c)) = *reinterpret_cast<uint4*>(hi);
-        *reinterpret_cast<uint4*>(st + RT_TILE + tc::swz_off(r, c)) = *reinterpret_cast<uint4*>(lo);
+  if (tid == 0) {
+    // ---- producer: three TMA tiles per k-block ----
+    int kbl = 0;
+    for (; kbl < RT_KBS; ++kbl) {
+      const int s = kbl % RT_NS;
+      if (kbl >= RT_NS && !mbar_wait(&empty[s], (uint32_t)((kbl / RT_NS - 1) & 1), status)) {
+        ok = false;
+        break;
       }
-      // router row e0 + r (MMA operand A)
-      const int e = e0 + r;
-#pragma unroll
-      for (int c = c0; c < c0 + 4; ++c) {
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (e < E) w = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H + kb * QK + 8 * c));
-        *reinterpret_cast<uint4*>(st + 2 * RT_TILE + tc::swz_off(r, c)) = w;
-      }
+      uint8_t* st = smem + (size_t)s * RT_STAGE;
+      const int k = (kb0 + kbl) * QK;
+      mbar_expect_tx(&full[s], RT_STAGE);
+      tma_load_2d(st, &map_xh, k, t0, &full[s]);
+      tma_load_2d(st + RT_TILE, &map_xl, k, t0, &full[s]);
+      tma_load_2d(st + 2 * RT_TILE, &map_wr, k, e0, &full[s]);
     }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&full[s]);
-    if (tid == 0) {
-      ok = ok && mbar_wait(&full[s], (uint32_t)((kbl / 2) & 1), status);
+    for (int back = 1; back <= RT_NS && back <= kbl; ++back)  // copies still in flight after a failure
+      mbar_wait(&full[(kbl - back) % RT_NS], (uint32_t)(((kbl - back) / RT_NS) & 1), status);
+  } else if (tid == 32) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = idesc_bf16_f32(RT_E, RT_T);
+    for (int kbl = 0; kbl < RT_KBS; ++kbl) {
+      const int s = kbl % RT_NS;
+      if (!mbar_wait(&full[s], (uint32_t)((kbl / RT_NS) & 1), status)) {
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
-      if (ok) {
-        const uint64_t ah = tc::smem_desc_sw128(smem_u32(st));
-        const uint64_t al = tc::smem_desc_sw128(smem_u32(st + RT_TILE));
-        const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + 2 * RT_TILE));
-        const int half = kbl >= RT_KBS / 2;
-        const uint32_t acc_tmem = tmem + (half ? (uint32_t)RT_T : 0u);
-        const bool first = kbl == (half ? RT_KBS / 2 : 0);
+      const uint8_t* st = smem + (size_t)s * RT_STAGE;
+      const uint64_t ah = tc::smem_desc_sw128(smem_u32(st));
+      const uint64_t al = tc::smem_desc_sw128(smem_u32(st + RT_TILE));
+      const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + 2 * RT_TILE));
+      const int half = kbl >= RT_KBS / 2;
+      const uint32_t acc_tmem = tmem + (half ? (uint32_t)RT_T : 0u);
+      const bool first = kbl == (half ? RT_KBS / 2 : 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_f16(acc_tmem, bd + 2 * kk, ah + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
-          tc::mma_f16(acc_tmem, bd + 2 * kk, al + 2 * kk, idesc, 1u);
-        }
+      for (int kk = 0; kk < 4; ++kk) {
+        tc::mma_f16(acc_tmem, bd + 2 * kk, ah + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+        tc::mma_f16(acc_tmem, bd + 2 * kk, al + 2 * kk, idesc, 1u);
       }
       tc::mma_commit(&empty[s]);
     }
+    tc::mma_commit(&done);  // after every MMA this thread issued
   }
-  if (tid == 0) tc::mma_commit(&done);
-  // epilogue: warps 0..3 own TMEM lane quadrants = expert rows; columns are tokens, so a warp's
-  // stores for one token cover 32 consecutive experts
-  if (warp < 4) {
-    ok = mbar_wait(&done, 0u, status) && ok;
-    tc::fence_after_sync();
-    const int e = e0 + 32 * warp + lane;
+  // ---- epilogue: warps 0..3 own TMEM lane quadrants = expert rows; columns are tokens, so a warp's
+  // stores for one token cover 32 consecutive experts ----
+  __syncwarp();
+  ok = mbar_wait(&done, 0u, status) && ok;
+  tc::fence_after_sync();
+  const int e = e0 + 32 * warp + lane;
 #pragma unroll 1
-    for (int ch = 0; ch < RT_T / 16; ++ch) {
-      float v[16], v2[16];
-      tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 16 * ch, v);
-      tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + RT_T + 16 * ch, v2);
-      if (ok && e < E) {
+  for (int ch = 0; ch < RT_T / 16; ++ch) {
+    float v[16], v2[16];
+    tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 16 * ch, v);
+    tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + RT_T + 16 * ch, v2);
+    if (ok && e < E) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = t0 + 16 * ch + i;
-          if (t < T) parts[((size_t)blockIdx.z * T + t) * EMAX + e] = v[i] + v2[i];
-        }
+      for (int i = 0; i < 16; ++i) {
+        const int t = t0 + 16 * ch + i;
+        if (t < T) parts[((size_t)blockIdx.z * T + t) * EMAX + e] = v[i] + v2[i];
       }
     }
-  } else if (tid == 128) {
-    mbar_wait(&done, 0u, status);  // every MMA has finished before TMEM is released
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc::tmem_dealloc(tmem, 256);
     tc::tmem_relinquish();
   }
 }
 
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][H]: boxes of 64 columns x 128 rows, 128-byte swizzle,
+// rows past the end read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_rt_attr[64];
+
 }  // namespace
 
-cudaError_t launch_router_tc(const float* x, const float* inv_rms, int T, const uint16_t* w_router, int E,
+cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16_t* w_router, int E, void* xbf,
                              float* parts, int* status, cudaStream_t s) {
-  const size_t smem = 2 * RT_STAGE + 1024;
-  cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xbf);
+  __nv_bfloat16* xl = xh + (size_t)T * H;
+  STRATA_LAUNCH(KID_ROUTER_PREP, s, router_prep_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, xh, xl, inv_rms));
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  CUtensorMap mh, ml, mw;
+  if (!make_map(&mh, xh, T) || !make_map(&ml, xl, T) || !make_map(&mw, w_router, E)) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)RT_NS * RT_STAGE + 1024;
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !g_rt_attr[dev]) {
+    if ((err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return err;
+    if (dev >= 0 && dev < 64) g_rt_attr[dev] = 1;
+  }
   dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ROUTER_KSPLIT);
-  STRATA_LAUNCH(KID_ROUTER_TC, s,
-                router_tc_kernel<<<grid, RT_THREADS, smem, s>>>(x, inv_rms, T, w_router, E, parts, status));
+  STRATA_LAUNCH(KID_ROUTER_TC, s, router_tc_kernel<<<grid, RT_THREADS, smem, s>>>(mh, ml, mw, T, E, parts, status));
   return cudaGetLastError();
 }
 
