@@ -9,8 +9,8 @@
 // x_hi = bf16(x) and x_lo = bf16(x - x_hi); both products accumulate into the same fp32 TMEM
 // accumulator, so each term carries x to about 16 significant bits (relative error ~2^-17).
 // The contraction is split two ways over CTAs (ROUTER_KSPLIT; 1,280 columns each) and, inside a
-// CTA, in two halves accumulated in separate TMEM columns; a CTA writes the sum of its halves to its
-// slice of the partial-logit buffer and the top-k kernel adds the slices in a fixed order (and the
+// CTA, into four accumulators in TMEM (even / odd k-blocks x the x_hi / x_lo products); a CTA writes
+// the sum of its four to its slice of the partial-logit buffer and the top-k kernel adds the slices in a fixed order (and the
 // bias), so results do not depend on scheduling.  Short accumulation chains keep the tensor core's
 // accumulation error (~1e-5 on a logit) far below the 1e-4 band within which tied logits may order
 // either way.
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
   const int kb0 = blockIdx.z * RT_KBS;
-  if (warp == 2) tc::tmem_alloc(&tmem_base, 256);
+  if (warp == 2) tc::tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
     for (int s = 0; s < RT_NS; ++s) {
       mbar_init(&full[s], 1);
@@ -142,13 +142,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
       const uint64_t ah = tc::smem_desc_sw128(smem_u32(st));
       const uint64_t al = tc::smem_desc_sw128(smem_u32(st + RT_TILE));
       const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + 2 * RT_TILE));
-      const int half = kbl >= RT_KBS / 2;
-      const uint32_t acc_tmem = tmem + (half ? (uint32_t)RT_T : 0u);
-      const bool first = kbl == (half ? RT_KBS / 2 : 0);
+      // four accumulation chains -- (k-block parity) x (x_hi, x_lo) -- interleaved, so consecutive MMAs
+      // never wait on each other's accumulator
+      const uint32_t acc0 = tmem + (uint32_t)((kbl & 1) * 2 * RT_T);
+      const bool first = kbl < 2;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        tc::mma_f16(acc_tmem, bd + 2 * kk, ah + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
-        tc::mma_f16(acc_tmem, bd + 2 * kk, al + 2 * kk, idesc, 1u);
+        tc::mma_f16(acc0, bd + 2 * kk, ah + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+        tc::mma_f16(acc0 + RT_T, bd + 2 * kk, al + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
       }
       tc::mma_commit(&empty[s]);
     }
@@ -162,21 +163,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   const int e = e0 + 32 * warp + lane;
 #pragma unroll 1
   for (int ch = 0; ch < RT_T / 16; ++ch) {
-    float v[16], v2[16];
-    tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 16 * ch, v);
-    tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + RT_T + 16 * ch, v2);
+    float v[4][16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c * RT_T + 16 * ch, v[c]);
     if (ok && e < E) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int t = t0 + 16 * ch + i;
-        if (t < T) parts[((size_t)blockIdx.z * T + t) * EMAX + e] = v[i] + v2[i];
+        if (t < T) parts[((size_t)blockIdx.z * T + t) * EMAX + e] = (v[0][i] + v[1][i]) + (v[2][i] + v[3][i]);
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 2) {
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, 512);
     tc::tmem_relinquish();
   }
 }
