@@ -12,15 +12,14 @@
 //             -> parts[pair][row] (fp32); two row tiles per item so each token tile is read half as often
 // Warp roles in each persistent CTA (one per SM; work items = (tile, 128-row tile of the weights)):
 //   warp 0      streams the token tile and the Q2_0 code chunk of each 64-wide k-block with
-//               cp.async.bulk into an 8-stage shared-memory ring;
-//   warps 4-11  dequantise the codes (fp16: (c + 1024) built by one LOP3 per pair, minus
-//               (1024 + q2_offset), times d -- all exact) and write them with tcgen05.st straight into
-//               a 4-stage ring of A operands in TMEM;
-//   warps 1, 3  issue tcgen05.mma (A from TMEM, the token tile from shared memory, fp32 accumulators
-//               in TMEM), one matrix's accumulation chain each, and commit to the stages' "empty"
-//               mbarriers;
-//   warps 12-15 read the accumulators with tcgen05.ld (one weight row per TMEM lane), release them,
-//               and write the epilogue while the next item's first k-blocks are dequantised;
+//               cp.async.bulk into a 6-stage ring;
+//   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
+//               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
+//               exact) in a 2-stage ring of weight tiles;
+//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into one of two TMEM accumulator buffers and
+//               commits to the stages' "empty" mbarriers;
+//   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
+//               epilogue while the next item accumulates into the other buffer;
 //   warp 2      owns the TMEM allocation.
 // Every wait is bounded (STRATA_E_TIMEOUT).
 //
@@ -34,6 +33,7 @@ namespace strata {
 namespace {
 
 constexpr int TCN = 128;        // max tokens per tile (MMA N)
+constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 64 fp16
 constexpr uint32_t B_TILE = TCN * 128;      // up to 128 token rows x 64 fp16
 
 // Position in the emitted order (0..15) of weight j of a 16-group: the order is 0,8,1,9,..,7,15.
@@ -144,13 +144,13 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const float* 
   }
 }
 
-// Dequantise one 16-byte Q2_0 code row (64 weights, scale d) into the 32 32-bit TMEM columns of one
-// A row: column 4c + m holds half2 number m of chunk c, where chunk c takes code bytes (c & 1) and
-// 2 + (c & 1) of word c / 2 (weights 4(c&1) .. +3 and 8 + 4(c&1) .. +3 of the 16-group c / 2) and half2
-// m holds field m (bits 2m, 2m + 1) of both bytes -- the emitted order.  OR-ing the field into the
-// mantissa of M_m = 2^(10 - 2m), whose last-place unit sits at bit 2m, gives M_m + code in one LOP3;
-// subtracting M_m + q2_offset and multiplying by d are exact.
-__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint32_t* out) {
+// Dequantise one 16-byte Q2_0 code row (64 weights, scale d) into the 8 swizzled 16-byte chunks of
+// row r of a K-major tile.  Chunk c holds code bytes (c & 1) and 2 + (c & 1) of word c / 2, i.e.
+// weights 4(c&1) .. +3 and 8 + 4(c&1) .. +3 of the 16-group c / 2; its half2 number m holds field m
+// (bits 2m, 2m + 1) of both bytes.  OR-ing the field into the mantissa of M_m = 2^(10 - 2m), whose
+// last-place unit sits at bit 2m, gives M_m + code in one LOP3; subtracting M_m + q2_offset and
+// multiplying by d are exact.
+__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r) {
   const __half2 d2 = __half2half2(d);
   const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
   __half2 sub[4];
@@ -159,20 +159,18 @@ __device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint32_t word = (c & 1) ? (w[c >> 1] >> 8) : w[c >> 1];
+    uint32_t out[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const uint32_t magic = (uint32_t)((25 - 2 * m) << 10) * 0x00010001u;  // half2(2^(10 - 2m))
       const uint32_t bits = (word & (0x00030003u << (2 * m))) | magic;       // half2(M_m + code)
       __half2 h = *reinterpret_cast<const __half2*>(&bits);
       h = __hmul2(__hsub2(h, sub[m]), d2);                                   // (code - q2_offset) * d
-      out[4 * c + m] = *reinterpret_cast<uint32_t*>(&h);
+      out[m] = *reinterpret_cast<uint32_t*>(&h);
     }
+    *reinterpret_cast<uint4*>(tile + tc::swz_off(r, c)) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
-
-// silu(g) * u with the fast exponential and division (relative error ~1e-6, far below the fp16
-// rounding h then takes)
-__device__ __forceinline__ float silu_mul_fast(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 
 struct TcParams {
   const uint8_t* blobs;
@@ -189,17 +187,15 @@ struct TcParams {
   int* status;
 };
 
-// Kernel geometry.  Warp 0: bulk-copy producer; warps 1 and 3: MMA issuers (one accumulation chain
-// each); warp 2: TMEM owner; warps 4..11: dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each, written
-// straight into TMEM); warps 12..15: epilogue (one TMEM lane = one weight row per thread).
+// Kernel geometry.  Warp 0: bulk-copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
+// dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each);
+// warps 12..15: epilogue (one TMEM lane = one weight row per thread).
 // gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
 // down (GU = false): item = (tile, pair of row tiles 2rp, 2rp + 1 of down): both share the token tile.
-// TMEM: accumulator of matrix j in columns [j*128, +128); weight stage s (of NS_A), matrix j in
-// columns [256 + s*64 + j*32, +32) -- the MMA's A operand comes from TMEM, so the only operand the
-// tensor core reads from shared memory is the token tile.
+// TMEM accumulator buffer b (of 2): matrix j in columns [b*256 + j*128, +128).
 constexpr int TC_THREADS = 512;
-constexpr int NS_TMA = 8;  // stages of (token tile, code chunks)
-constexpr int NS_A = 4;    // TMEM stages of dequantised weights
+constexpr int NS_TMA = 6;  // stages of (token tile, code chunks)
+constexpr int NS_A = 2;    // stages of dequantised weight tiles
 template <bool GU>
 struct TcGeo {
   static constexpr int NMAT = 2;
@@ -207,11 +203,10 @@ struct TcGeo {
   static constexpr int RTN = GU ? RT_GU : RT_D / 2;      // items per token tile
   static constexpr int CODE = GU ? GU_CHUNK : 2 * D_CHUNK; // code bytes per k-block
   static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
-  static constexpr uint32_t ACC_COLS = NMAT * TCN;     // 256
-  static constexpr uint32_t A_COLS = NMAT * 32;        // per weight stage
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + 1024;
-  static_assert(ACC_COLS + NS_A * A_COLS <= TMEM_COLS, "TMEM budget");
+  static constexpr uint32_t A_STAGE = NMAT * A_TILE;
+  static constexpr uint32_t TMEM_BUF = NMAT * TCN;     // accumulator columns per buffer
+  static constexpr uint32_t TMEM_COLS = 2 * TMEM_BUF;  // double buffered
+  static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
 };
 
 template <bool GU>
@@ -220,8 +215,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* tma_ring = smem;
+  uint8_t* a_ring = smem + (size_t)NS_TMA * G::TMA_STAGE;
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
-  __shared__ uint64_t tmem_full, tmem_empty, mma_done;
+  __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
@@ -230,15 +226,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   if (tid == 0) {
     for (int s = 0; s < NS_TMA; ++s) {
       mbar_init(&full_tma[s], 1);
-      mbar_init(&empty_tma[s], G::NMAT);  // one commit per MMA issuer
+      mbar_init(&empty_tma[s], 1);
     }
     for (int s = 0; s < NS_A; ++s) {
       mbar_init(&full_a[s], 8);
-      mbar_init(&empty_a[s], G::NMAT);
+      mbar_init(&empty_a[s], 1);
     }
-    mbar_init(&tmem_full, G::NMAT);
-    mbar_init(&tmem_empty, 4);
-    mbar_init(&mma_done, G::NMAT);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4);
+    }
+    mbar_init(&mma_done, 1);
     fence_mbar_init();
     s_fail = 0;
   }
@@ -246,7 +244,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t tmem_a = tmem + G::ACC_COLS;
   const int n_items = p.counts[1] * G::RTN;
   int* status = p.status;
 
@@ -286,22 +283,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       for (int back = 1; back <= NS_TMA && back <= it; ++back)  // copies still in flight after a failure
         mbar_wait(&full_tma[(it - back) % NS_TMA], (uint32_t)(((it - back) / NS_TMA) & 1), status);
     }
-  } else if (warp == 1 || warp == 3) {
-    // ---------------- MMA issuers: warp 1 the first matrix's accumulation chain, warp 3 the second's
-    // (an MMA into the accumulator the previous one wrote waits for it; two issuing threads keep two
-    // independent chains in flight) ----------------
-    const int mat = warp == 1 ? 0 : 1;
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
     if (lane == 0) {
       int it = 0, ti = 0;
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x, ++ti) {
         const TcTile tl = p.tiles[item / G::RTN];
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
-        if (ti >= 1 && !mbar_wait(&tmem_empty, (uint32_t)((ti - 1) & 1), status)) {  // epilogue drained
+        const int b = ti & 1;
+        if (ti >= 2 && !mbar_wait(&tmem_empty[b], (uint32_t)(((ti >> 1) - 1) & 1), status)) {
           s_fail = 1;
           break;
         }
         tc::fence_after_sync();
+        const uint32_t acc = tmem + b * G::TMEM_BUF;
         for (int kb = 0; kb < G::KBN; ++kb, ++it) {
           const int s = it % NS_TMA, sa = it % NS_A;
           if (!mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status) ||
@@ -311,24 +307,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
           }
           tc::fence_after_sync();
           const uint64_t bd = tc::smem_desc_sw128(smem_u32(tma_ring + (size_t)s * G::TMA_STAGE));
+          const uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_f16_ts(tmem + mat * TCN, tmem_a + sa * G::A_COLS + mat * 32 + 8 * kk, bd + 2 * kk, idesc,
-                           (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int mat = 0; mat < G::NMAT; ++mat) {
+            const uint64_t ad = tc::smem_desc_sw128(smem_u32(ast + mat * A_TILE));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_f16(acc + mat * TCN, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
           tc::mma_commit(&empty_tma[s]);
           tc::mma_commit(&empty_a[sa]);
         }
         if (s_fail) break;
-        tc::mma_commit(&tmem_full);
+        tc::mma_commit(&tmem_full[b]);
       }
       tc::mma_commit(&mma_done);  // every MMA this thread issued has finished before TMEM is released
       mbar_wait(&mma_done, 0u, status);
     }
   } else if (warp >= 4 && warp < 12) {
-    // ---------------- dequantisers: codes -> fp16 weights -> TMEM (A operand) ----------------
+    // ---------------- dequantisers ----------------
     const int dt = tid - 128;
-    const int row = dt & 127, sub = dt >> 7;  // matrix of the item; row = this warp's TMEM lane quadrant
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int row = dt & 127, sub = dt >> 7;  // matrix of the item
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -336,10 +335,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         const int s = it % NS_TMA, sa = it % NS_A;
         if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], (uint32_t)((it / NS_A - 1) & 1), status);
         ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status);
-        tc::fence_after_sync();
-        uint32_t out[32];
         if (ok) {
           const uint8_t* code = tma_ring + (size_t)s * G::TMA_STAGE + B_TILE;
+          uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
           // gate/up: 8 slab pieces {gate codes, up codes, {gate d, up d} per row}; down: two chunks
           uint4 cw;
           __half d;
@@ -353,13 +351,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
             cw = *reinterpret_cast<const uint4*>(cb + 16 * row);
             d = *reinterpret_cast<const __half*>(cb + 2048 + 2 * row);
           }
-          dequant_row(cw, d, p.q2_offset, out);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = 0u;
+          dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
         }
-        tc::tmem_st32(tmem_a + lane_base + sa * G::A_COLS + sub * 32, out);
-        tc::fence_before_sync();
+        tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&full_a[sa]);
       }
@@ -374,37 +368,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       const TcTile tl = p.tiles[item / G::RTN];
       const int rt = item % G::RTN;
       const int nrows = (tl.n + 15) / 16 * 16;
-      ok = ok && mbar_wait(&tmem_full, (uint32_t)(ti & 1), status);
+      const int b = ti & 1;
+      ok = ok && mbar_wait(&tmem_full[b], (uint32_t)((ti >> 1) & 1), status);
       tc::fence_after_sync();
-      const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
+      const uint32_t acc = tmem + b * G::TMEM_BUF + ((uint32_t)(32 * q) << 16);
       if (GU) {
-        // h = silu(g) * u for this row and every token column, packed to fp16 in registers, then the
-        // accumulator is released before the stores
         const int k = rt * 128 + erow;  // h index = the down projection's contraction index
         const int kbd = k >> 6, k64 = k & 63;
         const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
-        __half hv[TCN];
+        for (int ch = 0; ch < nrows / 16; ++ch) {
+          float g[16], u[16];
+          tc::tmem_ld16(acc + 16 * ch, g);
+          tc::tmem_ld16(acc + TCN + 16 * ch, u);
+          if (ok) {
 #pragma unroll
-        for (int ch = 0; ch < TCN / 16; ++ch) {
-          if (ch < nrows / 16) {
-            float g[16], u[16];
-            tc::tmem_ld16(acc + 16 * ch, g);
-            tc::tmem_ld16(acc + TCN + 16 * ch, u);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) hv[16 * ch + i] = __float2half_rn(silu_mul_fast(g[i], u[i]));
-          }
-        }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tmem_empty);
-        if (ok) {
-#pragma unroll
-          for (int col = 0; col < TCN; ++col) {
-            if (col < tl.n) {
-              const int64_t hrow = tl.q0pad + col;
-              __half* dst = reinterpret_cast<__half*>(p.hg + ((int64_t)kbd * p.rows_cap + hrow) * 128 +
-                                                      (((pos >> 3) ^ (hrow & 7)) << 4)) + (pos & 7);
-              *dst = hv[col];
+            for (int i = 0; i < 16; ++i) {
+              const int col = 16 * ch + i;
+              if (col < tl.n) {
+                const int64_t hrow = tl.q0pad + col;
+                __half* dst = reinterpret_cast<__half*>(p.hg + ((int64_t)kbd * p.rows_cap + hrow) * 128 +
+                                                        (((pos >> 3) ^ (hrow & 7)) << 4)) + (pos & 7);
+                *dst = __float2half_rn(silu_mul(g[i], u[i]));
+              }
             }
           }
         }
@@ -427,10 +412,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
             }
           }
         }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tmem_empty);
       }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[b]);
     }
   }
   tc::fence_before_sync();
