@@ -168,7 +168,14 @@ KERNEL_SOURCES = {
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture of the
 # workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
 # sources at capture time: once a source changes the figure no longer describes the kernel (null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (28,997,632 / 28,997,376 /
+    # 28,997,504 B read, 0 B written)
+    ("verify_4tok_1layer", "DECODE_LAYER"): (28997504, "e1d7d92a181e9284"),
+    # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (281050624 + 12867840, "c85a0ef53f848cde"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (121381888 + 146027264, "c85a0ef53f848cde"),
+}
 
 
 def source_digest(kernel):
