@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   const int T = p.T, E = p.E, P = T * K;
   int* bar = p.sync + WS_SYNC_BAR;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
-  int* h_cnt = p.sync + WS_SYNC_HREADY;
-  int* cnt_dn = p.sync + WS_SYNC_CNT_DN;
+  int* h_cnt = p.sync + WS_SYNC_HREADY;  // expert slot j at h_cnt[WS_SYNC_STRIDE * j]
+  int* cnt_dn = p.sync + WS_SYNC_CNT_DN;  // row tile r at cnt_dn[WS_SYNC_STRIDE * r]
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -224,12 +224,13 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     }
   }
 
-  // ---- grid barrier ----
+  // ---- grid barrier: CTA c counts into group c % 16, the last of a group into the top counter, the
+  // last group releases 16 flags (acq_rel adds: each step makes everything before it visible) ----
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(bar, 1) == G - 1) {
-      __threadfence();  // release: every CTA's phase-1 writes happen before any flag is seen
+    const int grp = c % WS_NREP, grp_size = (G - grp + WS_NREP - 1) / WS_NREP;
+    if (atom_acq_rel_add(p.sync + WS_SYNC_GRP + 32 * grp, 1) == grp_size - 1 &&
+        atom_acq_rel_add(bar, 1) == min(G, WS_NREP) - 1) {
 #pragma unroll
       for (int r = 0; r < WS_NREP; ++r) st_relaxed(p.sync + WS_SYNC_REL + 32 * r, 1);
     }
@@ -479,9 +480,12 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           p.hf[(size_t)(q0 + ii) * FF + sl * SLAB + r2] = silu_mul(g, uu);
         }
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) atomicAdd(&h_cnt[j], 1);
+        __syncthreads();  // every h store issued; the stage and the reduction buffer are free
+        if (tid == 0) {
+          red_release_add(&h_cnt[WS_SYNC_STRIDE * j], 1);
+          if (u + G * NS < n_units) issue(u + G * NS, i + NS);
+        }
+        continue;
       } else {
         // -------- down unit: row tile rtd of expert slot j --------
         const int v = u - n_gu;
@@ -492,7 +496,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         float* sh = reinterpret_cast<float*>(sqx);
         static_assert(sizeof(float) * TT * FF <= sizeof(QBlock) * TT * KB_GU, "h fits the activation space");
         if (tid == 0) {
-          bool okh = spin_until_geq(&h_cnt[j], DF_GU, p.status);
+          bool okh = spin_until_geq(&h_cnt[WS_SYNC_STRIDE * j], DF_GU, p.status);
           if (s_qx_pending) okh = mbar_wait(&bar_qx, 0u, p.status) && okh;  // (only if no gate/up unit ran)
           s_qx_pending = 0;
           if (okh) {
@@ -614,12 +618,10 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           if (ii < n) p.parts[(size_t)s_pair[q0 + ii] * H + row] = acc[ii];
         }
         const int row = rtd * RT + tid;  // combine: one output row per thread
-        __threadfence();
         __syncthreads();
-        if (tid == 0) s_flag = (atomicAdd(&cnt_dn[rtd], 1) == D - 1) ? 1 : 0;
+        if (tid == 0) s_flag = (atom_acq_rel_add(&cnt_dn[WS_SYNC_STRIDE * rtd], 1) == D - 1) ? 1 : 0;
         __syncthreads();
         if (s_flag) {
-          __threadfence();
           float pv[TT * K], xv[TT];  // every load first, then the k-ordered sums
 #pragma unroll
           for (int q = 0; q < TT * K; ++q) pv[q] = (q < T * K) ? __ldcg(p.parts + (size_t)q * H + row) : 0.f;
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
               p.out[(size_t)tt * H + row] = p.residual ? xv[tt] + a : a;
             }
           }
-          if (tid == 0) cnt_dn[rtd] = 0;
+          if (tid == 0) cnt_dn[WS_SYNC_STRIDE * rtd] = 0;
         }
       }
       __syncthreads();  // everyone is done with this stage and with sq / red
