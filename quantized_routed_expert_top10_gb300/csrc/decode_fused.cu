@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           }
           const uint8_t* xs = reinterpret_cast<const uint8_t*>(sqx);
           float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll 2
           for (int kk = 0; kk < KB_GU / 4; ++kk) {
             const int kb = warp * (KB_GU / 4) + kk;
             const uint8_t* piece = stage + kb * SLAB_KB;
@@ -391,20 +391,22 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             codes_to_half2(wg1, subq, hg1);
             codes_to_half2(wu0, subq, hu0);
             codes_to_half2(wu1, subq, hu1);
-            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+            // even and odd k-steps into separate accumulators: two independent MMA chains per matrix
+            float cg[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float cu[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
               const uint32_t a_g[4] = {hg0[2 * s], hg1[2 * s], hg0[2 * s + 1], hg1[2 * s + 1]};
               const uint32_t a_u[4] = {hu0[2 * s], hu1[2 * s], hu0[2 * s + 1], hu1[2 * s + 1]};
-              mma_16816(cg, a_g, bq[2 * s], bq[2 * s + 1]);
-              mma_16816(cu, a_u, bq[2 * s], bq[2 * s + 1]);
+              mma_16816(cg[s & 1], a_g, bq[2 * s], bq[2 * s + 1]);
+              mma_16816(cu[s & 1], a_u, bq[2 * s], bq[2 * s + 1]);
             }
             const float dg0 = __low2float(sc0), du0 = __high2float(sc0);
             const float dg1 = __low2float(sc1), du1 = __high2float(sc1);
-            ag[0] = fmaf(dg0, cg[0], ag[0]); ag[1] = fmaf(dg0, cg[1], ag[1]);
-            ag[2] = fmaf(dg1, cg[2], ag[2]); ag[3] = fmaf(dg1, cg[3], ag[3]);
-            au[0] = fmaf(du0, cu[0], au[0]); au[1] = fmaf(du0, cu[1], au[1]);
-            au[2] = fmaf(du1, cu[2], au[2]); au[3] = fmaf(du1, cu[3], au[3]);
+            ag[0] = fmaf(dg0, cg[0][0] + cg[1][0], ag[0]); ag[1] = fmaf(dg0, cg[0][1] + cg[1][1], ag[1]);
+            ag[2] = fmaf(dg1, cg[0][2] + cg[1][2], ag[2]); ag[3] = fmaf(dg1, cg[0][3] + cg[1][3], ag[3]);
+            au[0] = fmaf(du0, cu[0][0] + cu[1][0], au[0]); au[1] = fmaf(du0, cu[0][1] + cu[1][1], au[1]);
+            au[2] = fmaf(du1, cu[0][2] + cu[1][2], au[2]); au[3] = fmaf(du1, cu[0][3] + cu[1][3], au[3]);
           }
           // red[warp][mat][row][column]: the four warps' k ranges, added below in warp order
           float* rf = reinterpret_cast<float*>(red);
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           }
           const uint8_t* hx = reinterpret_cast<const uint8_t*>(sq);
           float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 1
+#pragma unroll 2
           for (int kb = 0; kb < KB_D; ++kb) {
             const uint8_t* chunk = stage + kb * D_CHUNK;
             uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
@@ -573,14 +575,14 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
               codes_to_half2(*reinterpret_cast<const uint32_t*>(chunk + 16 * R1 + 4 * t4), subq, h1);
               const float d0 = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * R0));
               const float d1 = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * R1));
-              float cc[4] = {0.f, 0.f, 0.f, 0.f};
+              float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
               for (int s = 0; s < 4; ++s) {
                 const uint32_t a[4] = {h0[2 * s], h1[2 * s], h0[2 * s + 1], h1[2 * s + 1]};
-                mma_16816(cc, a, bq[2 * s], bq[2 * s + 1]);
+                mma_16816(cc[s & 1], a, bq[2 * s], bq[2 * s + 1]);
               }
-              acc[rg][0] = fmaf(d0, cc[0], acc[rg][0]); acc[rg][1] = fmaf(d0, cc[1], acc[rg][1]);
-              acc[rg][2] = fmaf(d1, cc[2], acc[rg][2]); acc[rg][3] = fmaf(d1, cc[3], acc[rg][3]);
+              acc[rg][0] = fmaf(d0, cc[0][0] + cc[1][0], acc[rg][0]); acc[rg][1] = fmaf(d0, cc[0][1] + cc[1][1], acc[rg][1]);
+              acc[rg][2] = fmaf(d1, cc[0][2] + cc[1][2], acc[rg][2]); acc[rg][3] = fmaf(d1, cc[0][3] + cc[1][3], acc[rg][3]);
             }
           }
 #pragma unroll
