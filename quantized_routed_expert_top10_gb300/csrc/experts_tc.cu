@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full_a[sa]);
+        if (lane == 0) mbar_arrive(&full_a[sa]);
       }
     }
   } else if (warp >= 12) {
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tmem_empty[b]);
+      if (lane == 0) mbar_arrive(&tmem_empty[b]);
     }
   }
   tc::fence_before_sync();

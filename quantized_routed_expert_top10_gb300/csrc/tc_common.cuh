@@ -95,9 +95,6 @@ __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence
 // generic-proxy shared-memory writes -> visible to the tensor core (async proxy)
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // 32 lanes x 32 bits x 16 columns: thread t of the warp gets lane (quadrant*32 + t), 16 consecutive columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
