@@ -67,20 +67,19 @@ struct __align__(16) Tile {
 constexpr size_t WS_HEADER = 12288;
 constexpr size_t WS_STATUS = 0;     // int32 status word
 constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
-// Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): grid barrier top counter,
-// exit counter, per expert slot h counters (finished gate/up slabs) and per down row tile counters
-// (one 32-byte sector each), barrier release flags and the barrier's 16 group counters (one 128-byte
-// line each), so CTAs polling or bumping different words do not queue on the same line.
+// Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): exit counter, per expert
+// slot h counters (finished gate/up slabs) and per down row tile counters (one 32-byte sector each),
+// and the grid barrier's arrival counters (one 128-byte line each), so CTAs polling or bumping
+// different words do not queue on the same line.
 constexpr size_t WS_SYNC = 4096;
-constexpr int WS_SYNC_BAR = 0;
 constexpr int WS_SYNC_EXIT = 1;
 constexpr int WS_SYNC_STRIDE = 8;  // words between per-expert / per-tile counters
 constexpr int WS_SYNC_HREADY = 32;
 constexpr int WS_SYNC_CNT_DN = WS_SYNC_HREADY + WS_SYNC_STRIDE * DECODE_T_MAX * K;
-constexpr int WS_SYNC_REL = ((WS_SYNC_CNT_DN + WS_SYNC_STRIDE * RT_D + 31) / 32) * 32;  // release flags
-constexpr int WS_NREP = 16;                          // replicas of data every CTA reads at once
-constexpr int WS_SYNC_GRP = WS_SYNC_REL + 32 * WS_NREP;  // barrier group counters
-constexpr int WS_SYNC_WORDS = WS_SYNC_GRP + 32 * WS_NREP;
+constexpr int WS_NARR = 8;         // grid barrier arrival counters (CTA c counts into c % WS_NARR)
+constexpr int WS_SYNC_ARR = ((WS_SYNC_CNT_DN + WS_SYNC_STRIDE * RT_D + 31) / 32) * 32;
+constexpr int WS_NREP = 16;        // replicas of data every CTA reads at once
+constexpr int WS_SYNC_WORDS = WS_SYNC_ARR + 32 * WS_NARR;
 static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sync words must fit the header");
 
 struct WsLayout {

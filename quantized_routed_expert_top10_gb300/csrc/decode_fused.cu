@@ -137,12 +137,12 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ int s_pair[TT * K];
   __shared__ float s_rpart[4][TT];
   __shared__ float s_bias[EMAX];
+  __shared__ TopKScratch s_topk[DF_THREADS / 32];
   __shared__ int32_t s_qtmp[4][64];
   __shared__ int s_flag, s_ok, s_nact;
 
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
-  int* bar = p.sync + WS_SYNC_BAR;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
   int* h_cnt = p.sync + WS_SYNC_HREADY;  // expert slot j at h_cnt[WS_SYNC_STRIDE * j]
   int* cnt_dn = p.sync + WS_SYNC_CNT_DN;  // row tile r at cnt_dn[WS_SYNC_STRIDE * r]
@@ -159,7 +159,27 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     fence_mbar_init();
     s_ok = 1;
   }
-  for (int e = tid; e < E; e += DF_THREADS) s_bias[e] = p.bias ? __ldg(p.bias + e) : 0.f;
+  // loads for later steps, issued first so their latency hides under the router rows': the bias
+  // (used by the top-k) and this warp's first block of x to quantise
+  float bias_v[EMAX / DF_THREADS];
+#pragma unroll
+  for (int i = 0; i < EMAX / DF_THREADS; ++i) {
+    const int e = tid + DF_THREADS * i;
+    bias_v[i] = (p.bias && e < E) ? __ldg(p.bias + e) : 0.f;
+  }
+  const int t4x = lane >> 3, qx8 = lane & 7;  // fragment-order position of this lane's x pair (T >= 2)
+  auto load_block = [&](int b, float2& v, float& xa, float& xb) {
+    const int t = b / KB_GU, kb = b % KB_GU;
+    v = __ldg(reinterpret_cast<const float2*>(p.x + (size_t)t * H + kb * QK + 2 * lane));
+    if constexpr (MMA) {
+      const float* src = p.x + (size_t)t * H + kb * QK + 16 * t4x + 4 * (qx8 >> 2) + (qx8 & 3);
+      xa = __ldg(src);
+      xb = __ldg(src + 8);
+    }
+  };
+  float2 v0 = make_float2(0.f, 0.f);
+  float xa0 = 0.f, xb0 = 0.f;
+  if (c + G * warp < T * KB_GU) load_block(c + G * warp, v0, xa0, xb0);
 
   // ---- 1. router dot products (two warps per row), x quantisation, block sums of squares ----
   for (int e0 = c; e0 < E; e0 += 2 * G) {
@@ -209,32 +229,31 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   }
   for (int b = c + G * warp; b < T * KB_GU; b += 4 * G) {
     const int t = b / KB_GU, kb = b % KB_GU;
-    const float2 v = __ldg(reinterpret_cast<const float2*>(p.x + (size_t)t * H + kb * QK + 2 * lane));
+    float2 v = v0;
+    float xa = xa0, xb = xb0;
+    if (b != c + G * warp) load_block(b, v, xa, xb);
     const float ss = warp_sum(v.x * v.x + v.y * v.y);
     if (lane == 0)
 #pragma unroll
       for (int r = 0; r < WS_NREP; ++r) p.sumsq[(size_t)r * T * KB_GU + b] = ss;
     if constexpr (MMA) {  // fp16 x in fragment order: xs[kb][t4][token][16 halves]
-      const int t4 = lane >> 3, q = lane & 7, bb = q >> 2, mm = q & 3;
-      const float* src = p.x + (size_t)t * H + kb * QK + 16 * t4 + 4 * bb + mm;
-      const __half2 x2 = __floats2half2_rn(__ldg(src), __ldg(src + 8));
-      reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.qx) + ((size_t)(kb * 4 + t4) * T + t) * 32)[q] = x2;
+      const __half2 x2 = __floats2half2_rn(xa, xb);
+      reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.qx) + ((size_t)(kb * 4 + t4x) * T + t) * 32)[qx8] = x2;
     } else {
       quantise_block_warp(v.x, v.y, p.q2_offset, p.qx + b, s_qtmp[warp]);
     }
   }
 
-  // ---- grid barrier: CTA c counts into group c % 16, the last of a group into the top counter, the
-  // last group releases 16 flags (acq_rel adds: each step makes everything before it visible) ----
+#pragma unroll
+  for (int i = 0; i < EMAX / DF_THREADS; ++i)
+    if (tid + DF_THREADS * i < E) s_bias[tid + DF_THREADS * i] = bias_v[i];
+
+  // ---- grid barrier: each CTA makes its writes visible and counts into one of WS_NARR counters
+  // (release add, no reply awaited), then polls all of them ----
   __syncthreads();
   if (tid == 0) {
-    const int grp = c % WS_NREP, grp_size = (G - grp + WS_NREP - 1) / WS_NREP;
-    if (atom_acq_rel_add(p.sync + WS_SYNC_GRP + 32 * grp, 1) == grp_size - 1 &&
-        atom_acq_rel_add(bar, 1) == min(G, WS_NREP) - 1) {
-#pragma unroll
-      for (int r = 0; r < WS_NREP; ++r) st_relaxed(p.sync + WS_SYNC_REL + 32 * r, 1);
-    }
-    s_ok = spin_until_geq(p.sync + WS_SYNC_REL + 32 * (c % WS_NREP), 1, p.status) ? 1 : 0;
+    red_release_add(p.sync + WS_SYNC_ARR + 32 * (c % WS_NARR), 1);
+    s_ok = spin_grid_arrivals<WS_NARR>(p.sync + WS_SYNC_ARR, 32, G, p.status) ? 1 : 0;
     if (s_ok) {
       // every token's quantised activations (written by all CTAs before the barrier) into shared
       // memory; the async-proxy copy is ordered after the acquire by the proxy fence
@@ -249,30 +268,26 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 
   // ---- 2. top-10 and grouping, redundantly in every CTA ----
   if (s_ok) {
-    if (tid < T) {
-      float inv = 1.f;
-      if (p.residual) {
-        float s = 0.f;
-        const float* ssq = p.sumsq + ((size_t)(c % WS_NREP) * T + tid) * KB_GU;
-        for (int kb = 0; kb < KB_GU; ++kb) s += __ldcg(ssq + kb);
-        inv = 1.f / sqrtf(s / (float)H + 1e-6f);
-      }
-      s_inv[tid] = inv;
-    }
     if (tid == 0) s_nact = 0;
-    __syncthreads();
     for (int t = warp; t < T; t += 4) {
-      const float inv = s_inv[t];
       const float* d = p.dots + ((size_t)(c % WS_NREP) * T + t) * EMAX;
       float lg[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = lane + 32 * j;
-        lg[j] = (e < E) ? __ldcg(d + e) * inv + s_bias[e] : 0.f;
+      for (int j = 0; j < 16; ++j) lg[j] = (lane + 32 * j < E) ? __ldcg(d + lane + 32 * j) : 0.f;
+      float inv = 1.f;  // rmsnorm of a residual layer: 1 / rms from the 40 block sums of squares
+      if (p.residual) {
+        const float* ssq = p.sumsq + ((size_t)(c % WS_NREP) * T + t) * KB_GU;
+        float s = __ldcg(ssq + lane);
+        if (lane + 32 < KB_GU) s += __ldcg(ssq + lane + 32);
+        inv = 1.f / sqrtf(warp_sum(s) / (float)H + 1e-6f);
       }
+      if (lane == 0) s_inv[t] = inv;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (lane + 32 * j < E) lg[j] = lg[j] * inv + s_bias[lane + 32 * j];
       int id;
       float w;
-      top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, &id, &w);
+      top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, s_topk[warp], &id, &w);
       if (lane < K) {
         s_ids[t * K + lane] = id;
         s_w[t * K + lane] = w;

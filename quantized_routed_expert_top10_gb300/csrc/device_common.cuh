@@ -5,7 +5,6 @@
 namespace strata {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any wait in a correct run
-constexpr float kRenormFloor = 6.103515625e-05f;            // 2^-14, ggml's lower clamp
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -95,6 +94,34 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Bounded wait (one thread) until all G CTAs of the grid have arrived on the N counters at base
+// (stride words apart; CTA c adds 1 to counter c % N): counter i reaches the number of c < G with
+// c % N == i.  The counters are polled with relaxed loads, all N in flight at once; the fence after
+// the last reads makes them acquires.  False and ST_TIMEOUT if the grid never completes.
+template <int N>
+__device__ __forceinline__ bool spin_grid_arrivals(const int* base, int stride, int G, int* status) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) all &= ld_relaxed(base + stride * i) >= (G - i + N - 1) / N;
+    if (all) break;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      set_status(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+  fence_acq_rel_gpu();
+  return true;
+}
+
 // Bounded spin until *p >= target (one thread); false and ST_TIMEOUT if it never got there.
 __device__ __forceinline__ bool spin_until_geq(const int* p, int target, int* status) {
   if (ld_acquire(p) >= target) return true;
@@ -119,83 +146,102 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* f) {
   f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xffff0000u);
 }
 
-// top-k of one token by one warp.  logit(e) is the logit of expert e (E % 32 == 0, E <= 512):
-// softmax over E, the K largest probabilities in descending order (equal values: lower id first),
-// renormalised as p / max(sum, 2^-14).  Lane k (< K) returns the (id, weight) of rank k.
-// Each lane holds 16 candidates; every round takes a tree argmax over the lane's candidates and a
-// butterfly argmax over the warp (a total order on (p, -id), so all lanes agree), then removes the
-// winner.  The round loop is kept rolled so the code stays small.
+// Orderable key of a logit: a larger float gets a larger unsigned key (-0 one below +0).  No number
+// maps to 0, which marks an absent or removed entry.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+constexpr int TOPK_CAP = 64;  // candidates ranked directly; more (mass ties) take the round-by-round path
+struct TopKScratch {          // one per warp, in shared memory
+  uint2 cand[TOPK_CAP];       // (key, expert id)
+  uint2 sel[K];               // rank k -> (key, expert id)
+};
+
+// top-k of one token by one warp.  logit(e) is the logit of expert e (E % 32 == 0, 32 <= E <= 512).
+// The stable descending order of the softmax probabilities is the order of the logits (exp is
+// increasing), equal logits by lower id; lane k (< K) returns the (id, weight) of rank k.
+// Renormalisation: p_i / max(sum of the K selected p, 2^-14) with p_i = exp(l_i - max) / z.  The K
+// largest of E probabilities sum to at least K / E >= 10 / 512 > 2^-14, so the clamp never binds and
+// the weight is exp(l_i - l_0) / sum over the selected of exp(l_j - l_0); z is never needed.
+// Selection: tau = the K-th largest of the 32 lane maxima; the K lanes whose maxima rank above it
+// hold K keys >= tau, so every top-K key is >= tau.  The keys >= tau (typically 10-25) are compacted
+// into shared memory and each is ranked by counting the candidates ahead of it (key, then lower id):
+// a few short independent steps instead of K dependent warp-wide argmax rounds.
 template <typename LogitFn>
-__device__ __forceinline__ void top_k_warp_fn(LogitFn logit, int E, int* out_id, float* out_w) {
+__device__ __forceinline__ void top_k_warp_fn(LogitFn logit, int E, TopKScratch& sc, int* out_id, float* out_w) {
   const int lane = threadIdx.x & 31;
   const int per = E >> 5;
-  float p[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) p[j] = (j < per) ? logit(lane + 32 * j) : -INFINITY;
-  float m = p[0];
-#pragma unroll
-  for (int j = 1; j < 16; ++j) m = fmaxf(m, p[j]);
-  m = warp_max(m);
-  float z = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    p[j] = (j < per) ? expf(p[j] - m) : 0.f;
-    z += p[j];
-  }
-  z = warp_sum(z);
-  const float rz = 1.f / z;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) p[j] = (j < per) ? p[j] * rz : -1.f;
-  // Keys: probability bits + 1 for live candidates (p >= 0, so bit order = value order), 0 for
-  // removed or absent ones.  Each round: per-lane tree argmax (lower j on ties), warp max of the
-  // keys with redux.sync, then the lowest expert id among the lanes holding that max.
   uint32_t key[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) key[j] = (j < per) ? __float_as_uint(p[j]) + 1u : 0u;
-  float s = 0.f, my_p = 0.f;
-  int my_id = 0;
-#pragma unroll 1
-  for (int k = 0; k < K; ++k) {
-    uint32_t v8[8];
-    int j8[8];
+  for (int j = 0; j < 16; ++j) key[j] = (j < per) ? logit_key(logit(lane + 32 * j)) : 0u;
+  uint32_t mk = key[0];
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      const bool r = key[2 * a + 1] > key[2 * a];
-      v8[a] = r ? key[2 * a + 1] : key[2 * a];
-      j8[a] = r ? 2 * a + 1 : 2 * a;
-    }
+  for (int j = 1; j < 16; ++j) mk = max(mk, key[j]);
+  int r = 0;  // rank of this lane's maximum among the lanes' (maximum, lane)
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const bool r = v8[2 * a + 1] > v8[2 * a];
-      v8[a] = r ? v8[2 * a + 1] : v8[2 * a];
-      j8[a] = r ? j8[2 * a + 1] : j8[2 * a];
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-      const bool r = v8[2 * a + 1] > v8[2 * a];
-      v8[a] = r ? v8[2 * a + 1] : v8[2 * a];
-      j8[a] = r ? j8[2 * a + 1] : j8[2 * a];
-    }
-    const bool r = v8[1] > v8[0];
-    const uint32_t bk = r ? v8[1] : v8[0];
-    const uint32_t bid = (uint32_t)(lane + 32 * (r ? j8[1] : j8[0]));
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t id = __reduce_min_sync(0xffffffffu, bk == mx ? bid : 0xffffffffu);
-    if ((int)(id & 31u) == lane) {
-      const int jw = (int)(id >> 5);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j == jw) key[j] = 0u;
-    }
-    const float pv = __uint_as_float(mx - 1u);
-    if (lane == k) {
-      my_p = pv;
-      my_id = (int)id;
-    }
-    s += pv;
+  for (int o = 1; o < 32; ++o) {
+    const int src = (lane + o) & 31;
+    const uint32_t v = __shfl_sync(0xffffffffu, mk, src);
+    r += (v > mk || (v == mk && src < lane)) ? 1 : 0;
   }
-  *out_id = my_id;
-  *out_w = my_p / fmaxf(s, kRenormFloor);
+  const uint32_t tau = __shfl_sync(0xffffffffu, mk, __ffs(__ballot_sync(0xffffffffu, r == K - 1)) - 1);
+  const uint32_t below = (1u << lane) - 1u;
+  int C = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool is = key[j] >= tau;
+    const uint32_t bal = __ballot_sync(0xffffffffu, is);
+    const int pos = C + __popc(bal & below);
+    if (is && pos < TOPK_CAP) sc.cand[pos] = make_uint2(key[j], (uint32_t)(lane + 32 * j));
+    C += __popc(bal);
+  }
+  __syncwarp();
+  if (C <= TOPK_CAP) {
+    for (int i = lane; i < C; i += 32) {
+      const uint2 me = sc.cand[i];
+      int rank = 0;
+#pragma unroll 4
+      for (int q = 0; q < C; ++q) {
+        const uint2 o = sc.cand[q];
+        rank += (o.x > me.x || (o.x == me.x && o.y < me.y)) ? 1 : 0;
+      }
+      if (rank < K) sc.sel[rank] = me;
+    }
+  } else {
+    // more than TOPK_CAP keys tie around the threshold: K rounds of a warp argmax on (key, -id)
+#pragma unroll 1
+    for (int k = 0; k < K; ++k) {
+      uint32_t bk = key[0];
+      int bj = 0;
+#pragma unroll
+      for (int j = 1; j < 16; ++j)
+        if (key[j] > bk) {
+          bk = key[j];
+          bj = j;
+        }
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t id = __reduce_min_sync(0xffffffffu, bk == mx ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
+      if ((int)(id & 31u) == lane) {
+        const int jw = (int)(id >> 5);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j == jw) key[j] = 0u;
+      }
+      if (lane == 0) sc.sel[k] = make_uint2(mx, id);
+    }
+  }
+  __syncwarp();
+  const uint2 me = sc.sel[lane < K ? lane : 0];
+  const float l0 = key_logit(sc.sel[0].x);
+  const float e = lane < K ? expf(key_logit(me.x) - l0) : 0.f;
+  const float s = warp_sum(e);
+  *out_id = (int)me.y;
+  *out_w = e / s;
 }
 
 // Exclusive scan of cnt[0..E) (shared) by the whole CTA (blockDim multiple of 32, <= 1024); returns

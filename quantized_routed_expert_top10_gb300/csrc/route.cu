@@ -11,10 +11,10 @@ namespace strata {
 namespace {
 
 // top-k of one token's logits (global memory written by other CTAs or kernels) by one warp.
-__device__ void top_k_warp(const float* logits, int E, int32_t* ids, float* weights) {
+__device__ void top_k_warp(const float* logits, int E, TopKScratch& sc, int32_t* ids, float* weights) {
   int id;
   float w;
-  top_k_warp_fn([&](int e) { return __ldcg(logits + e); }, E, &id, &w);
+  top_k_warp_fn([&](int e) { return __ldcg(logits + e); }, E, sc, &id, &w);
   const int lane = threadIdx.x & 31;
   if (lane < K) {
     ids[lane] = id;
@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
   __shared__ int s_tile[EMAX];
   __shared__ int s_scratch[32];
   __shared__ int s_last;
+  __shared__ TopKScratch s_topk[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // 1/rms per token (every CTA recomputes it; x is tiny and L2-resident).
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int t = warp; t < T; t += 4) top_k_warp(logits + (size_t)t * EMAX, E, ids + t * K, weights + t * K);
+  for (int t = warp; t < T; t += 4)
+    top_k_warp(logits + (size_t)t * EMAX, E, s_topk[warp], ids + t * K, weights + t * K);
   for (int i = tid; i < E; i += 128) s_cnt[i] = 0;
   __syncthreads();
   const int P = T * K;
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
                                                     const float* __restrict__ bias, float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids, float* __restrict__ weights) {
   static_assert(ROUTER_KSPLIT == 2, "the fixed summation order below assumes two slices");
+  __shared__ TopKScratch s_topk[4];
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const size_t slice = (size_t)T * EMAX;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
   }
   int id;
   float w;
-  top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, &id, &w);
+  top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, s_topk[threadIdx.x >> 5], &id, &w);
   if (lane < K) {
     ids[t * K + lane] = id;
     weights[t * K + lane] = w;
