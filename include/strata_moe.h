@@ -90,7 +90,10 @@ typedef struct strata_experts {
 /* Bytes of workspace a call with T tokens needs (any entry point below). */
 size_t strata_moe_workspace_bytes(int32_t T);
 
-/* Zero the workspace's counters and status word (enqueued on stream). Call once after allocating. */
+/* Zero the workspace's counters, status word and call epoch and, when ws_bytes covers it (any
+ * workspace sized for T >= 1), the decode path's exchange area, whose 64-bit words carry the tag of
+ * the call that wrote them (enqueued on stream).  Call once after allocating, with the size the calls
+ * will pass. */
 strata_status strata_moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Steps 1-2. x fp32 [T][2560] (the router input, already normalised if the layer normalises);

@@ -80,7 +80,8 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
   float* wts_d = weights ? weights : (float*)(w + L.weights);
   const int norm = (flags & STRATA_MOE_RESIDUAL_RMSNORM) ? 1 : 0;
   if (T <= DECODE_T_MAX) {
-    STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, out, ids_d, wts_d, L, w, s));
+    const int alias = (x < out + (size_t)T * H && out < x + (size_t)T * H) ? 1 : 0;  // in-place call
+    STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, alias, out, ids_d, wts_d, L, w, s));
     return STRATA_OK;
   }
   STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
@@ -107,7 +108,8 @@ strata_status strata_moe_workspace_init(void* ws, size_t ws_bytes, void* stream)
   if (!ws) return STRATA_E_INVAL;
   if (!aligned(ws, 256)) return STRATA_E_ALIGN;
   if (ws_bytes < WS_HEADER) return STRATA_E_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(ws, 0, WS_HEADER, (cudaStream_t)stream));
+  // the header and, when the workspace holds it, the decode exchange area (tag 0 = no value)
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes < DX_END ? WS_HEADER : DX_END, (cudaStream_t)stream));
 }
 
 strata_status strata_moe_route(const float* x, int32_t T, const uint16_t* w_router, const float* bias,
@@ -195,11 +197,18 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
   }
   if (n_layers == 0 || T == 0) return STRATA_OK;
   const int E = ex[0].n_expert;
+  // decode stacks alternate between x and a workspace buffer, so no layer writes the array it reads
+  // (the one-kernel layer then needs no release/acquire pair around its router exchange); an odd
+  // stack ends with one copy back into x
+  float* bufs[2] = {x, T <= DECODE_T_MAX && ws ? (float*)((char*)ws + ws_layout(T).xpp) : x};
   for (int l = 0; l < n_layers; ++l) {
-    STRATA_TRY(layer_impl(&ex[l], w_router + (size_t)l * E * H, bias ? bias + (size_t)l * E : nullptr, x, T,
-                          STRATA_MOE_RESIDUAL_RMSNORM, x, ids ? ids + (size_t)l * T * K : nullptr,
+    STRATA_TRY(layer_impl(&ex[l], w_router + (size_t)l * E * H, bias ? bias + (size_t)l * E : nullptr, bufs[l & 1], T,
+                          STRATA_MOE_RESIDUAL_RMSNORM, bufs[(l + 1) & 1], ids ? ids + (size_t)l * T * K : nullptr,
                           weights ? weights + (size_t)l * T * K : nullptr, ws, ws_bytes, (cudaStream_t)stream));
   }
+  if (bufs[n_layers & 1] != x)
+    STRATA_CUDA(cudaMemcpyAsync(x, bufs[n_layers & 1], sizeof(float) * (size_t)T * H, cudaMemcpyDeviceToDevice,
+                                (cudaStream_t)stream));
   return STRATA_OK;
 }
 

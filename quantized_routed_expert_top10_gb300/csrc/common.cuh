@@ -67,20 +67,22 @@ struct __align__(16) Tile {
 constexpr size_t WS_HEADER = 12288;
 constexpr size_t WS_STATUS = 0;     // int32 status word
 constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
-// Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): exit counter, per expert
-// slot h counters (finished gate/up slabs) and per down row tile counters (one 32-byte sector each),
-// and the grid barrier's arrival counters (one 128-byte line each), so CTAs polling or bumping
-// different words do not queue on the same line.
+// Sync words of the one-kernel decode layer (int32 indices from WS_SYNC): the exit counter and the
+// call epoch (the tag of the values one call exchanges through the area below).
 constexpr size_t WS_SYNC = 4096;
 constexpr int WS_SYNC_EXIT = 1;
-constexpr int WS_SYNC_STRIDE = 8;  // words between per-expert / per-tile counters
-constexpr int WS_SYNC_HREADY = 32;
-constexpr int WS_SYNC_CNT_DN = WS_SYNC_HREADY + WS_SYNC_STRIDE * DECODE_T_MAX * K;
-constexpr int WS_NARR = 8;         // grid barrier arrival counters (CTA c counts into c % WS_NARR)
-constexpr int WS_SYNC_ARR = ((WS_SYNC_CNT_DN + WS_SYNC_STRIDE * RT_D + 31) / 32) * 32;
-constexpr int WS_NREP = 16;        // replicas of data every CTA reads at once
-constexpr int WS_SYNC_WORDS = WS_SYNC_ARR + 32 * WS_NARR;
+constexpr int WS_SYNC_EPOCH = 32;  // own 128-byte line
+constexpr int WS_SYNC_WORDS = 64;
+constexpr int WS_NREP = 16;        // replicas of the router dot products (every CTA reads all of them)
 static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sync words must fit the header");
+// Decode exchange area, right after the header at the same offset for every T >= 1: 64-bit words
+// (value bits, call tag), each written once per call and polled by the CTAs that need it, so a
+// reader learns that a value is there from the value itself.  strata_moe_workspace_init zeroes it;
+// tag 0 never marks a value.
+constexpr size_t DX_DOTS = WS_HEADER;                                              // [WS_NREP][8][EMAX]
+constexpr size_t DX_H = DX_DOTS + sizeof(uint64_t) * WS_NREP * DECODE_T_MAX * EMAX;  // [8 * K][FF]
+constexpr size_t DX_PARTS = DX_H + sizeof(uint64_t) * DECODE_T_MAX * K * FF;          // [8 * K][H]
+constexpr size_t DX_END = DX_PARTS + sizeof(uint64_t) * DECODE_T_MAX * K * H;
 
 struct WsLayout {
   size_t status, cnt_route;
@@ -90,16 +92,14 @@ struct WsLayout {
   size_t weights;     // fp32 [T][K]
   size_t inv_rms;     // fp32 [T] 1/rms of each token (residual layers, T > DECODE_T_MAX)
   size_t xbf;         // bf16 [2][T][H] router operand: x_hi, x_lo (T > DECODE_T_MAX)
-  size_t sumsq;       // fp32 [WS_NREP][T][KB_GU] per-block sums of squares, replicated (one-kernel decode layer)
-  size_t dots_rep;    // fp32 [WS_NREP][T][EMAX] replicated router dot products (one-kernel decode layer)
   size_t expert_off;  // int32 [EMAX + 1]
   size_t pair;        // int32 [T*K]
   size_t active;      // int32 [EMAX]
   size_t n_active;    // int32 [4]: n_active, n_tiles
   size_t tiles;       // Tile [max_tiles]
   size_t chunk_cnt;   // int32 [n_chunks][EMAX]
-  size_t qx;          // QBlock [T][KB_GU] quantised layer input (one-kernel decode layer)
-  size_t hf;          // fp32 [min(T, DECODE_T_MAX) * K][FF] h of each pair (one-kernel decode layer)
+  size_t qx;          // QBlock [T][KB_GU] quantised layer input (T <= DECODE_T_MAX routing kernel)
+  size_t xpp;         // fp32 [T][H] (T <= DECODE_T_MAX): the other buffer of a decode stack's ping-pong
   size_t parts;       // fp32 [T*K][H]
   size_t xg;          // tensor-core expert path: gathered fp16 tokens [KB_GU][rows][128 B]
   size_t hg;          //                                      fp16 h [KB_D][rows][128 B]
@@ -133,15 +133,13 @@ inline WsLayout ws_layout(int T) {
   if (L.n_chunks < 1) L.n_chunks = 1;
   L.status = WS_STATUS;
   L.cnt_route = WS_CNT_ROUTE;
-  size_t o = WS_HEADER;
+  size_t o = DX_END;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
   L.logits = take(sizeof(float) * (size_t)ROUTER_KSPLIT * T * EMAX);
   L.ids = take(sizeof(int32_t) * (size_t)P);
   L.weights = take(sizeof(float) * (size_t)P);
   L.inv_rms = take(T > DECODE_T_MAX ? sizeof(float) * (size_t)T : 0);
   L.xbf = take(T > DECODE_T_MAX ? sizeof(uint16_t) * 2 * (size_t)T * H : 0);
-  L.sumsq = take(sizeof(float) * (size_t)WS_NREP * T * KB_GU);
-  L.dots_rep = take(sizeof(float) * (size_t)WS_NREP * (T < DECODE_T_MAX ? T : DECODE_T_MAX) * EMAX);
   L.expert_off = take(sizeof(int32_t) * (EMAX + 1));
   L.pair = take(sizeof(int32_t) * (size_t)P);
   L.active = take(sizeof(int32_t) * EMAX);
@@ -149,9 +147,7 @@ inline WsLayout ws_layout(int T) {
   L.tiles = take(sizeof(Tile) * (size_t)L.max_tiles);
   L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.n_chunks * EMAX);
   L.qx = take(sizeof(QBlock) * (size_t)T * KB_GU);
-  // sized for min(T, DECODE_T_MAX) so the total grows with T (a workspace sized for T serves any T' <= T)
-  const int Td = T < DECODE_T_MAX ? T : DECODE_T_MAX;
-  L.hf = take(sizeof(float) * (size_t)Td * K * FF);
+  L.xpp = take(T <= DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);
   L.parts = take(sizeof(float) * (size_t)P * H);
   L.xg = take(tc_xg_bytes(T));
   L.hg = take(tc_hg_bytes(T));
@@ -292,7 +288,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
-                                const float* x, int T, int residual, float* out, int32_t* ids, float* weights,
+                                const float* x, int T, int residual, int alias, float* out, int32_t* ids, float* weights,
                                 const WsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_pack_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed,
                                int64_t dst_stride, int64_t n_blobs, cudaStream_t s);

@@ -6,23 +6,26 @@
 // expert), the Q2_0 SwiGLU experts (ai.thesatyajit.com "Strata engine", "The CPU kernels": codes
 // {0,1,2,3} = {-1,0,1,2} x d with the offset removed once per block) and the weighted combine -- runs
 // as one cooperative launch of two 128-thread CTAs per SM:
-//   1. every CTA computes a few router rows and quantises a few 64-blocks of x (16-bit integers split
-//      into hi/lo bytes, see QBlock) and their sums of squares (for the rmsnorm of residual layers);
-//   2. one grid barrier; then every CTA redundantly computes the top-10 of all tokens and the
-//      grouping in shared memory (identical results everywhere, no second barrier);
-//   3. right after the barrier each CTA copies every token's quantised activations into shared
-//      memory (one bulk copy, overlapping the top-k); the expert bytes are cut into equal
-//      23,040-byte units -- gate/up units (expert, slab of 16 rows, all 40 k-blocks: contiguous in
-//      the packed blob) and down units (expert, 128-row tile, all 10 k-blocks) -- dealt round robin
-//      to the CTAs, gate/up units first.  Each CTA streams its units through a ring of shared memory
-//      stages with cp.async.bulk (L2 evict-first) as soon as routing is known;
-//   4. a gate/up unit finishes g and u of its 16 rows for the expert's tokens (8 thread groups of 5
-//      k-blocks, added in group order), writes h = silu(g) * u and bumps the expert's h counter; a
-//      down unit waits (bounded) until all 40 slabs of its expert are in, quantises h itself, and the
-//      last down unit of each output row tile combines the ten weighted expert outputs of every
-//      token in k order (+ the residual).
-// All waits are bounded by %globaltimer and record STRATA_E_TIMEOUT in the status word.  The last CTA
-// to leave resets the counters, so the workspace is ready for the next call.
+//   1. every CTA stages all tokens' activations in shared memory (16-bit integer blocks for one
+//      token, fp16 in MMA fragment order for more) with their rmsnorm, then computes a few router
+//      rows and publishes them;
+//   2. every CTA polls all router dot products and redundantly computes the top-10 of all tokens
+//      and the grouping (identical results everywhere);
+//   3. the expert bytes are cut into equal 23,040-byte units -- gate/up units (expert, slab of 16
+//      rows, all 40 k-blocks: contiguous in the packed blob) and down units (expert, 128-row tile,
+//      all 10 k-blocks) -- dealt round robin to the CTAs, gate/up units first.  Each CTA streams its
+//      units through a ring of shared-memory stages with cp.async.bulk (L2 evict-first) as soon as
+//      routing is known.  A gate/up unit publishes h = silu(g) * u of its 16 rows; a down unit polls
+//      the h of its expert's tokens and publishes its 128 output rows per pair;
+//   4. the CTA of down unit (expert slot j, row tile r) then polls the outputs of every pair for
+//      share j of tile r's rows and writes their weighted sum in k order (+ the residual).
+// Every exchanged value travels as one 64-bit word (value bits, call tag) in the workspace's decode
+// exchange area: a reader polls the words it needs until all carry this call's tag, so learning
+// that a value is ready and fetching it take one round trip.  When the output aliases the input,
+// the router publication is a release (after every read of x by its CTA) and its polling an
+// acquire, which orders all reads of x before any write of the output.  Every wait is bounded by
+// %globaltimer and records STRATA_E_TIMEOUT in the status word.  The last CTA to leave advances the
+// call epoch.
 #include "device_common.cuh"
 
 namespace strata {
@@ -32,9 +35,11 @@ constexpr int DF_UNIT = 23040;                 // bytes per work unit
 constexpr int DF_GU = N_SLAB;                  // 40 gate/up units (slabs) per expert
 constexpr int DF_DN = RT_D;                    // 20 down units per expert
 constexpr int DF_MAXD = DECODE_T_MAX * K;      // at most 80 distinct experts
-constexpr int DF_THREADS = 128;
-constexpr int DF_KG = DF_THREADS / SLAB;       // 8 k-block groups per gate/up unit
+constexpr int DF_THREADS = 256;
+constexpr int DF_NW = DF_THREADS / 32;         // 8 warps
+constexpr int DF_KG = DF_NW;                   // k-block groups per gate/up unit (one token: a warp each)
 constexpr int DF_KBG = KB_GU / DF_KG;          // 5 k-blocks per group
+static_assert(DF_KG * DF_KBG == KB_GU && 2 * SLAB * DF_KG == DF_THREADS, "gate/up unit split");
 static_assert(SLAB_BYTES == DF_UNIT && KB_D * D_CHUNK == DF_UNIT, "equal unit sizes");
 // Ring stages per CTA: three, or two when eight tokens' activations take the shared memory.
 template <int TT>
@@ -48,20 +53,72 @@ struct DecodeParams {
   const float* x;  // [T][H] layer input (may alias out)
   float* out;      // [T][H]
   int T, E, q2_offset, residual;
+  int alias;           // out overlaps x: release/acquire around the router exchange (see step 1b)
   const uint16_t* wr;  // [E][H] bf16
   const float* bias;   // [E] or null
   const uint8_t* blobs;
   int64_t stride;
   int32_t* ids_out;  // [T][K]
   float* w_out;      // [T][K]
-  float* dots;       // ws [WS_NREP][T][EMAX] raw router dot products, replicated
-  float* sumsq;      // ws [WS_NREP][T][KB_GU], replicated
-  QBlock* qx;        // ws [T][KB_GU]
-  float* hf;         // ws [T*K][FF] h of each pair, in slot order
-  float* parts;      // ws [T*K][H]
+  uint64_t* dots;    // exchange area: router dot products [WS_NREP][DECODE_T_MAX][EMAX]
+  uint64_t* htag;    //                h of each slot [DECODE_T_MAX * K][FF]
+  uint64_t* ptag;    //                expert outputs of each pair [DECODE_T_MAX * K][H]
   int* sync;         // ws sync words (WS_SYNC)
   int* status;
 };
+
+// Exchange words: (value bits, call tag).  A 64-bit aligned access is single-copy atomic, so a
+// reader that sees the tag sees the value stored with it.
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p));
+  return w;
+}
+__device__ __forceinline__ bool has_tag(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+__device__ __forceinline__ float tagged_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+
+// Bounded poll (whole CTA) of `count` exchange words src[map(i)], i < count, into dst[i] (shared):
+// each thread owns entries tid + DF_THREADS * k, k < KMAX (count <= KMAX * DF_THREADS), and re-reads
+// the ones still missing, all in flight at once, until every entry of the CTA carries `tag`.  The
+// verdicts are CTA-wide (barrier reductions), so every thread leaves on the same pass.  Between
+// passes the CTA sleeps, 64 ns doubling up to 512 ns: a spinning CTA would take issue slots from the
+// other CTA on its SM.  False (and ST_TIMEOUT) once the wait limit has passed.
+template <int KMAX, typename Map>
+__device__ __forceinline__ bool poll_tagged(const uint64_t* src, Map map, int count, uint32_t tag, float* dst,
+                                            int* status) {
+  static_assert(KMAX <= 64, "one mask bit per entry");
+  const int tid = threadIdx.x;
+  uint64_t missing = 0;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+    if (tid + DF_THREADS * k < count) missing |= 1ull << k;
+  const unsigned long long t0 = globaltimer();
+  unsigned sleep_ns = 64;
+  while (true) {
+    uint64_t w[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if ((missing >> k) & 1) w[k] = ld_tagged(src + map(tid + DF_THREADS * k));
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (((missing >> k) & 1) && has_tag(w[k], tag)) {
+        dst[tid + DF_THREADS * k] = tagged_value(w[k]);
+        missing &= ~(1ull << k);
+      }
+    if (__syncthreads_and(missing == 0 ? 1 : 0)) return true;
+    if (__syncthreads_or(globaltimer() - t0 > kWaitLimitNs ? 1 : 0)) {
+      if (tid == 0) set_status(status, ST_TIMEOUT);
+      return false;
+    }
+    __nanosleep(sleep_ns);
+    sleep_ns = min(2 * sleep_ns, 512u);
+  }
+}
+
 
 __device__ __forceinline__ void unpack_words(const QBlock& a, uint32_t* hi, uint32_t* lo) {
 #pragma unroll
@@ -117,74 +174,175 @@ template <int TT>
 __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const DecodeParams p) {
   constexpr bool MMA = TT >= 2;  // one token: dp4a on the codes; more: tensor-core products
   constexpr int NS = df_stages<TT>();
+  constexpr int ROWS_MAX = 16;   // router rows per CTA (grids of >= 32 CTAs)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;                                                 // NS * DF_UNIT
   QBlock* sqx = reinterpret_cast<QBlock*>(smem + NS * DF_UNIT);         // [T][KB_GU] all tokens
   QBlock* sq = sqx + TT * KB_GU;                                        // [KB_D][TT] h of a down unit
-  float2* red = reinterpret_cast<float2*>(sq);                          // [DF_KG][TT][SLAB] (gate/up)
-  static_assert(sizeof(float2) * DF_KG * TT * SLAB <= sizeof(QBlock) * KB_D * TT, "reduction fits");
+  float* red = reinterpret_cast<float*>(sq);                            // gate/up partial sums
+  static_assert(sizeof(float) * 2 * DF_NW * TT * SLAB <= sizeof(QBlock) * KB_D * TT, "reduction fits");
   __shared__ uint64_t bars[NS];
-  __shared__ uint64_t bar_qx, bar_h;
   __shared__ int s_pending[NS];
-  __shared__ int s_qx_pending, s_h_pending;
   __shared__ float s_inv[TT];
-  __shared__ int s_ids[TT * K];
+  __shared__ float s_ssq[DF_NW];
+  __shared__ float s_dot[ROWS_MAX][TT];
+  __shared__ __align__(16) int s_ids[(TT * K + 3) / 4 * 4];
   __shared__ float s_w[TT * K];
   __shared__ int s_te[DF_MAXD];   // expert slot j -> expert id
   __shared__ int s_tn[DF_MAXD];   //               -> tokens routed to it
   __shared__ int s_tq[DF_MAXD];   //               -> first slot in s_pair
-  __shared__ int s_first[TT * K];
+  __shared__ int s_first[TT * K];  // expert id of each slot (grouping)
+  __shared__ int s_wcnt[DF_NW];
   __shared__ int s_pair[TT * K];
-  __shared__ float s_rpart[4][TT];
+  __shared__ float s_rpart[DF_NW][TT];
   __shared__ float s_bias[EMAX];
-  __shared__ TopKScratch s_topk[DF_THREADS / 32];
-  __shared__ int32_t s_qtmp[4][64];
-  __shared__ int s_flag, s_ok, s_nact;
+  TopKScratch* s_topk = reinterpret_cast<TopKScratch*>(ring);  // [DF_NW], routing only (ring idle)
+  static_assert(sizeof(TopKScratch) * DF_NW <= DF_UNIT, "top-k scratch fits the first stage");
+  __shared__ int32_t s_qtmp[DF_NW][64];
+  __shared__ int s_flag, s_ok, s_nact, s_dots0;
 
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
-  int* h_cnt = p.sync + WS_SYNC_HREADY;  // expert slot j at h_cnt[WS_SYNC_STRIDE * j]
-  int* cnt_dn = p.sync + WS_SYNC_CNT_DN;  // row tile r at cnt_dn[WS_SYNC_STRIDE * r]
+  // this call's tag: one more than the previous call's (the last CTA to leave advances the epoch)
+  const uint32_t ep = (uint32_t)ld_relaxed(p.sync + WS_SYNC_EPOCH) + 1u;
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars[s], 1);
       s_pending[s] = -1;
     }
-    mbar_init(&bar_qx, 1);
-    mbar_init(&bar_h, 1);
-    s_qx_pending = 0;
-    s_h_pending = -1;
     fence_mbar_init();
     s_ok = 1;
   }
-  // loads for later steps, issued first so their latency hides under the router rows': the bias
-  // (used by the top-k) and this warp's first block of x to quantise
+  // loads for later steps, issued first: the bias (used by the top-k) and this CTA's first router
+  // row (two warps per row, each over one half of the columns), with the x values it multiplies
+  // when there is one token
   float bias_v[EMAX / DF_THREADS];
 #pragma unroll
   for (int i = 0; i < EMAX / DF_THREADS; ++i) {
     const int e = tid + DF_THREADS * i;
     bias_v[i] = (p.bias && e < E) ? __ldg(p.bias + e) : 0.f;
   }
-  const int t4x = lane >> 3, qx8 = lane & 7;  // fragment-order position of this lane's x pair (T >= 2)
-  auto load_block = [&](int b, float2& v, float& xa, float& xb) {
-    const int t = b / KB_GU, kb = b % KB_GU;
-    v = __ldg(reinterpret_cast<const float2*>(p.x + (size_t)t * H + kb * QK + 2 * lane));
-    if constexpr (MMA) {
-      const float* src = p.x + (size_t)t * H + kb * QK + 16 * t4x + 4 * (qx8 >> 2) + (qx8 & 3);
-      xa = __ldg(src);
-      xb = __ldg(src + 8);
+  const int half = warp & 1;
+  uint4 wq[H / 512];
+  float4 xa[TT == 1 ? H / 512 : 1], xb[TT == 1 ? H / 512 : 1];
+  {
+    const int e = c + G * (warp >> 1);
+    if (e < E) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(p.wr + (size_t)e * H);
+#pragma unroll
+      for (int i = 0; i < H / 512; ++i) wq[i] = __ldg(wrow + ((half * (H / 2) + 8 * lane + 256 * i) >> 3));
     }
-  };
-  float2 v0 = make_float2(0.f, 0.f);
-  float xa0 = 0.f, xb0 = 0.f;
-  if (c + G * warp < T * KB_GU) load_block(c + G * warp, v0, xa0, xb0);
+    if constexpr (TT == 1) {
+#pragma unroll
+      for (int i = 0; i < H / 512; ++i) {
+        const float* xs = p.x + half * (H / 2) + 8 * lane + 256 * i;
+        xa[i] = __ldg(reinterpret_cast<const float4*>(xs));
+        xb[i] = __ldg(reinterpret_cast<const float4*>(xs + 4));
+      }
+    }
+  }
 
-  // ---- 1. router dot products (two warps per row), x quantisation, block sums of squares ----
-  for (int e0 = c; e0 < E; e0 += 2 * G) {
+  // ---- 1a. every token's activations into shared memory, and their rmsnorm ----
+  if constexpr (!MMA) {
+    // one token: 40 blocks quantised to QBlocks, one thread per half block (32 values, the two
+    // halves in adjacent lanes) -- the same QBlock as quantise_block_warp builds
+    static_assert(2 * KB_GU <= DF_THREADS, "one thread per half block");
+    const int b = tid >> 1, hb = tid & 1;
+    const bool live = tid < 2 * KB_GU;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 a = live ? __ldg(reinterpret_cast<const float4*>(p.x + b * QK + 32 * hb) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+    }
+    float amax = 0.f, ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      amax = fmaxf(amax, fabsf(v[i]));
+      ss = fmaf(v[i], v[i], ss);
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    ss = warp_sum(ss);
+    if (lane == 0) s_ssq[warp] = ss;
+    int qv[32];
+    int qs = 0;
+    const float qinv = amax > 0.f ? 32767.f / amax : 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      qv[i] = amax > 0.f ? max(-32767, min(32767, __float2int_rn(v[i] * qinv))) : 0;
+      qs += qv[i];
+    }
+    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+    if (live) {
+      // word (q4, m), q4 = 2 hb + g: bytes b' = 0..3 of the values 16 q4 + 4 b' + m
+      uint32_t hw[8], lw[8];
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          uint32_t hi = 0, lo = 0;
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int val = qv[16 * g + 4 * bb + m];
+            hi |= (uint32_t)((val >> 8) & 0xFF) << (8 * bb);
+            lo |= (uint32_t)(val & 0xFF) << (8 * bb);
+          }
+          hw[4 * g + m] = hi;
+          lw[4 * g + m] = lo;
+        }
+      QBlock& dst = sqx[b];
+      uint4* dh = reinterpret_cast<uint4*>(dst.hi + 8 * hb);
+      uint4* dl = reinterpret_cast<uint4*>(dst.lo + 8 * hb);
+      dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+      dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+      if (hb == 0) {
+        dst.s64 = amax > 0.f ? (amax / 32767.f) * (1.f / 64.f) : 0.f;
+        dst.qoff = 64 * p.q2_offset * qs;
+      }
+    }
+  } else {
+    // fp16 x in fragment order, xs[16-group][token][16 halves]; warp w takes tokens w, w + 4, lane
+    // the 16-groups lane + 32 i
+    for (int t = warp; t < T; t += DF_NW) {
+      float4 a[H / 16 / 32][4];
+#pragma unroll
+      for (int i = 0; i < H / 16 / 32; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          a[i][q] = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + 16 * (lane + 32 * i) + 4 * q));
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < H / 16 / 32; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          ss += a[i][q].x * a[i][q].x + a[i][q].y * a[i][q].y + a[i][q].z * a[i][q].z + a[i][q].w * a[i][q].w;
+      ss = warp_sum(ss);
+      if (lane == 0) s_inv[t] = p.residual ? 1.f / sqrtf(ss / (float)H + 1e-6f) : 1.f;
+#pragma unroll
+      for (int i = 0; i < H / 16 / 32; ++i) {
+        const float f[16] = {a[i][0].x, a[i][0].y, a[i][0].z, a[i][0].w, a[i][1].x, a[i][1].y, a[i][1].z, a[i][1].w,
+                             a[i][2].x, a[i][2].y, a[i][2].z, a[i][2].w, a[i][3].x, a[i][3].y, a[i][3].z, a[i][3].w};
+        uint32_t hq[8];
+        to_fragment_order(f, hq);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sqx) + ((size_t)(lane + 32 * i) * T + t) * 32);
+        dst[0] = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+        dst[1] = make_uint4(hq[4], hq[5], hq[6], hq[7]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < EMAX / DF_THREADS; ++i)
+    if (tid + DF_THREADS * i < E) s_bias[tid + DF_THREADS * i] = bias_v[i];
+  __syncthreads();
+
+  // ---- 1b. router dot products: row c + G m, m = 0, 1, ... (two warps per row, DF_NW / 2 rows a round) ----
+  int n_rows = 0;
+  for (int e0 = c, it = 0; e0 < E; e0 += (DF_NW / 2) * G, ++it) {
     const int e = e0 + G * (warp >> 1);
-    const int half = warp & 1;
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.f;
@@ -194,12 +352,18 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       for (int i = 0; i < H / 512; ++i) {
         const int col = half * (H / 2) + 8 * lane + 256 * i;
         float wf[8];
-        bf16x8_to_f32(__ldg(wrow + (col >> 3)), wf);
+        bf16x8_to_f32(it == 0 ? wq[i] : __ldg(wrow + (col >> 3)), wf);
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           if (t < T) {
-            const float4 a4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
-            const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col + 4));
+            float4 a4, b4;
+            if (TT == 1 && it == 0) {
+              a4 = xa[TT == 1 ? i : 0];
+              b4 = xb[TT == 1 ? i : 0];
+            } else {
+              a4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
+              b4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col + 4));
+            }
             float sacc = acc[t];
             sacc = fmaf(wf[0], a4.x, sacc); sacc = fmaf(wf[1], a4.y, sacc);
             sacc = fmaf(wf[2], a4.z, sacc); sacc = fmaf(wf[3], a4.w, sacc);
@@ -216,120 +380,155 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       if (lane == 0) s_rpart[warp][t] = r;
     }
     __syncthreads();
-    if (tid < 2 * TT) {
-      const int w2 = tid / TT, t = tid % TT;
-      const int e2 = e0 + G * w2;
-      if (e2 < E && t < T) {
-        const float v = s_rpart[2 * w2][t] + s_rpart[2 * w2 + 1][t];
-#pragma unroll
-        for (int r = 0; r < WS_NREP; ++r) p.dots[((size_t)r * T + t) * EMAX + e2] = v;
-      }
+    if (tid < (DF_NW / 2) * TT) {
+      const int w2 = tid / TT, t = tid % TT, m = (DF_NW / 2) * it + w2;
+      if (m < ROWS_MAX) s_dot[m][t] = s_rpart[2 * w2][t] + s_rpart[2 * w2 + 1][t];
     }
     __syncthreads();
+    n_rows = min((DF_NW / 2) * (it + 1), ROWS_MAX);
   }
-  for (int b = c + G * warp; b < T * KB_GU; b += 4 * G) {
-    const int t = b / KB_GU, kb = b % KB_GU;
-    float2 v = v0;
-    float xa = xa0, xb = xb0;
-    if (b != c + G * warp) load_block(b, v, xa, xb);
-    const float ss = warp_sum(v.x * v.x + v.y * v.y);
-    if (lane == 0)
-#pragma unroll
-      for (int r = 0; r < WS_NREP; ++r) p.sumsq[(size_t)r * T * KB_GU + b] = ss;
-    if constexpr (MMA) {  // fp16 x in fragment order: xs[kb][t4][token][16 halves]
-      const __half2 x2 = __floats2half2_rn(xa, xb);
-      reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.qx) + ((size_t)(kb * 4 + t4x) * T + t) * 32)[qx8] = x2;
-    } else {
-      quantise_block_warp(v.x, v.y, p.q2_offset, p.qx + b, s_qtmp[warp]);
+  // publish.  When out aliases x, the publication is a release (fence, then the tagged stores) after
+  // every read of x by this CTA and the routing poll an acquire: every CTA's reads of x then happen
+  // before any CTA's combine writes the output.  Otherwise the fences are left out.
+  for (int idx = tid; idx < n_rows * T * WS_NREP; idx += DF_THREADS) {
+    const int r = idx % WS_NREP, t = (idx / WS_NREP) % T, m = idx / (WS_NREP * T);
+    const int e = c + G * m;
+    if (e < E) {
+      if (p.alias && idx == tid) fence_acq_rel_gpu();
+      st_tagged(p.dots + ((size_t)r * DECODE_T_MAX + t) * EMAX + e, s_dot[m][t], ep);
     }
   }
-
-#pragma unroll
-  for (int i = 0; i < EMAX / DF_THREADS; ++i)
-    if (tid + DF_THREADS * i < E) s_bias[tid + DF_THREADS * i] = bias_v[i];
-
-  // ---- grid barrier: each CTA makes its writes visible and counts into one of WS_NARR counters
-  // (release add, no reply awaited), then polls all of them ----
-  __syncthreads();
-  if (tid == 0) {
-    red_release_add(p.sync + WS_SYNC_ARR + 32 * (c % WS_NARR), 1);
-    s_ok = spin_grid_arrivals<WS_NARR>(p.sync + WS_SYNC_ARR, 32, G, p.status) ? 1 : 0;
-    if (s_ok) {
-      // every token's quantised activations (written by all CTAs before the barrier) into shared
-      // memory; the async-proxy copy is ordered after the acquire by the proxy fence
-      fence_proxy_async_global();
-      const uint32_t xbytes = MMA ? (uint32_t)(KB_GU * 4 * 32 * T) : (uint32_t)(sizeof(QBlock) * T * KB_GU);
-      mbar_expect_tx(&bar_qx, xbytes);
-      bulk_g2s(sqx, p.qx, xbytes, &bar_qx);
-      s_qx_pending = 1;
-    }
-  }
-  __syncthreads();
 
   // ---- 2. top-10 and grouping, redundantly in every CTA ----
-  if (s_ok) {
-    if (tid == 0) s_nact = 0;
-    for (int t = warp; t < T; t += 4) {
-      const float* d = p.dots + ((size_t)(c % WS_NREP) * T + t) * EMAX;
-      float lg[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) lg[j] = (lane + 32 * j < E) ? __ldcg(d + lane + 32 * j) : 0.f;
-      float inv = 1.f;  // rmsnorm of a residual layer: 1 / rms from the 40 block sums of squares
-      if (p.residual) {
-        const float* ssq = p.sumsq + ((size_t)(c % WS_NREP) * T + t) * KB_GU;
-        float s = __ldcg(ssq + lane);
-        if (lane + 32 < KB_GU) s += __ldcg(ssq + lane + 32);
-        inv = 1.f / sqrtf(warp_sum(s) / (float)H + 1e-6f);
+  if (tid == 0) {
+    s_nact = 0;
+    s_dots0 = 0;
+  }
+  __syncthreads();
+  bool okr = true;
+  for (int t = warp; t < T; t += DF_NW) {
+    // this token's dot products from replica c % WS_NREP: poll until all carry this call's tag.
+    // Only token 0's warp polls from the start; the others wait (in shared memory) until token 0's
+    // products are all in -- the publishers wrote every token's products together -- so the CTAs
+    // do not flood the L2 with T times the polling reads.
+    const uint64_t* src = p.dots + ((size_t)(c % WS_NREP) * DECODE_T_MAX + t) * EMAX;
+    const int per = E >> 5;
+    float lg[16];
+    uint32_t missing = (1u << per) - 1u;
+    const unsigned long long t0 = globaltimer();
+    if (t > 0) {
+      while (*reinterpret_cast<volatile int*>(&s_dots0) == 0) {
+        if (__shfl_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs ? 1 : 0, 0)) break;
+        __nanosleep(128);
       }
-      if (lane == 0) s_inv[t] = inv;
+      __syncwarp();
+    }
+    while (true) {
+      uint64_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (lane + 32 * j < E) lg[j] = lg[j] * inv + s_bias[lane + 32 * j];
-      int id;
-      float w;
-      top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, s_topk[warp], &id, &w);
+        if ((missing >> j) & 1) w[j] = ld_tagged(src + lane + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (((missing >> j) & 1) && has_tag(w[j], ep)) {
+          lg[j] = tagged_value(w[j]);
+          missing &= ~(1u << j);
+        }
+      if (__all_sync(0xffffffffu, missing == 0)) break;
+      if (__shfl_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs ? 1 : 0, 0)) {
+        if (lane == 0) set_status(p.status, ST_TIMEOUT);
+        okr = false;
+        break;
+      }
+      __nanosleep(100);  // back off: every CTA polls the same lines
+    }
+    if (t == 0 && lane == 0) *reinterpret_cast<volatile int*>(&s_dots0) = 1;
+    if (!okr) break;
+    if (p.alias) fence_acq_rel_gpu();  // acquire: pairs with every publisher's release
+    float inv;
+    if constexpr (MMA) {
+      inv = s_inv[t];
+    } else {
+      float ssq = 0.f;
+#pragma unroll
+      for (int w = 0; w < DF_NW; ++w) ssq += s_ssq[w];
+      inv = p.residual ? 1.f / sqrtf(ssq / (float)H + 1e-6f) : 1.f;
+      if (lane == 0) s_inv[0] = inv;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < per) lg[j] = lg[j] * inv + s_bias[lane + 32 * j];
+    int id;
+    float w;
+    top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, s_topk[warp], &id, &w);
+    if (lane < K) {
+      s_ids[t * K + lane] = id;
+      s_w[t * K + lane] = w;
+    }
+    if constexpr (TT == 1) {
+      // one token: its K ids are distinct, so expert slot = pair slot = the id's rank among them
+      int below = 0;
+#pragma unroll
+      for (int q = 0; q < K; ++q) below += (__shfl_sync(0xffffffffu, id, q) < id) ? 1 : 0;
       if (lane < K) {
-        s_ids[t * K + lane] = id;
-        s_w[t * K + lane] = w;
+        s_pair[below] = lane;
+        s_te[below] = id;
+        s_tn[below] = 1;
+        s_tq[below] = below;
       }
+      if (lane == 0) s_nact = K;
     }
-    __syncthreads();
-    // grouping of the P <= 80 pairs, directly on the pairs: slot of pair q = (pairs with a smaller
-    // expert id) + (earlier pairs with the same expert); expert slot j = (distinct smaller ids).
-    if (tid < P) {
-      const int e = s_ids[tid];
-      int first = 1;
-      for (int q = 0; q < tid; ++q) first &= (s_ids[q] != e);
-      s_first[tid] = first;
-    }
-    __syncthreads();
-    if (tid < P) {
-      const int e = s_ids[tid];
-      int below = 0, same_before = 0, cnt = 0, dbelow = 0;
-      for (int q = 0; q < P; ++q) {
-        const int f = s_ids[q];
-        below += (f < e);
-        cnt += (f == e);
-        same_before += (q < tid && f == e);
-        dbelow += (s_first[q] && f < e);
-      }
-      s_pair[below + same_before] = tid;
-      if (s_first[tid]) {
-        s_te[dbelow] = e;
-        s_tn[dbelow] = cnt;
-        s_tq[dbelow] = below;
-        atomicAdd(&s_nact, 1);
-      }
-    }
-    if (c == 0)
-      for (int q = tid; q < P; q += DF_THREADS) {
-        p.ids_out[q] = s_ids[q];
-        p.w_out[q] = s_w[q];
-      }
-    __syncthreads();
   }
+  const bool routed = __syncthreads_and(okr ? 1 : 0);
+  if (!routed) {
+    if (tid == 0) s_ok = 0;
+  } else if constexpr (TT > 1) {
+    // grouping of the P <= 80 pairs by a counting sort: the slot of pair q is its rank by (expert id,
+    // q); a slot whose id differs from the previous slot's starts the next expert slot
+    for (int q = P + tid; q < (P + 3) / 4 * 4; q += DF_THREADS) s_ids[q] = EMAX;  // pad to whole int4
+    __syncthreads();
+    if (tid < P) {
+      const int e = s_ids[tid];
+      const int key = e * DF_MAXD + tid;
+      int rank = 0;
+      const int4* ids4 = reinterpret_cast<const int4*>(s_ids);
+      for (int q4 = 0; q4 < (P + 3) / 4; ++q4) {
+        const int4 f = ids4[q4];
+        rank += (f.x * DF_MAXD + 4 * q4 < key) + (f.y * DF_MAXD + 4 * q4 + 1 < key) +
+                (f.z * DF_MAXD + 4 * q4 + 2 < key) + (f.w * DF_MAXD + 4 * q4 + 3 < key);
+      }
+      s_pair[rank] = tid;
+      s_first[rank] = e;  // the expert id of each slot
+    }
+    __syncthreads();
+    const bool starts = tid < P && (tid == 0 || s_first[tid - 1] != s_first[tid]);
+    const uint32_t bal = __ballot_sync(0xffffffffu, starts);
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    if (starts) {
+      int j = __popc(bal & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) j += s_wcnt[w];
+      const int id = s_first[tid];
+      int n = 0;
+      for (int q = tid; q < P && s_first[q] == id; ++q) ++n;
+      s_te[j] = id;
+      s_tn[j] = n;
+      s_tq[j] = tid;
+    }
+    if (tid == 0) {
+      int d = 0;
+      for (int w = 0; w < DF_THREADS / 32; ++w) d += s_wcnt[w];
+      s_nact = d;
+    }
+  }
+  if (c == 0 && routed)
+    for (int q = tid; q < P; q += DF_THREADS) {
+      p.ids_out[q] = s_ids[q];
+      p.w_out[q] = s_w[q];
+    }
+  __syncthreads();
 
-  // ---- 3-4. expert units ----
+  // ---- 3. expert units ----
   if (s_ok) {
     const int D = s_nact;
     const int n_gu = D * DF_GU, n_units = D * (DF_GU + DF_DN);
@@ -353,7 +552,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       for (int i = 0; i < NS; ++i)
         if (c + G * i < n_units) issue(c + G * i, i);
 
-    int i = 0, n_dn = 0;
+    int i = 0;
     for (int u = c; u < n_units; u += G, ++i) {
       const int st = i % NS;
       const uint32_t par = (uint32_t)((i / NS) & 1);
@@ -362,19 +561,14 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         // -------- gate/up unit: slab sl (rows 16 sl ..) of expert slot j, all k-blocks --------
         const int j = u / DF_GU, sl = u % DF_GU;
         const int n = s_tn[j], q0 = s_tq[j];
-        bool ready = mbar_wait(&bars[st], par, p.status);
-        if (s_qx_pending) ready = mbar_wait(&bar_qx, 0u, p.status) && ready;
-        if (!__syncthreads_and(ready ? 1 : 0)) {
+        if (!__syncthreads_and(mbar_wait(&bars[st], par, p.status) ? 1 : 0)) {
           if (tid == 0) s_ok = 0;
           __syncthreads();
           break;
         }
-        if (tid == 0) {
-          s_pending[st] = -1;
-          s_qx_pending = 0;
-        }
+        if (tid == 0) s_pending[st] = -1;
         if constexpr (MMA) {
-          // warp w: k-blocks [10 w, 10 w + 10) of the 16-row slab, all T tokens as columns
+          // warp w: k-blocks [5 w, 5 w + 5) of the 16-row slab, all T tokens as columns
           const int g = lane >> 2, t4 = lane & 3;
           uint32_t subq[4];
 #pragma unroll
@@ -384,9 +578,9 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           }
           const uint8_t* xs = reinterpret_cast<const uint8_t*>(sqx);
           float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-          for (int kk = 0; kk < KB_GU / 4; ++kk) {
-            const int kb = warp * (KB_GU / 4) + kk;
+#pragma unroll 1
+          for (int kk = 0; kk < KB_GU / DF_NW; ++kk) {
+            const int kb = warp * (KB_GU / DF_NW) + kk;
             const uint8_t* piece = stage + kb * SLAB_KB;
             const uint32_t wg0 = *reinterpret_cast<const uint32_t*>(piece + 16 * g + 4 * t4);
             const uint32_t wg1 = *reinterpret_cast<const uint32_t*>(piece + 16 * (g + 8) + 4 * t4);
@@ -423,8 +617,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             au[0] = fmaf(du0, cu[0][0] + cu[1][0], au[0]); au[1] = fmaf(du0, cu[0][1] + cu[1][1], au[1]);
             au[2] = fmaf(du1, cu[0][2] + cu[1][2], au[2]); au[3] = fmaf(du1, cu[0][3] + cu[1][3], au[3]);
           }
-          // red[warp][mat][row][column]: the four warps' k ranges, added below in warp order
-          float* rf = reinterpret_cast<float*>(red);
+          // red[warp][mat][row][column]: the warps' k ranges, added below in warp order
+          float* rf = red;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int row = g + 8 * (e >> 1), col = 2 * t4 + (e & 1);
@@ -439,97 +633,75 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             const int tk = s_pair[q0 + ii] / K;
             float gg = 0.f, uu = 0.f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
+            for (int w = 0; w < DF_NW; ++w) {
               gg += rf[((w * 2 + 0) * SLAB + r2) * TT + tk];
               uu += rf[((w * 2 + 1) * SLAB + r2) * TT + tk];
             }
             const float inv = s_inv[tk];
-            p.hf[(size_t)(q0 + ii) * FF + sl * SLAB + r2] = silu_mul(gg * inv, uu * inv);
+            st_tagged(p.htag + (size_t)(q0 + ii) * FF + sl * SLAB + r2, silu_mul(gg * inv, uu * inv), ep);
           }
         } else {
-        const int r = tid % SLAB, grp = tid / SLAB;  // row of the slab, group of DF_KBG k-blocks
-        int tok[TT];
-        float tinv[TT];
-#pragma unroll
-        for (int ii = 0; ii < TT; ++ii) {
-          tok[ii] = (ii < n) ? s_pair[q0 + ii] / K : 0;
-          tinv[ii] = (ii < n) ? s_inv[tok[ii]] : 0.f;
-        }
-        float accg[TT], accu[TT];
-#pragma unroll
-        for (int ii = 0; ii < TT; ++ii) { accg[ii] = 0.f; accu[ii] = 0.f; }
-#pragma unroll 1
-        for (int kk = 0; kk < DF_KBG; ++kk) {
-          const int kb = grp * DF_KBG + kk;
-          const uint8_t* piece = stage + kb * SLAB_KB;
-          const uint4 gc = *reinterpret_cast<const uint4*>(piece + 16 * r);
-          const uint4 uc = *reinterpret_cast<const uint4*>(piece + 256 + 16 * r);
-          const __half2 sc = *reinterpret_cast<const __half2*>(piece + 512 + 4 * r);
-          const float dg = __low2float(sc), du = __high2float(sc);
-          const Masked gm = mask_codes(gc), um = mask_codes(uc);
+          // thread: row r of the slab, matrix mat (gate, up), group grp = warp of DF_KBG k-blocks
+          const int r = tid % SLAB, mat = (tid / SLAB) & 1, grp = warp;
+          int tok[TT];
+          float tinv[TT];
 #pragma unroll
           for (int ii = 0; ii < TT; ++ii) {
-            if (ii < n) {
-              const QBlock& a = sqx[tok[ii] * KB_GU + kb];
-              uint32_t hi[16], lo[16];
-              unpack_words(a, hi, lo);
-              const float f = a.s64 * tinv[ii];
-              const int vg = dot64(gm, hi, lo) - a.qoff;
-              const int vu = dot64(um, hi, lo) - a.qoff;
-              accg[ii] = fmaf(dg * f, (float)vg, accg[ii]);
-              accu[ii] = fmaf(du * f, (float)vu, accu[ii]);
+            tok[ii] = (ii < n) ? s_pair[q0 + ii] / K : 0;
+            tinv[ii] = (ii < n) ? s_inv[tok[ii]] : 0.f;
+          }
+          float acc[TT];
+#pragma unroll
+          for (int ii = 0; ii < TT; ++ii) acc[ii] = 0.f;
+#pragma unroll 1
+          for (int kk = 0; kk < DF_KBG; ++kk) {
+            const int kb = grp * DF_KBG + kk;
+            const uint8_t* piece = stage + kb * SLAB_KB;
+            const uint4 cw = *reinterpret_cast<const uint4*>(piece + 256 * mat + 16 * r);
+            const float d = __half2float(*reinterpret_cast<const __half*>(piece + 512 + 4 * r + 2 * mat));
+            const Masked cm = mask_codes(cw);
+#pragma unroll
+            for (int ii = 0; ii < TT; ++ii) {
+              if (ii < n) {
+                const QBlock& a = sqx[tok[ii] * KB_GU + kb];
+                uint32_t hi[16], lo[16];
+                unpack_words(a, hi, lo);
+                const int vv = dot64(cm, hi, lo) - a.qoff;
+                acc[ii] = fmaf(d * (a.s64 * tinv[ii]), (float)vv, acc[ii]);
+              }
             }
           }
-        }
 #pragma unroll
-        for (int ii = 0; ii < TT; ++ii)
-          if (ii < n) red[(grp * TT + ii) * SLAB + r] = make_float2(accg[ii], accu[ii]);
-        __syncthreads();
-        if (tid < SLAB * n) {  // (row, token): the 8 groups added in group order
-          const int r2 = tid % SLAB, ii = tid / SLAB;
-          float g = 0.f, uu = 0.f;
+          for (int ii = 0; ii < TT; ++ii)
+            if (ii < n) red[((grp * 2 + mat) * TT + ii) * SLAB + r] = acc[ii];
+          __syncthreads();
+          if (tid < SLAB * n) {  // (row, token): the groups added in group order
+            const int r2 = tid % SLAB, ii = tid / SLAB;
+            float g = 0.f, uu = 0.f;
 #pragma unroll
-          for (int q = 0; q < DF_KG; ++q) {
-            const float2 v = red[(q * TT + ii) * SLAB + r2];
-            g += v.x;
-            uu += v.y;
+            for (int q = 0; q < DF_KG; ++q) {
+              g += red[((q * 2 + 0) * TT + ii) * SLAB + r2];
+              uu += red[((q * 2 + 1) * TT + ii) * SLAB + r2];
+            }
+            st_tagged(p.htag + (size_t)(q0 + ii) * FF + sl * SLAB + r2, silu_mul(g, uu), ep);
           }
-          p.hf[(size_t)(q0 + ii) * FF + sl * SLAB + r2] = silu_mul(g, uu);
         }
-        }
-        __syncthreads();  // every h store issued; the stage and the reduction buffer are free
-        if (tid == 0) {
-          red_release_add(&h_cnt[WS_SYNC_STRIDE * j], 1);
-          if (u + G * NS < n_units) issue(u + G * NS, i + NS);
-        }
-        continue;
       } else {
         // -------- down unit: row tile rtd of expert slot j --------
         const int v = u - n_gu;
         const int j = v / DF_DN, rtd = v % DF_DN;
         const int n = s_tn[j], q0 = s_tq[j];
-        // h of the expert's n tokens (contiguous rows of hf) into shared memory with one bulk copy,
-        // once all 40 slabs are in; the token activations' space is free (no gate/up unit follows)
+        // h of the expert's n tokens (n * FF words from slot q0 on) into shared memory; the token
+        // activations' space is free (no gate/up unit follows)
         float* sh = reinterpret_cast<float*>(sqx);
         static_assert(sizeof(float) * TT * FF <= sizeof(QBlock) * TT * KB_GU, "h fits the activation space");
-        if (tid == 0) {
-          bool okh = spin_until_geq(&h_cnt[WS_SYNC_STRIDE * j], DF_GU, p.status);
-          if (s_qx_pending) okh = mbar_wait(&bar_qx, 0u, p.status) && okh;  // (only if no gate/up unit ran)
-          s_qx_pending = 0;
-          if (okh) {
-            fence_proxy_async_global();
-            mbar_expect_tx(&bar_h, (uint32_t)(sizeof(float) * n * FF));
-            bulk_g2s(sh, p.hf + (size_t)q0 * FF, (uint32_t)(sizeof(float) * n * FF), &bar_h);
-            s_h_pending = n_dn & 1;
-          }
-          s_flag = okh ? 1 : 0;
+        const uint64_t* hsrc = p.htag + (size_t)q0 * FF;
+        if (!poll_tagged<(TT * FF + DF_THREADS - 1) / DF_THREADS>(hsrc, [](int x) { return x; }, n * FF, ep, sh,
+                                                                 p.status)) {
+          if (tid == 0) s_ok = 0;
+          __syncthreads();
+          break;
         }
-        __syncthreads();
-        if (!s_flag) { if (tid == 0) s_ok = 0; __syncthreads(); break; }
-        const bool hok = mbar_wait(&bar_h, (uint32_t)(n_dn & 1), p.status);
-        ++n_dn;
-        if (!__syncthreads_and(hok ? 1 : 0)) { if (tid == 0) s_ok = 0; __syncthreads(); break; }
-        if (tid == 0) s_h_pending = -1;
         if constexpr (MMA) {  // h in fp16 fragment order: hx[kb][t4][slot][16 halves]
           uint8_t* hx = reinterpret_cast<uint8_t*>(sq);
           for (int idx = tid; idx < n * KB_D * 4; idx += DF_THREADS) {
@@ -561,8 +733,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         }
         if (tid == 0) s_pending[st] = -1;
         if constexpr (MMA) {
-          // warp w: rows 32 w .. 32 w + 31 of the tile (two 16-row groups), all 10 k-blocks; columns =
-          // the expert's pairs
+          // warp w: rows 16 w .. 16 w + 15 of the tile, all 10 k-blocks; columns = the expert's pairs
           const int g = lane >> 2, t4 = lane & 3;
           uint32_t subq[4];
 #pragma unroll
@@ -571,7 +742,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             subq[m] = *reinterpret_cast<const uint32_t*>(&s2);
           }
           const uint8_t* hx = reinterpret_cast<const uint8_t*>(sq);
-          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          constexpr int RG = RT / (16 * DF_NW);  // 16-row groups per warp
+          float acc[RG][4] = {};
 #pragma unroll 2
           for (int kb = 0; kb < KB_D; ++kb) {
             const uint8_t* chunk = stage + kb * D_CHUNK;
@@ -583,8 +755,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             }
             const uint32_t bq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-            for (int rg = 0; rg < 2; ++rg) {
-              const int R0 = 32 * warp + 16 * rg + g, R1 = R0 + 8;
+            for (int rg = 0; rg < RG; ++rg) {
+              const int R0 = 16 * RG * warp + 16 * rg + g, R1 = R0 + 8;
               uint32_t h0[8], h1[8];
               codes_to_half2(*reinterpret_cast<const uint32_t*>(chunk + 16 * R0 + 4 * t4), subq, h0);
               codes_to_half2(*reinterpret_cast<const uint32_t*>(chunk + 16 * R1 + 4 * t4), subq, h1);
@@ -601,84 +773,108 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             }
           }
 #pragma unroll
-          for (int rg = 0; rg < 2; ++rg)
+          for (int rg = 0; rg < RG; ++rg)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = 2 * t4 + (e & 1);
-              const int row = rtd * RT + 32 * warp + 16 * rg + g + 8 * (e >> 1);
-              if (col < n) p.parts[(size_t)s_pair[q0 + col] * H + row] = acc[rg][e];
+              const int row = rtd * RT + 16 * RG * warp + 16 * rg + g + 8 * (e >> 1);
+              if (col < n) st_tagged(p.ptag + (size_t)s_pair[q0 + col] * H + row, acc[rg][e], ep);
             }
         } else {
-        float acc[TT];
+          // thread: row tid % RT, k-blocks [5 h, 5 h + 5) with h = tid / RT; the halves' sums meet in
+          // the activation space (free once h is quantised)
+          static_assert(DF_THREADS == 2 * RT, "two threads per down row");
+          const int row = tid % RT, hh = tid / RT;
+          float acc[TT];
 #pragma unroll
-        for (int ii = 0; ii < TT; ++ii) acc[ii] = 0.f;
+          for (int ii = 0; ii < TT; ++ii) acc[ii] = 0.f;
 #pragma unroll 1
-        for (int kb = 0; kb < KB_D; ++kb) {
-          const uint8_t* chunk = stage + kb * D_CHUNK;
-          const uint4 cw = *reinterpret_cast<const uint4*>(chunk + 16 * tid);
-          const float d = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * tid));
-          const Masked m = mask_codes(cw);
+          for (int kk = 0; kk < KB_D / 2; ++kk) {
+            const int kb = hh * (KB_D / 2) + kk;
+            const uint8_t* chunk = stage + kb * D_CHUNK;
+            const uint4 cw = *reinterpret_cast<const uint4*>(chunk + 16 * row);
+            const float d = __half2float(*reinterpret_cast<const __half*>(chunk + 2048 + 2 * row));
+            const Masked m = mask_codes(cw);
 #pragma unroll
-          for (int ii = 0; ii < TT; ++ii) {
-            if (ii < n) {
-              const QBlock& a = sq[kb * TT + ii];
-              uint32_t hi[16], lo[16];
-              unpack_words(a, hi, lo);
-              const int vv = dot64(m, hi, lo) - a.qoff;
-              acc[ii] = fmaf(d * a.s64, (float)vv, acc[ii]);
+            for (int ii = 0; ii < TT; ++ii) {
+              if (ii < n) {
+                const QBlock& a = sq[kb * TT + ii];
+                uint32_t hi[16], lo[16];
+                unpack_words(a, hi, lo);
+                const int vv = dot64(m, hi, lo) - a.qoff;
+                acc[ii] = fmaf(d * a.s64, (float)vv, acc[ii]);
+              }
             }
           }
-        }
-        const int row = rtd * RT + tid;
+          float* rdn = reinterpret_cast<float*>(sqx);  // [2][TT][RT]
+          static_assert(sizeof(float) * 2 * TT * RT <= sizeof(QBlock) * TT * KB_GU, "down halves fit");
 #pragma unroll
-        for (int ii = 0; ii < TT; ++ii)
-          if (ii < n) p.parts[(size_t)s_pair[q0 + ii] * H + row] = acc[ii];
-        }
-        const int row = rtd * RT + tid;  // combine: one output row per thread
-        __syncthreads();
-        if (tid == 0) s_flag = (atom_acq_rel_add(&cnt_dn[WS_SYNC_STRIDE * rtd], 1) == D - 1) ? 1 : 0;
-        __syncthreads();
-        if (s_flag) {
-          float pv[TT * K], xv[TT];  // every load first, then the k-ordered sums
+          for (int ii = 0; ii < TT; ++ii)
+            if (ii < n) rdn[(hh * TT + ii) * RT + row] = acc[ii];
+          __syncthreads();
+          if (tid < RT)
 #pragma unroll
-          for (int q = 0; q < TT * K; ++q) pv[q] = (q < T * K) ? __ldcg(p.parts + (size_t)q * H + row) : 0.f;
-#pragma unroll
-          for (int tt = 0; tt < TT; ++tt) xv[tt] = (tt < T && p.residual) ? p.x[(size_t)tt * H + row] : 0.f;
-#pragma unroll
-          for (int tt = 0; tt < TT; ++tt) {
-            if (tt < T) {
-              float a = 0.f;
-#pragma unroll
-              for (int k = 0; k < K; ++k) a = fmaf(s_w[tt * K + k], pv[tt * K + k], a);
-              p.out[(size_t)tt * H + row] = p.residual ? xv[tt] + a : a;
-            }
-          }
-          if (tid == 0) cnt_dn[WS_SYNC_STRIDE * rtd] = 0;
+            for (int ii = 0; ii < TT; ++ii)
+              if (ii < n)
+                st_tagged(p.ptag + (size_t)s_pair[q0 + ii] * H + rtd * RT + tid,
+                          rdn[ii * RT + tid] + rdn[(TT + ii) * RT + tid], ep);
         }
       }
       __syncthreads();  // everyone is done with this stage and with sq / red
       if (tid == 0 && u + G * NS < n_units) issue(u + G * NS, i + NS);
     }
+
+    // ---- 4. combine: for each down unit (slot j, tile rtd) of this CTA, rows [j rp, (j + 1) rp) of
+    // the tile: every pair's output polled into shared memory, then the k-ordered weighted sums ----
+    const int rp = (RT + D - 1) / D;  // D >= K, so rp <= 13
+    float* cs = reinterpret_cast<float*>(sqx);  // [pair][row of the share]
+    static_assert(sizeof(float) * TT * K * ((RT + K - 1) / K) <= sizeof(QBlock) * TT * KB_GU, "share fits");
+    for (int u = c; u < n_units && s_ok; u += G) {
+      if (u < n_gu) continue;
+      const int v = u - n_gu;
+      const int j = v / DF_DN, rtd = v % DF_DN;
+      const int r0 = j * rp, nr = min(RT, r0 + rp) - r0;
+      if (nr <= 0) continue;
+      const uint64_t* psrc = p.ptag + rtd * RT + r0;
+      constexpr int KC = (TT * K * ((RT + K - 1) / K) + DF_THREADS - 1) / DF_THREADS;
+      if (!poll_tagged<KC>(psrc, [nr](int x) { return (x / nr) * H + x % nr; }, P * nr, ep, cs, p.status)) {
+        if (tid == 0) s_ok = 0;
+        __syncthreads();
+        break;
+      }
+      if (tid < nr * T) {
+        const int r = tid % nr, tt = tid / nr;
+        const int row = rtd * RT + r0 + r;
+        const float xv = p.residual ? p.x[(size_t)tt * H + row] : 0.f;
+        float a = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) a = fmaf(s_w[tt * K + k], cs[(tt * K + k) * nr + r], a);
+        p.out[(size_t)tt * H + row] = p.residual ? xv + a : a;
+      }
+      __syncthreads();
+    }
   }
 
-  // ---- leave: drain copies still in flight (only after a failed wait), last CTA resets counters ----
+  // ---- leave: drain copies still in flight (only after a failed wait); the last CTA advances the
+  // epoch (at the last tag, it clears the exchange area and starts again from 0) ----
   __syncthreads();
   if (tid == 0) {
     for (int st = 0; st < NS; ++st)
       if (s_pending[st] >= 0) mbar_wait(&bars[st], (uint32_t)s_pending[st], p.status);
-    if (s_qx_pending) mbar_wait(&bar_qx, 0u, p.status);
-    if (s_h_pending >= 0) mbar_wait(&bar_h, (uint32_t)s_h_pending, p.status);
     __threadfence();
     s_flag = (atomicAdd(exit_cnt, 1) == G - 1) ? 1 : 0;
   }
   __syncthreads();
   if (s_flag) {
     __threadfence();
-    for (int w = tid; w < WS_SYNC_WORDS; w += DF_THREADS)
-      if (w != WS_SYNC_EXIT) p.sync[w] = 0;
+    if (ep == 0xffffffffu) {
+      uint4* area = reinterpret_cast<uint4*>(p.dots);
+      for (size_t w = tid; w < (DX_END - DX_DOTS) / 16; w += DF_THREADS) area[w] = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
     if (tid == 0) {
       __threadfence();
+      p.sync[WS_SYNC_EPOCH] = ep == 0xffffffffu ? 0 : (int)ep;
       *exit_cnt = 0;
     }
   }
@@ -707,6 +903,7 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
       return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     grid = sms * (per_sm < 2 ? per_sm : 2);
+    if (grid < 32) return cudaErrorInvalidConfiguration;  // router rows per CTA are bounded by 16
     if (dev >= 0 && dev < 64) g_info[dev].grid[vi] = grid;
   }
   void* args[] = {(void*)&prm};
@@ -718,7 +915,7 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
-                                const float* x, int T, int residual, float* out, int32_t* ids, float* weights,
+                                const float* x, int T, int residual, int alias, float* out, int32_t* ids, float* weights,
                                 const WsLayout& L, char* ws, cudaStream_t s) {
   DecodeParams prm;
   prm.x = x;
@@ -727,17 +924,16 @@ cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_ro
   prm.E = ex.n_expert;
   prm.q2_offset = ex.q2_offset;
   prm.residual = residual;
+  prm.alias = alias;
   prm.wr = w_router;
   prm.bias = bias;
   prm.blobs = (const uint8_t*)ex.blobs;
   prm.stride = ex.blob_stride;
   prm.ids_out = ids;
   prm.w_out = weights;
-  prm.dots = (float*)(ws + L.dots_rep);
-  prm.sumsq = (float*)(ws + L.sumsq);
-  prm.qx = (QBlock*)(ws + L.qx);
-  prm.hf = (float*)(ws + L.hf);
-  prm.parts = (float*)(ws + L.parts);
+  prm.dots = (uint64_t*)(ws + DX_DOTS);
+  prm.htag = (uint64_t*)(ws + DX_H);
+  prm.ptag = (uint64_t*)(ws + DX_PARTS);
   prm.sync = (int*)(ws + WS_SYNC);
   prm.status = (int*)(ws + L.status);
   if (T <= 1) return launch_tt<1>(prm, s);
