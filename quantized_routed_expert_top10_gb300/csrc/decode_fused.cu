@@ -170,6 +170,51 @@ __device__ __forceinline__ void to_fragment_order(const float* v, uint32_t* h) {
   }
 }
 
+// Quantise a 64-value block held as two halves in adjacent lanes (lane 2i + hb holds values
+// 32 hb .. 32 hb + 31 in v, and its own max |v| in amax) into a QBlock: the same QBlock that
+// quantise_block_warp builds, with one thread per half block instead of a warp per block.  Whole
+// warps call it (the halves meet through shuffles); only `live` lanes store.
+__device__ __forceinline__ void quantise_half_block(const float (&v)[32], float amax, bool live, int hb,
+                                                    int q2_offset, QBlock* dst) {
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  int qv[32];
+  int qs = 0;
+  const float qinv = amax > 0.f ? 32767.f / amax : 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    qv[i] = amax > 0.f ? max(-32767, min(32767, __float2int_rn(v[i] * qinv))) : 0;
+    qs += qv[i];
+  }
+  qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+  if (!live) return;
+  // word (q4, m), q4 = 2 hb + g: bytes b' = 0..3 of the values 16 q4 + 4 b' + m
+  uint32_t hw[8], lw[8];
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint32_t hi = 0, lo = 0;
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int val = qv[16 * g + 4 * bb + m];
+        hi |= (uint32_t)((val >> 8) & 0xFF) << (8 * bb);
+        lo |= (uint32_t)(val & 0xFF) << (8 * bb);
+      }
+      hw[4 * g + m] = hi;
+      lw[4 * g + m] = lo;
+    }
+  uint4* dh = reinterpret_cast<uint4*>(dst->hi + 8 * hb);
+  uint4* dl = reinterpret_cast<uint4*>(dst->lo + 8 * hb);
+  dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+  if (hb == 0) {
+    dst->s64 = amax > 0.f ? (amax / 32767.f) * (1.f / 64.f) : 0.f;
+    dst->qoff = 64 * q2_offset * qs;
+  }
+}
+
 template <int TT>
 __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const DecodeParams p) {
   constexpr bool MMA = TT >= 2;  // one token: dp4a on the codes; more: tensor-core products
@@ -198,7 +243,6 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ float s_bias[EMAX];
   TopKScratch* s_topk = reinterpret_cast<TopKScratch*>(ring);  // [DF_NW], routing only (ring idle)
   static_assert(sizeof(TopKScratch) * DF_NW <= DF_UNIT, "top-k scratch fits the first stage");
-  __shared__ int32_t s_qtmp[DF_NW][64];
   __shared__ int s_flag, s_ok, s_nact, s_dots0;
 
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -263,47 +307,9 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       amax = fmaxf(amax, fabsf(v[i]));
       ss = fmaf(v[i], v[i], ss);
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     ss = warp_sum(ss);
     if (lane == 0) s_ssq[warp] = ss;
-    int qv[32];
-    int qs = 0;
-    const float qinv = amax > 0.f ? 32767.f / amax : 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      qv[i] = amax > 0.f ? max(-32767, min(32767, __float2int_rn(v[i] * qinv))) : 0;
-      qs += qv[i];
-    }
-    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-    if (live) {
-      // word (q4, m), q4 = 2 hb + g: bytes b' = 0..3 of the values 16 q4 + 4 b' + m
-      uint32_t hw[8], lw[8];
-#pragma unroll
-      for (int g = 0; g < 2; ++g)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint32_t hi = 0, lo = 0;
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const int val = qv[16 * g + 4 * bb + m];
-            hi |= (uint32_t)((val >> 8) & 0xFF) << (8 * bb);
-            lo |= (uint32_t)(val & 0xFF) << (8 * bb);
-          }
-          hw[4 * g + m] = hi;
-          lw[4 * g + m] = lo;
-        }
-      QBlock& dst = sqx[b];
-      uint4* dh = reinterpret_cast<uint4*>(dst.hi + 8 * hb);
-      uint4* dl = reinterpret_cast<uint4*>(dst.lo + 8 * hb);
-      dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-      dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-      if (hb == 0) {
-        dst.s64 = amax > 0.f ? (amax / 32767.f) * (1.f / 64.f) : 0.f;
-        dst.qoff = 64 * p.q2_offset * qs;
-      }
-    }
+    quantise_half_block(v, amax, live, hb, p.q2_offset, sqx + b);
   } else {
     // fp16 x in fragment order, xs[16-group][token][16 halves]; warp w takes tokens w, w + 4, lane
     // the 16-groups lane + 32 i
@@ -578,16 +584,23 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           }
           const uint8_t* xs = reinterpret_cast<const uint8_t*>(sqx);
           float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-          for (int kk = 0; kk < KB_GU / DF_NW; ++kk) {
-            const int kb = warp * (KB_GU / DF_NW) + kk;
+          // software pipeline: the A fragments of k-block kb + 1 are built while kb's MMAs run
+          uint32_t hg0[8], hg1[8], hu0[8], hu1[8];
+          __half2 sc0, sc1;
+          auto dequant = [&](int kb) {
             const uint8_t* piece = stage + kb * SLAB_KB;
-            const uint32_t wg0 = *reinterpret_cast<const uint32_t*>(piece + 16 * g + 4 * t4);
-            const uint32_t wg1 = *reinterpret_cast<const uint32_t*>(piece + 16 * (g + 8) + 4 * t4);
-            const uint32_t wu0 = *reinterpret_cast<const uint32_t*>(piece + 256 + 16 * g + 4 * t4);
-            const uint32_t wu1 = *reinterpret_cast<const uint32_t*>(piece + 256 + 16 * (g + 8) + 4 * t4);
-            const __half2 sc0 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * g);
-            const __half2 sc1 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * (g + 8));
+            codes_to_half2(*reinterpret_cast<const uint32_t*>(piece + 16 * g + 4 * t4), subq, hg0);
+            codes_to_half2(*reinterpret_cast<const uint32_t*>(piece + 16 * (g + 8) + 4 * t4), subq, hg1);
+            codes_to_half2(*reinterpret_cast<const uint32_t*>(piece + 256 + 16 * g + 4 * t4), subq, hu0);
+            codes_to_half2(*reinterpret_cast<const uint32_t*>(piece + 256 + 16 * (g + 8) + 4 * t4), subq, hu1);
+            sc0 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * g);
+            sc1 = *reinterpret_cast<const __half2*>(piece + 512 + 4 * (g + 8));
+          };
+          constexpr int KPW = KB_GU / DF_NW;  // k-blocks per warp
+          dequant(warp * KPW);
+#pragma unroll
+          for (int kk = 0; kk < KPW; ++kk) {
+            const int kb = warp * KPW + kk;
             uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
             if (g < T) {
               const uint4* xp = reinterpret_cast<const uint4*>(xs + ((size_t)(kb * 4 + t4) * T + g) * 32);
@@ -595,23 +608,24 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
               x1 = xp[1];
             }
             const uint32_t bq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            uint32_t hg0[8], hg1[8], hu0[8], hu1[8];
-            codes_to_half2(wg0, subq, hg0);
-            codes_to_half2(wg1, subq, hg1);
-            codes_to_half2(wu0, subq, hu0);
-            codes_to_half2(wu1, subq, hu1);
+            uint32_t a_g[4][4], a_u[4][4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              a_g[s][0] = hg0[2 * s]; a_g[s][1] = hg1[2 * s]; a_g[s][2] = hg0[2 * s + 1]; a_g[s][3] = hg1[2 * s + 1];
+              a_u[s][0] = hu0[2 * s]; a_u[s][1] = hu1[2 * s]; a_u[s][2] = hu0[2 * s + 1]; a_u[s][3] = hu1[2 * s + 1];
+            }
+            const __half2 c0 = sc0, c1 = sc1;
+            if (kk + 1 < KPW) dequant(kb + 1);
             // even and odd k-steps into separate accumulators: two independent MMA chains per matrix
             float cg[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             float cu[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-              const uint32_t a_g[4] = {hg0[2 * s], hg1[2 * s], hg0[2 * s + 1], hg1[2 * s + 1]};
-              const uint32_t a_u[4] = {hu0[2 * s], hu1[2 * s], hu0[2 * s + 1], hu1[2 * s + 1]};
-              mma_16816(cg[s & 1], a_g, bq[2 * s], bq[2 * s + 1]);
-              mma_16816(cu[s & 1], a_u, bq[2 * s], bq[2 * s + 1]);
+              mma_16816(cg[s & 1], a_g[s], bq[2 * s], bq[2 * s + 1]);
+              mma_16816(cu[s & 1], a_u[s], bq[2 * s], bq[2 * s + 1]);
             }
-            const float dg0 = __low2float(sc0), du0 = __high2float(sc0);
-            const float dg1 = __low2float(sc1), du1 = __high2float(sc1);
+            const float dg0 = __low2float(c0), du0 = __high2float(c0);
+            const float dg1 = __low2float(c1), du1 = __high2float(c1);
             ag[0] = fmaf(dg0, cg[0][0] + cg[1][0], ag[0]); ag[1] = fmaf(dg0, cg[0][1] + cg[1][1], ag[1]);
             ag[2] = fmaf(dg1, cg[0][2] + cg[1][2], ag[2]); ag[3] = fmaf(dg1, cg[0][3] + cg[1][3], ag[3]);
             au[0] = fmaf(du0, cu[0][0] + cu[1][0], au[0]); au[1] = fmaf(du0, cu[0][1] + cu[1][1], au[1]);
@@ -720,11 +734,22 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
             dst[1] = make_uint4(hq[4], hq[5], hq[6], hq[7]);
           }
         } else {
-          for (int item = warp; item < n * KB_D; item += DF_THREADS / 32) {  // quantise h, one warp per block
-            const int ii = item / KB_D, kb = item % KB_D;
-            const float2 hv = reinterpret_cast<const float2*>(sh + ii * FF + kb * QK)[lane];
-            quantise_block_warp(hv.x, hv.y, p.q2_offset, sq + kb * TT + ii, s_qtmp[warp]);
+          // quantise h: one thread per half block (T = 1 here: 10 blocks)
+          static_assert(TT * KB_D * 2 <= DF_THREADS, "one thread per half block of h");
+          const int blk = tid >> 1, hb = tid & 1;
+          const bool live = blk < n * KB_D;
+          const int ii = live ? blk / KB_D : 0, kb = live ? blk % KB_D : 0;
+          float v[32];
+          float amax = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = live ? reinterpret_cast<const float4*>(sh + ii * FF + kb * QK + 32 * hb)[q]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+          if (warp * 32 < 2 * n * KB_D) quantise_half_block(v, amax, live, hb, p.q2_offset, sq + kb * TT + ii);
         }
         if (!__syncthreads_and(mbar_wait(&bars[st], par, p.status) ? 1 : 0)) {
           if (tid == 0) s_ok = 0;
