@@ -258,6 +258,9 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     }
     fence_mbar_init();
     s_ok = 1;
+    // the router words this CTA will poll into L2 now, so the publishers' stores and the polls meet
+    // in L2 instead of each paying a miss later
+    bulk_prefetch_l2(p.dots + (size_t)(c % WS_NREP) * DECODE_T_MAX * EMAX, (uint32_t)(sizeof(uint64_t) * T * EMAX));
   }
   // loads for later steps, issued first: the bias (used by the top-k) and this CTA's first router
   // row (two warps per row, each over one half of the columns), with the x values it multiplies
@@ -554,9 +557,9 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       mbar_expect_tx(&bars[st], DF_UNIT);
       bulk_g2s_stream(ring + (size_t)st * DF_UNIT, src, DF_UNIT, &bars[st], pol);
     };
-    if (tid == 0)
-      for (int i = 0; i < NS; ++i)
-        if (c + G * i < n_units) issue(c + G * i, i);
+    // only the first unit's copy now: issued alone, it is not queued behind every CTA's later stages,
+    // so the first unit starts computing while the rest streams in (issued once it has arrived)
+    if (tid == 0 && c < n_units) issue(c, 0);
 
     int i = 0;
     for (int u = c; u < n_units; u += G, ++i) {
@@ -572,7 +575,12 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           __syncthreads();
           break;
         }
-        if (tid == 0) s_pending[st] = -1;
+        if (tid == 0) {
+          s_pending[st] = -1;
+          if (i == 0)
+            for (int k = 1; k < NS; ++k)
+              if (c + G * k < n_units) issue(c + G * k, k);
+        }
         if constexpr (MMA) {
           // warp w: k-blocks [5 w, 5 w + 5) of the 16-row slab, all T tokens as columns
           const int g = lane >> 2, t4 = lane & 3;
@@ -756,7 +764,12 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           __syncthreads();
           break;
         }
-        if (tid == 0) s_pending[st] = -1;
+        if (tid == 0) {
+          s_pending[st] = -1;
+          if (i == 0)
+            for (int k = 1; k < NS; ++k)
+              if (c + G * k < n_units) issue(c + G * k, k);
+        }
         if constexpr (MMA) {
           // warp w: rows 16 w .. 16 w + 15 of the tile, all 10 k-blocks; columns = the expert's pairs
           const int g = lane >> 2, t4 = lane & 3;
