@@ -169,12 +169,12 @@ KERNEL_SOURCES = {
 # workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
 # sources at capture time: once a source changes the figure no longer describes the kernel (null).
 NCU_TRAFFIC = {
-    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (28,997,632 / 28,997,376 /
-    # 28,997,504 B read, 0 B written)
-    ("verify_4tok_1layer", "DECODE_LAYER"): (28997504, "e1d7d92a181e9284"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,639,168 / 29,630,976 /
+    # 29,630,976 B read, 6,912 / 0 / 0 B written)
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29636011, "2fa0582a05568b3a"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (281050624 + 12867840, "c85a0ef53f848cde"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (121381888 + 146027264, "c85a0ef53f848cde"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (281075968 + 12581632, "48d549082ee35f29"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (122246656 + 146020608, "48d549082ee35f29"),
 }
 
 
@@ -383,9 +383,12 @@ def step_breakdown(qre, fn, args, stream, L, steps=2):
 
 
 def path_dtype(T):
-    """Arithmetic of the path: decode = dp4a on 2-bit codes x int16-split activations (int32 partial
-    sums, fp32 accumulation); prefill = fp16 x fp16 tensor-core products with fp32 accumulation."""
-    return "s8 dp4a (q2 x int16-split x), fp32 acc" if T <= 8 else "f16 tcgen05, fp32 acc"
+    """Arithmetic of the path: one token = dp4a on 2-bit codes x int16-split activations (int32 partial
+    sums, fp32 accumulation); 2-8 tokens = fp16 x fp16 warp MMA (mma.sync) with fp32 accumulation;
+    prefill = fp16 x fp16 tcgen05 products with fp32 accumulation."""
+    if T <= 1:
+        return "s8 dp4a (q2 x int16-split x), fp32 acc"
+    return "f16 mma.sync, fp32 acc" if T <= 8 else "f16 tcgen05, fp32 acc"
 
 
 def workload_config(cfg, seed, world, need_flush, distinct):
