@@ -6,18 +6,18 @@
 // Q2_0 codes {0,1,2,3} mean {-1,0,1,2} x the block scale.
 //
 // Per expert e with n_e tokens (its slots in the grouping), two grouped GEMMs with the weights as the
-// M = 128 operand ("swap AB") and the expert's tokens as N (up to 128 per tile):
+// M = 128 operand ("swap AB") and the expert's tokens as N (up to 256 per tile):
 //   gate/up:  [g; u] (2 x 128 rows x N) = [G_rt; U_rt] (128 x 2560) * X_e^T, h = silu(g) * u -> Hg (fp16)
 //   down:     [y_2rp; y_2rp+1] (2 x 128 rows x N) = [D_2rp; D_2rp+1] (128 x 640 each) * H_e^T
 //             -> parts[pair][row] (fp32); two row tiles per item so each token tile is read half as often
 // Warp roles in each persistent CTA (one per SM; work items = (tile, 128-row tile of the weights)):
 //   warp 0      streams the token tile and the Q2_0 code chunk of each 64-wide k-block with
-//               cp.async.bulk into a 6-stage ring;
+//               cp.async.bulk into a 4-stage (gate/up) or 6-stage (down) ring;
 //   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
 //               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
 //               exact) in a 2-stage ring of weight tiles;
-//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into one of two TMEM accumulator buffers and
-//               commits to the stages' "empty" mbarriers;
+//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (one half for a tile of up to 128
+//               tokens, both for a wider one) and commits to the stages' "empty" mbarriers;
 //   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
 //               epilogue while the next item accumulates into the other buffer;
 //   warp 2      owns the TMEM allocation.
@@ -32,9 +32,9 @@
 namespace strata {
 namespace {
 
-constexpr int TCN = 128;        // max tokens per tile (MMA N)
+constexpr int TCN = 256;        // max tokens per tile (MMA N)
+constexpr int TCN_HALF = 128;   // tiles up to this wide take one half of TMEM (double-buffered)
 constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 64 fp16
-constexpr uint32_t B_TILE = TCN * 128;      // up to 128 token rows x 64 fp16
 
 // Position in the emitted order (0..15) of weight j of a 16-group: the order is 0,8,1,9,..,7,15.
 __host__ __device__ __forceinline__ int pi16_inv(int j) { return 2 * (j & 3) + 8 * ((j >> 2) & 1) + ((j >> 3) & 1); }
@@ -50,9 +50,9 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ active,
                                                          const int32_t* __restrict__ n_active, int E, int P,
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
-                                                         int32_t* __restrict__ counts, int max_tiles,
-                                                         int* __restrict__ status) {
-  __shared__ int s_pad[EMAX], s_nt[EMAX], s_scratch[32];
+                                                         TcTile* __restrict__ half_tiles, int32_t* __restrict__ counts,
+                                                         int max_tiles, int max_half_tiles, int* __restrict__ status) {
+  __shared__ int s_pad[EMAX], s_nt[EMAX], s_nh[EMAX], s_scratch[32];
   const int i = threadIdx.x;
   const int na = max(0, min(*n_active, E));
   int e = 0, q0 = 0, n = 0;
@@ -70,20 +70,28 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   }
   s_pad[i] = (i < na) ? (n + 7) / 8 * 8 : 0;
   s_nt[i] = (i < na) ? (n + TCN - 1) / TCN : 0;
+  s_nh[i] = (i < na) ? (n + TCN_HALF - 1) / TCN_HALF : 0;
   __syncthreads();
   const int ppad = cta_exclusive_scan(s_pad, s_pad, EMAX, s_scratch);
   const int ntiles = cta_exclusive_scan(s_nt, s_nt, EMAX, s_scratch);
+  const int nhalf = cta_exclusive_scan(s_nh, s_nh, EMAX, s_scratch);
   if (i < na) {
     exps[i] = TcExpert{e, q0, n, s_pad[i]};
     for (int t = 0; t * TCN < n; ++t) {
       const int idx = s_nt[i] + t;
       if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t * TCN, min(TCN, n - t * TCN), s_pad[i] + t * TCN};
     }
+    for (int t = 0; t * TCN_HALF < n; ++t) {
+      const int idx = s_nh[i] + t;
+      if (idx < max_half_tiles)
+        half_tiles[idx] = TcTile{e, q0 + t * TCN_HALF, min(TCN_HALF, n - t * TCN_HALF), s_pad[i] + t * TCN_HALF};
+    }
   }
   if (i == 0) {
     counts[0] = na;
     counts[1] = min(ntiles, max_tiles);
     counts[2] = ppad;
+    counts[3] = min(nhalf, max_half_tiles);
   }
 }
 
@@ -192,22 +200,34 @@ struct TcParams {
 // warps 12..15: epilogue (one TMEM lane = one weight row per thread).
 // gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
 // down (GU = false): item = (tile, pair of row tiles 2rp, 2rp + 1 of down): both share the token tile.
-// TMEM accumulator buffer b (of 2): matrix j in columns [b*256 + j*128, +128).
+// TMEM: a tile of up to 128 tokens accumulates in half b (alternating) -- matrix j in columns
+// [b*256 + j*128, +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256
+// tokens, one dequantised weight tile serving all of them) takes both halves, matrix j in [j*256, +256).
 constexpr int TC_THREADS = 512;
-constexpr int NS_TMA = 6;  // stages of (token tile, code chunks)
 constexpr int NS_A = 2;    // stages of dequantised weight tiles
 template <bool GU>
 struct TcGeo {
   static constexpr int NMAT = 2;
   static constexpr int KBN = GU ? KB_GU : KB_D;          // k-blocks per item
-  static constexpr int RTN = GU ? RT_GU : RT_D / 2;      // items per token tile
+  static constexpr int RTN = GU ? RT_GU : RT_D / 2;      // weight row tiles (or pairs) per token tile
   static constexpr int CODE = GU ? GU_CHUNK : 2 * D_CHUNK; // code bytes per k-block
+  static constexpr uint32_t B_TILE = (GU ? TCN : TCN_HALF) * 128;  // token rows x 64 fp16
   static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
+  static constexpr int NS_TMA = GU ? 4 : 6;            // stages of (token tile, code chunks)
   static constexpr uint32_t A_STAGE = NMAT * A_TILE;
-  static constexpr uint32_t TMEM_BUF = NMAT * TCN;     // accumulator columns per buffer
-  static constexpr uint32_t TMEM_COLS = 2 * TMEM_BUF;  // double buffered
+  static constexpr uint32_t TMEM_COLS = 512;           // two halves of NMAT x 128 columns
   static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
+
+// Item -> (token tile, weight row tile rt).  Gate/up items take tiles of up to 256 tokens (one
+// dequantised weight tile serves all of them); down items take tiles of up to 128 tokens, so their
+// short 10-k-block main loops keep double-buffered accumulators.
+template <bool GU>
+__device__ __forceinline__ TcTile item_tile(const TcParams& p, int item, int& rt) {
+  rt = item % TcGeo<GU>::RTN;
+  return p.tiles[item / TcGeo<GU>::RTN];
+}
 
 template <bool GU>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams p) {
@@ -215,6 +235,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* tma_ring = smem;
+  constexpr int NS_TMA = G::NS_TMA;
+  constexpr uint32_t B_TILE = G::B_TILE;
   uint8_t* a_ring = smem + (size_t)NS_TMA * G::TMA_STAGE;
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
   __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
@@ -244,7 +266,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int n_items = p.counts[1] * G::RTN;
+  const int n_items = p.counts[GU ? 1 : 3] * G::RTN;
   int* status = p.status;
 
   if (warp == 0) {
@@ -253,8 +275,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       const uint64_t pol = policy_evict_first();
       int it = 0;
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
-        const TcTile tl = p.tiles[item / G::RTN];
-        const int rt = item % G::RTN;
+        int rt;
+        const TcTile tl = item_tile<GU>(p, item, rt);
+        if (tl.n == 0) continue;
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint8_t* blob = p.blobs + (int64_t)tl.e * p.stride;
         for (int kb = 0; kb < G::KBN; ++kb, ++it) {
@@ -286,18 +309,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      int it = 0, ti = 0;
-      for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x, ++ti) {
-        const TcTile tl = p.tiles[item / G::RTN];
+      int it = 0, n_small = 0;
+      int uses[2] = {0, 0};  // items issued into each TMEM half so far
+      for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
+        int rt;
+        const TcTile tl = item_tile<GU>(p, item, rt);
+        if (tl.n == 0) continue;
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
-        const int b = ti & 1;
-        if (ti >= 2 && !mbar_wait(&tmem_empty[b], (uint32_t)(((ti >> 1) - 1) & 1), status)) {
+        // a tile wider than 128 takes both halves (matrix j in half j); a narrower one takes half b,
+        // alternating, matrix j at column b * 256 + 128 j
+        const bool wide = nrows > TCN_HALF;
+        const int b = wide ? 0 : (n_small++ & 1);
+        bool okw = true;
+        for (int h = 0; h < 2; ++h)
+          if ((wide || h == b) && uses[h] >= 1)
+            okw = okw && mbar_wait(&tmem_empty[h], (uint32_t)((uses[h] - 1) & 1), status);
+        if (!okw) {
           s_fail = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t acc = tmem + b * G::TMEM_BUF;
+        const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u);
+        const uint32_t mat_cols = wide ? 256u : 128u;
         for (int kb = 0; kb < G::KBN; ++kb, ++it) {
           const int s = it % NS_TMA, sa = it % NS_A;
           if (!mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status) ||
@@ -313,13 +347,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
             const uint64_t ad = tc::smem_desc_sw128(smem_u32(ast + mat * A_TILE));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc::mma_f16(acc + mat * TCN, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_f16(acc + mat * mat_cols, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           tc::mma_commit(&empty_tma[s]);
           tc::mma_commit(&empty_a[sa]);
         }
         if (s_fail) break;
-        tc::mma_commit(&tmem_full[b]);
+        for (int h = 0; h < 2; ++h)
+          if (wide || h == b) {
+            tc::mma_commit(&tmem_full[h]);
+            ++uses[h];
+          }
       }
       tc::mma_commit(&mma_done);  // every MMA this thread issued has finished before TMEM is released
       mbar_wait(&mma_done, 0u, status);
@@ -331,6 +369,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      int rt_unused;
+      if (item_tile<GU>(p, item, rt_unused).n == 0) continue;
       for (int kb = 0; kb < G::KBN; ++kb, ++it) {
         const int s = it % NS_TMA, sa = it % NS_A;
         if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], (uint32_t)((it / NS_A - 1) & 1), status);
@@ -362,16 +402,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
     // ---------------- epilogue ----------------
     const int q = warp & 3;
     const int erow = 32 * q + lane;
-    int ti = 0;
+    int n_small = 0;
+    int uses[2] = {0, 0};  // items drained from each TMEM half so far (same assignment as the issuer)
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ti) {
-      const TcTile tl = p.tiles[item / G::RTN];
-      const int rt = item % G::RTN;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      int rt;
+      const TcTile tl = item_tile<GU>(p, item, rt);
+      if (tl.n == 0) continue;
       const int nrows = (tl.n + 15) / 16 * 16;
-      const int b = ti & 1;
-      ok = ok && mbar_wait(&tmem_full[b], (uint32_t)((ti >> 1) & 1), status);
+      const bool wide = nrows > TCN_HALF;
+      const int b = wide ? 0 : (n_small++ & 1);
+      for (int h = 0; h < 2; ++h)
+        if (wide || h == b) ok = ok && mbar_wait(&tmem_full[h], (uint32_t)(uses[h] & 1), status);
       tc::fence_after_sync();
-      const uint32_t acc = tmem + b * G::TMEM_BUF + ((uint32_t)(32 * q) << 16);
+      const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u) + ((uint32_t)(32 * q) << 16);
+      const uint32_t mat_cols = wide ? 256u : 128u;
       if (GU) {
         const int k = rt * 128 + erow;  // h index = the down projection's contraction index
         const int kbd = k >> 6, k64 = k & 63;
@@ -379,7 +424,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         for (int ch = 0; ch < nrows / 16; ++ch) {
           float g[16], u[16];
           tc::tmem_ld16(acc + 16 * ch, g);
-          tc::tmem_ld16(acc + TCN + 16 * ch, u);
+          tc::tmem_ld16(acc + mat_cols + 16 * ch, u);
           if (ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -398,7 +443,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         for (int ch = 0; ch < nrows / 16; ++ch) {
           float y0[16], y1[16];
           tc::tmem_ld16(acc + 16 * ch, y0);
-          tc::tmem_ld16(acc + TCN + 16 * ch, y1);
+          tc::tmem_ld16(acc + mat_cols + 16 * ch, y1);
           if (ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -415,7 +460,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[b]);
+      if (lane == 0)
+        for (int h = 0; h < 2; ++h)
+          if (wide || h == b) mbar_arrive(&tmem_empty[h]);
+      for (int h = 0; h < 2; ++h)
+        if (wide || h == b) ++uses[h];
     }
   }
   tc::fence_before_sync();
@@ -436,21 +485,22 @@ int64_t tc_rows_cap(int T) { return (int64_t)T * K + 8 * EMAX + TCN; }
 size_t tc_xg_bytes(int T) { return (size_t)KB_GU * tc_rows_cap(T) * 128; }
 size_t tc_hg_bytes(int T) { return (size_t)KB_D * tc_rows_cap(T) * 128; }
 size_t tc_meta_bytes(int T) {
-  return sizeof(TcExpert) * EMAX + sizeof(TcTile) * (size_t)(T * K / TCN + EMAX) + 64;
+  return sizeof(TcExpert) * EMAX + sizeof(TcTile) * (size_t)(T * K / TCN + EMAX + T * K / TCN_HALF + EMAX) + 64;
 }
 
 cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
                               const int32_t* expert_off,
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
                               uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s) {
-  const int max_tiles = T * K / TCN + EMAX;
+  const int max_tiles = T * K / TCN + EMAX, max_half = T * K / TCN_HALF + EMAX;
   TcExpert* exps = reinterpret_cast<TcExpert*>(meta);
   TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * EMAX);
-  int32_t* counts = reinterpret_cast<int32_t*>(meta + sizeof(TcExpert) * EMAX + sizeof(TcTile) * max_tiles);
+  TcTile* half_tiles = tiles + max_tiles;
+  int32_t* counts = reinterpret_cast<int32_t*>(half_tiles + max_half);
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
-                                                    counts, max_tiles, status));
+                                                    half_tiles, counts, max_tiles, max_half, status));
   STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, T * K, exps, counts, xg,
                                                                                    rows_cap, status));
   cudaError_t err = cudaGetLastError();
@@ -471,6 +521,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   TcParams dp = gp;
   dp.act = hg;
+  dp.tiles = half_tiles;
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<false>::SMEM)) != cudaSuccess)
     return err;
