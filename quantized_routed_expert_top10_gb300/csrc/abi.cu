@@ -65,7 +65,7 @@ strata_status route_and_group(const float* x, int T, int norm, const uint16_t* w
 
 strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, const float* bias, const float* x,
                          int32_t T, int32_t flags, float* out, int32_t* ids, float* weights, void* ws,
-                         size_t ws_bytes, cudaStream_t s) {
+                         size_t ws_bytes, cudaStream_t s, const DecodeNext* next = nullptr) {
   STRATA_TRY(check_T(T));
   if (!w_router || !x || !out) return STRATA_E_INVAL;
   STRATA_TRY(check_experts(ex));
@@ -81,7 +81,7 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
   const int norm = (flags & STRATA_MOE_RESIDUAL_RMSNORM) ? 1 : 0;
   if (T <= DECODE_T_MAX) {
     const int alias = (x < out + (size_t)T * H && out < x + (size_t)T * H) ? 1 : 0;  // in-place call
-    STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, alias, out, ids_d, wts_d, L, w, s));
+    STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, alias, out, ids_d, wts_d, next, L, w, s));
     return STRATA_OK;
   }
   STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
@@ -202,9 +202,16 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
   // stack ends with one copy back into x
   float* bufs[2] = {x, T <= DECODE_T_MAX && ws ? (float*)((char*)ws + ws_layout(T).xpp) : x};
   for (int l = 0; l < n_layers; ++l) {
+    // decode layers look one layer ahead: the next router on this layer's input names the experts to
+    // prefetch into L2
+    DecodeNext next{};
+    if (l + 1 < n_layers)
+      next = DecodeNext{w_router + (size_t)(l + 1) * E * H, bias ? bias + (size_t)(l + 1) * E : nullptr,
+                        (const uint8_t*)ex[l + 1].blobs, ex[l + 1].blob_stride};
     STRATA_TRY(layer_impl(&ex[l], w_router + (size_t)l * E * H, bias ? bias + (size_t)l * E : nullptr, bufs[l & 1], T,
                           STRATA_MOE_RESIDUAL_RMSNORM, bufs[(l + 1) & 1], ids ? ids + (size_t)l * T * K : nullptr,
-                          weights ? weights + (size_t)l * T * K : nullptr, ws, ws_bytes, (cudaStream_t)stream));
+                          weights ? weights + (size_t)l * T * K : nullptr, ws, ws_bytes, (cudaStream_t)stream,
+                          l + 1 < n_layers ? &next : nullptr));
   }
   if (bufs[n_layers & 1] != x)
     STRATA_CUDA(cudaMemcpyAsync(x, bufs[n_layers & 1], sizeof(float) * (size_t)T * H, cudaMemcpyDeviceToDevice,

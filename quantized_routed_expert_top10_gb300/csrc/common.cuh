@@ -82,7 +82,10 @@ static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sy
 constexpr size_t DX_DOTS = WS_HEADER;                                              // [WS_NREP][8][EMAX]
 constexpr size_t DX_H = DX_DOTS + sizeof(uint64_t) * WS_NREP * DECODE_T_MAX * EMAX;  // [8 * K][FF]
 constexpr size_t DX_PARTS = DX_H + sizeof(uint64_t) * DECODE_T_MAX * K * FF;          // [8 * K][H]
-constexpr size_t DX_END = DX_PARTS + sizeof(uint64_t) * DECODE_T_MAX * K * H;
+constexpr size_t DX_PRED = DX_PARTS + sizeof(uint64_t) * DECODE_T_MAX * K * H;    // [8][EMAX] next layer
+constexpr size_t DX_PRED_IDS = DX_PRED + sizeof(uint64_t) * DECODE_T_MAX * EMAX;     // [1 + 8 * K]
+constexpr size_t DX_END = (DX_PRED_IDS + sizeof(uint64_t) * (1 + DECODE_T_MAX * K) + 255) / 256 * 256;
+static_assert(DX_END % 256 == 0 && DX_PRED_IDS % 256 == 0, "exchange area regions stay 256-byte aligned");
 
 struct WsLayout {
   size_t status, cnt_route;
@@ -287,9 +290,17 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
                               uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
+// The next layer of a decode stack, for the lookahead (its router on this layer's input predicts its
+// experts, which are prefetched into L2 while this layer finishes).
+struct DecodeNext {
+  const uint16_t* wr;  // [E][H] bf16
+  const float* bias;   // [E] or null
+  const uint8_t* blobs;
+  int64_t stride;
+};
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
                                 const float* x, int T, int residual, int alias, float* out, int32_t* ids, float* weights,
-                                const WsLayout& L, char* ws, cudaStream_t s);
+                                const DecodeNext* next, const WsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_pack_device(const uint8_t* canonical, int64_t src_stride, uint8_t* packed,
                                int64_t dst_stride, int64_t n_blobs, cudaStream_t s);
 }  // namespace strata

@@ -63,6 +63,12 @@ struct DecodeParams {
   uint64_t* dots;    // exchange area: router dot products [WS_NREP][DECODE_T_MAX][EMAX]
   uint64_t* htag;    //                h of each slot [DECODE_T_MAX * K][FF]
   uint64_t* ptag;    //                expert outputs of each pair [DECODE_T_MAX * K][H]
+  uint64_t* pred;    //                next layer's predicted router logits [DECODE_T_MAX][EMAX]
+  uint64_t* pred_ids;  //              [0]: D' predicted experts, [1 + j]: their ids, ascending
+  const uint16_t* wr_next;  // next layer of a stack (lookahead), or null
+  const float* bias_next;
+  const uint8_t* blobs_next;
+  int64_t stride_next;
   int* sync;         // ws sync words (WS_SYNC)
   int* status;
 };
@@ -215,6 +221,32 @@ __device__ __forceinline__ void quantise_half_block(const float (&v)[32], float 
   }
 }
 
+// Bounded poll (one warp) of one token's E logit words src[e] (lane holds e = lane + 32 j) into lg
+// until all carry `tag`; the warp leaves together.  False (and ST_TIMEOUT) once the wait limit passes.
+__device__ __forceinline__ bool warp_poll_logits(const uint64_t* src, int E, uint32_t tag, float* lg, int* status) {
+  const int lane = threadIdx.x & 31;
+  uint32_t missing = (1u << (E >> 5)) - 1u;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    uint64_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if ((missing >> j) & 1) w[j] = ld_tagged(src + lane + 32 * j);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (((missing >> j) & 1) && has_tag(w[j], tag)) {
+        lg[j] = tagged_value(w[j]);
+        missing &= ~(1u << j);
+      }
+    if (__all_sync(0xffffffffu, missing == 0)) return true;
+    if (__shfl_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs ? 1 : 0, 0)) {
+      if (lane == 0) set_status(status, ST_TIMEOUT);
+      return false;
+    }
+    __nanosleep(100);  // back off: every CTA polls the same lines
+  }
+}
+
 template <int TT>
 __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const DecodeParams p) {
   constexpr bool MMA = TT >= 2;  // one token: dp4a on the codes; more: tensor-core products
@@ -240,6 +272,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ int s_wcnt[DF_NW];
   __shared__ int s_pair[TT * K];
   __shared__ float s_rpart[DF_NW][TT];
+  __shared__ float s_lpart[4][TT];  // lookahead rows' partial sums (warps 4-7)
   __shared__ float s_bias[EMAX];
   TopKScratch* s_topk = reinterpret_cast<TopKScratch*>(ring);  // [DF_NW], routing only (ring idle)
   static_assert(sizeof(TopKScratch) * DF_NW <= DF_UNIT, "top-k scratch fits the first stage");
@@ -287,6 +320,28 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         const float* xs = p.x + half * (H / 2) + 8 * lane + 256 * i;
         xa[i] = __ldg(reinterpret_cast<const float4*>(xs));
         xb[i] = __ldg(reinterpret_cast<const float4*>(xs + 4));
+      }
+    }
+  }
+
+  // previous layer of a stack predicted this layer's experts (words tagged with the previous call's
+  // tag): this CTA prefetches its share of their units into L2 while routing goes on.  A hint only.
+  if (tid == DF_THREADS - 1) {
+    if (p.wr_next && TT <= 4)  // this CTA's rows of the next layer's router, for the lookahead below
+      for (int e = c; e < E; e += G) bulk_prefetch_l2(p.wr_next + (size_t)e * H, (uint32_t)(sizeof(uint16_t) * H));
+    const uint64_t w0 = ld_tagged(p.pred_ids);
+    if (has_tag(w0, ep - 1u)) {
+      const int D = min(__float_as_int(tagged_value(w0)), DF_MAXD);
+      for (int u = c; u < D * (DF_GU + DF_DN); u += G) {
+        const bool gu = u < D * DF_GU;
+        const int j = gu ? u / DF_GU : (u - D * DF_GU) / DF_DN;
+        const uint64_t wj = ld_tagged(p.pred_ids + 1 + j);
+        const int e = __float_as_int(tagged_value(wj));
+        if (!has_tag(wj, ep - 1u) || e < 0 || e >= E) continue;
+        const uint8_t* b = p.blobs + (int64_t)e * p.stride;
+        bulk_prefetch_l2(gu ? b + (int64_t)(u % DF_GU) * SLAB_BYTES
+                            : b + D_REGION + (int64_t)((u - D * DF_GU) % DF_DN) * KB_D * D_CHUNK,
+                         DF_UNIT);
       }
     }
   }
@@ -408,6 +463,63 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     }
   }
 
+  // ---- lookahead (decode stacks, T <= 4): while warps 0-3 route, warps 4-7 compute this CTA's rows of
+  // the next layer's router on this layer's normalised input and publish them for the lookahead CTA
+  // (step 5), which names the experts the next layer's CTAs prefetch into L2 ----
+  if (TT <= 4 && p.wr_next && warp >= 4) {
+    const int lw = warp - 4, lt = tid - 128;
+    float inv1 = 1.f;  // one token: 1/rms from the staging's partial sums (as the routing computes it)
+    if constexpr (!MMA) {
+      float ssq = 0.f;
+#pragma unroll
+      for (int w = 0; w < DF_NW; ++w) ssq += s_ssq[w];
+      inv1 = p.residual ? 1.f / sqrtf(ssq / (float)H + 1e-6f) : 1.f;
+    }
+    for (int e0 = c; e0 < E; e0 += 2 * G) {
+      const int e = e0 + G * (lw >> 1);
+      float acc[TT];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+      if (e < E) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(p.wr_next + (size_t)e * H);
+#pragma unroll
+        for (int i = 0; i < H / 512; ++i) {
+          const int col = (lw & 1) * (H / 2) + 8 * lane + 256 * i;
+          float wf[8];
+          bf16x8_to_f32(__ldg(wrow + (col >> 3)), wf);
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            if (t < T) {
+              const float4 a4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
+              const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col + 4));
+              float sacc = acc[t];
+              sacc = fmaf(wf[0], a4.x, sacc); sacc = fmaf(wf[1], a4.y, sacc);
+              sacc = fmaf(wf[2], a4.z, sacc); sacc = fmaf(wf[3], a4.w, sacc);
+              sacc = fmaf(wf[4], b4.x, sacc); sacc = fmaf(wf[5], b4.y, sacc);
+              sacc = fmaf(wf[6], b4.z, sacc); sacc = fmaf(wf[7], b4.w, sacc);
+              acc[t] = sacc;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const float r = warp_sum(acc[t]);
+        if (lane == 0) s_lpart[lw][t] = r;
+      }
+      named_barrier(1, 128);
+      if (lt < 2 * TT) {
+        const int w2 = lt / TT, t = lt % TT, e2 = e0 + G * w2;
+        if (e2 < E && t < T) {
+          const float inv = MMA ? s_inv[t] : inv1;
+          const float v = (s_lpart[2 * w2][t] + s_lpart[2 * w2 + 1][t]) * inv + (p.bias_next ? __ldg(p.bias_next + e2) : 0.f);
+          st_tagged(p.pred + (size_t)t * EMAX + e2, v, ep);
+        }
+      }
+      named_barrier(1, 128);
+    }
+  }
+
   // ---- 2. top-10 and grouping, redundantly in every CTA ----
   if (tid == 0) {
     s_nact = 0;
@@ -423,34 +535,15 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     const uint64_t* src = p.dots + ((size_t)(c % WS_NREP) * DECODE_T_MAX + t) * EMAX;
     const int per = E >> 5;
     float lg[16];
-    uint32_t missing = (1u << per) - 1u;
-    const unsigned long long t0 = globaltimer();
     if (t > 0) {
+      const unsigned long long t0 = globaltimer();
       while (*reinterpret_cast<volatile int*>(&s_dots0) == 0) {
         if (__shfl_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs ? 1 : 0, 0)) break;
         __nanosleep(128);
       }
       __syncwarp();
     }
-    while (true) {
-      uint64_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if ((missing >> j) & 1) w[j] = ld_tagged(src + lane + 32 * j);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (((missing >> j) & 1) && has_tag(w[j], ep)) {
-          lg[j] = tagged_value(w[j]);
-          missing &= ~(1u << j);
-        }
-      if (__all_sync(0xffffffffu, missing == 0)) break;
-      if (__shfl_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs ? 1 : 0, 0)) {
-        if (lane == 0) set_status(p.status, ST_TIMEOUT);
-        okr = false;
-        break;
-      }
-      __nanosleep(100);  // back off: every CTA polls the same lines
-    }
+    okr = warp_poll_logits(src, E, ep, lg, p.status);
     if (t == 0 && lane == 0) *reinterpret_cast<volatile int*>(&s_dots0) = 1;
     if (!okr) break;
     if (p.alias) fence_acq_rel_gpu();  // acquire: pairs with every publisher's release
@@ -891,6 +984,44 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       }
       __syncthreads();
     }
+
+    // ---- 5. lookahead CTA (the last one, which has the fewest units): the next layer's predicted
+    // top-10 of every token and the distinct experts among them ----
+    if (p.wr_next && c == G - 1 && s_ok) {
+      bool okp = true;
+      for (int t = warp; t < T && okp; t += DF_NW) {
+        float lg[16];
+        okp = warp_poll_logits(p.pred + (size_t)t * EMAX, E, ep, lg, p.status);
+        if (okp) {
+          int id;
+          float w;
+          top_k_warp_fn([&](int e) { return lg[e >> 5]; }, E, s_topk[warp], &id, &w);
+          if (lane < K) s_first[t * K + lane] = id;  // (grouping scratch, free now)
+        }
+      }
+      // the distinct predicted experts in ascending id order (the order of expert slots), published
+      // for the next layer's CTAs, which prefetch them into L2 while they route
+      if (__syncthreads_and(okp ? 1 : 0)) {
+        if (tid < P) {
+          const int e = s_first[tid];
+          int f = 1;
+          for (int q = 0; q < tid; ++q) f &= (s_first[q] != e);
+          s_pair[tid] = f;  // (grouping scratch, free now)
+        }
+        __syncthreads();
+        if (tid < P && s_pair[tid]) {
+          const int e = s_first[tid];
+          int j = 0;
+          for (int q = 0; q < P; ++q) j += (s_pair[q] && s_first[q] < e) ? 1 : 0;
+          st_tagged(p.pred_ids + 1 + j, __int_as_float(e), ep);
+        }
+        if (tid == 0) {
+          int d = 0;
+          for (int q = 0; q < P; ++q) d += s_pair[q];
+          st_tagged(p.pred_ids, __int_as_float(d), ep);
+        }
+      }
+    }
   }
 
   // ---- leave: drain copies still in flight (only after a failed wait); the last CTA advances the
@@ -954,7 +1085,7 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
 
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
                                 const float* x, int T, int residual, int alias, float* out, int32_t* ids, float* weights,
-                                const WsLayout& L, char* ws, cudaStream_t s) {
+                                const DecodeNext* next, const WsLayout& L, char* ws, cudaStream_t s) {
   DecodeParams prm;
   prm.x = x;
   prm.out = out;
@@ -972,6 +1103,12 @@ cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_ro
   prm.dots = (uint64_t*)(ws + DX_DOTS);
   prm.htag = (uint64_t*)(ws + DX_H);
   prm.ptag = (uint64_t*)(ws + DX_PARTS);
+  prm.pred = (uint64_t*)(ws + DX_PRED);
+  prm.pred_ids = (uint64_t*)(ws + DX_PRED_IDS);
+  prm.wr_next = next ? next->wr : nullptr;
+  prm.bias_next = next ? next->bias : nullptr;
+  prm.blobs_next = next ? next->blobs : nullptr;
+  prm.stride_next = next ? next->stride : 0;
   prm.sync = (int*)(ws + WS_SYNC);
   prm.status = (int*)(ws + L.status);
   if (T <= 1) return launch_tt<1>(prm, s);
