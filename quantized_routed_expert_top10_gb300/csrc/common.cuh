@@ -72,7 +72,8 @@ constexpr size_t WS_CNT_ROUTE = 64; // int32 router last-CTA counter
 constexpr size_t WS_SYNC = 4096;
 constexpr int WS_SYNC_EXIT = 1;
 constexpr int WS_SYNC_EPOCH = 32;  // own 128-byte line
-constexpr int WS_SYNC_WORDS = 64;
+constexpr int WS_SYNC_SMRANK = 64;  // [256] per-SM arrival tickets (which of an SM's CTAs is which)
+constexpr int WS_SYNC_WORDS = WS_SYNC_SMRANK + 256;
 constexpr int WS_NREP = 16;        // replicas of the router dot products (every CTA reads all of them)
 static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sync words must fit the header");
 // Decode exchange area, right after the header at the same offset for every T >= 1: 64-bit words

@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ float s_bias[EMAX];
   TopKScratch* s_topk = reinterpret_cast<TopKScratch*>(ring);  // [DF_NW], routing only (ring idle)
   static_assert(sizeof(TopKScratch) * DF_NW <= DF_UNIT, "top-k scratch fits the first stage");
-  __shared__ int s_flag, s_ok, s_nact, s_dots0;
+  __shared__ int s_flag, s_ok, s_nact, s_dots0, s_tw0;
 
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
@@ -327,6 +327,10 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   // previous layer of a stack predicted this layer's experts (words tagged with the previous call's
   // tag): this CTA prefetches its share of their units into L2 while routing goes on.  A hint only.
   if (tid == DF_THREADS - 1) {
+    // one or two tokens: the SM's two CTAs route on different warps (0-1, 2-3), hence on different
+    // schedulers -- the top-10 is a latency chain that two warps on one scheduler would share
+    s_tw0 = TT <= 2 ? 2 * (int)(atomicAdd(reinterpret_cast<unsigned*>(p.sync + WS_SYNC_SMRANK + (sm_id() & 255)), 1u) & 1u)
+                    : 0;
     if (p.wr_next && TT <= 4)  // this CTA's rows of the next layer's router, for the lookahead below
       for (int e = c; e < E; e += G) bulk_prefetch_l2(p.wr_next + (size_t)e * H, (uint32_t)(sizeof(uint16_t) * H));
     const uint64_t w0 = ld_tagged(p.pred_ids);
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   }
   __syncthreads();
   bool okr = true;
-  for (int t = warp; t < T; t += DF_NW) {
+  for (int t = (warp - s_tw0 + DF_NW) % DF_NW; t < T; t += DF_NW) {
     // this token's dot products from replica c % WS_NREP: poll until all carry this call's tag.
     // Only token 0's warp polls from the start; the others wait (in shared memory) until token 0's
     // products are all in -- the publishers wrote every token's products together -- so the CTAs
