@@ -24,8 +24,8 @@
 // that a value is ready and fetching it take one round trip.  When the output aliases the input,
 // the router publication is a release (after every read of x by its CTA) and its polling an
 // acquire, which orders all reads of x before any write of the output.  Every wait is bounded by
-// %globaltimer and records STRATA_E_TIMEOUT in the status word.  The last CTA to leave advances the
-// call epoch.
+// %globaltimer and records STRATA_E_TIMEOUT in the status word.  Every CTA advances the call epoch as
+// it leaves (a max with no reply).
 #include "device_common.cuh"
 
 namespace strata {
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
-  // this call's tag: one more than the previous call's (the last CTA to leave advances the epoch)
+  // this call's tag: one more than the previous call's (the CTAs advance the epoch as they leave)
   const uint32_t ep = (uint32_t)ld_relaxed(p.sync + WS_SYNC_EPOCH) + 1u;
 
   if (tid == 0) {
@@ -1028,26 +1028,31 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     }
   }
 
-  // ---- leave: drain copies still in flight (only after a failed wait); the last CTA advances the
-  // epoch (at the last tag, it clears the exchange area and starts again from 0) ----
+  // ---- leave: drain copies still in flight (only after a failed wait) and advance the epoch: every
+  // CTA adds its max(epoch, tag) without waiting for a reply -- every CTA read the epoch before it
+  // published anything, and the next call reads it after this one has ended.  At the last tag the CTAs
+  // count out instead, and the last one clears the exchange area and restarts the epoch from 0. ----
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0)
     for (int st = 0; st < NS; ++st)
       if (s_pending[st] >= 0) mbar_wait(&bars[st], (uint32_t)s_pending[st], p.status);
+  if (ep != 0xffffffffu) {
+    if (tid == 0) red_max_u32(reinterpret_cast<unsigned*>(p.sync + WS_SYNC_EPOCH), ep);
+    return;
+  }
+  if (tid == 0) {
     __threadfence();
     s_flag = (atomicAdd(exit_cnt, 1) == G - 1) ? 1 : 0;
   }
   __syncthreads();
   if (s_flag) {
     __threadfence();
-    if (ep == 0xffffffffu) {
-      uint4* area = reinterpret_cast<uint4*>(p.dots);
-      for (size_t w = tid; w < (DX_END - DX_DOTS) / 16; w += DF_THREADS) area[w] = make_uint4(0, 0, 0, 0);
-    }
+    uint4* area = reinterpret_cast<uint4*>(p.dots);
+    for (size_t w = tid; w < (DX_END - DX_DOTS) / 16; w += DF_THREADS) area[w] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (tid == 0) {
       __threadfence();
-      p.sync[WS_SYNC_EPOCH] = ep == 0xffffffffu ? 0 : (int)ep;
+      p.sync[WS_SYNC_EPOCH] = 0;
       *exit_cnt = 0;
     }
   }

@@ -92,6 +92,10 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Relaxed max with no reply.
+__device__ __forceinline__ void red_max_u32(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Acquire-release add returning the old value.
 __device__ __forceinline__ int atom_acq_rel_add(int* p, int v) {
   int old;
