@@ -21,12 +21,12 @@ def layer0():
     torch.cuda.empty_cache()
 
 
-def parity(layer0, x, wr, bias, flags=0, q2_offset=1):
+def parity(layer0, x, wr, bias, flags=0, q2_offset=1, E=512):
     blobs, cache = layer0
-    out, ids, w = run_layer(blobs, wr, bias, x, flags, q2_offset)
+    out, ids, w = run_layer(blobs, wr, bias, x, flags, q2_offset, E=E)
     ref_r = oracle.route(x, wr, bias, residual=bool(flags))
     ties = check_routing(ids, ref_r["ids"], ref_r["logits"])
-    ref = oracle.moe_layer(x, wr, bias, cache.layer_list(0, ids), q2_offset=q2_offset, residual=bool(flags),
+    ref = oracle.moe_layer(x, wr, bias, cache.layer_list(0, ids, E), q2_offset=q2_offset, residual=bool(flags),
                            ids_in=ids)
     np.testing.assert_allclose(w, ref["w"], rtol=0, atol=W_TOL)
     if flags:
@@ -48,6 +48,13 @@ def test_config1_verify_window(layer0):
 @pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 37, 300])
 def test_ragged_token_counts_with_zipf_bias(layer0, T):
     parity(layer0, gen.activations_fast(11, T), gen.router_weights(0, 0), gen.zipf_bias(0, 0))
+
+
+@pytest.mark.parametrize("E,T", [(256, 1), (256, 4), (256, 8), (256, 300), (32, 4), (32, 64)])
+def test_smaller_expert_counts(layer0, E, T):
+    """The 256-expert variant (and the smallest E the ABI takes): routing over the first E experts of
+    the layer, decode (T <= 8) and prefill paths."""
+    parity(layer0, gen.activations_fast(13, T), gen.router_weights(0, 0, E_=E), None, E=E)
 
 
 @pytest.mark.parametrize("T", [1, 3, 20])
