@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   float* red = reinterpret_cast<float*>(sq);                            // gate/up partial sums
   static_assert(sizeof(float) * 2 * DF_NW * TT * SLAB <= sizeof(QBlock) * KB_D * TT, "reduction fits");
   __shared__ uint64_t bars[NS];
+  __shared__ uint64_t bar_x;
   __shared__ int s_pending[NS];
   __shared__ float s_inv[TT];
   __shared__ float s_ssq[DF_NW];
@@ -284,13 +285,25 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   // this call's tag: one more than the previous call's (the CTAs advance the epoch as they leave)
   const uint32_t ep = (uint32_t)ld_relaxed(p.sync + WS_SYNC_EPOCH) + 1u;
 
+  // up to four tokens: every token's x (fp32) into the ring (idle until the units) with bulk copies,
+  // read from there by the staging, the router rows and the lookahead
+  constexpr bool XS = TT <= 4;
+  const float* xs32 = reinterpret_cast<const float*>(ring + 8192);  // after the top-k scratch
+  static_assert(!XS || 8192 + sizeof(float) * TT * H <= (size_t)NS * DF_UNIT, "x fits the ring");
+  static_assert(sizeof(TopKScratch) * DF_NW <= 8192, "top-k scratch before x");
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars[s], 1);
       s_pending[s] = -1;
     }
+    mbar_init(&bar_x, 1);
     fence_mbar_init();
     s_ok = 1;
+    if (XS) {
+      mbar_expect_tx(&bar_x, (uint32_t)(sizeof(float) * T * H));
+      for (int t = 0; t < T; ++t)
+        bulk_g2s(ring + 8192 + sizeof(float) * t * H, p.x + (size_t)t * H, (uint32_t)(sizeof(float) * H), &bar_x);
+    }
     // the router words this CTA will poll into L2 now, so the publishers' stores and the polls meet
     // in L2 instead of each paying a miss later
     bulk_prefetch_l2(p.dots + (size_t)(c % WS_NREP) * DECODE_T_MAX * EMAX, (uint32_t)(sizeof(uint64_t) * T * EMAX));
@@ -306,7 +319,6 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   }
   const int half = warp & 1;
   uint4 wq[H / 512];
-  float4 xa[TT == 1 ? H / 512 : 1], xb[TT == 1 ? H / 512 : 1];
   {
     const int e = c + G * (warp >> 1);
     if (e < E) {
@@ -314,15 +326,14 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 #pragma unroll
       for (int i = 0; i < H / 512; ++i) wq[i] = __ldg(wrow + ((half * (H / 2) + 8 * lane + 256 * i) >> 3));
     }
-    if constexpr (TT == 1) {
-#pragma unroll
-      for (int i = 0; i < H / 512; ++i) {
-        const float* xs = p.x + half * (H / 2) + 8 * lane + 256 * i;
-        xa[i] = __ldg(reinterpret_cast<const float4*>(xs));
-        xb[i] = __ldg(reinterpret_cast<const float4*>(xs + 4));
-      }
-    }
   }
+  // x of token t at column col: the ring copy (up to four tokens) or global memory
+  auto x4 = [&](int t, int col) {
+    return XS ? *reinterpret_cast<const float4*>(xs32 + (size_t)t * H + col)
+              : __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
+  };
+  __syncthreads();  // the barriers are initialised before anyone waits on them
+  if (XS) mbar_wait(&bar_x, 0u, p.status);  // bounded; a failure is in the status word
 
   // previous layer of a stack predicted this layer's experts (words tagged with the previous call's
   // tag): this CTA prefetches its share of their units into L2 while routing goes on.  A hint only.
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     float v[32];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 a = live ? __ldg(reinterpret_cast<const float4*>(p.x + b * QK + 32 * hb) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 a = live ? x4(0, b * QK + 32 * hb + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
       v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
     }
     float amax = 0.f, ss = 0.f;
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       for (int i = 0; i < H / 16 / 32; ++i)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          a[i][q] = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + 16 * (lane + 32 * i) + 4 * q));
+          a[i][q] = x4(t, 16 * (lane + 32 * i) + 4 * q);
       float ss = 0.f;
 #pragma unroll
       for (int i = 0; i < H / 16 / 32; ++i)
@@ -424,14 +435,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           if (t < T) {
-            float4 a4, b4;
-            if (TT == 1 && it == 0) {
-              a4 = xa[TT == 1 ? i : 0];
-              b4 = xb[TT == 1 ? i : 0];
-            } else {
-              a4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
-              b4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col + 4));
-            }
+            const float4 a4 = x4(t, col), b4 = x4(t, col + 4);
             float sacc = acc[t];
             sacc = fmaf(wf[0], a4.x, sacc); sacc = fmaf(wf[1], a4.y, sacc);
             sacc = fmaf(wf[2], a4.z, sacc); sacc = fmaf(wf[3], a4.w, sacc);
@@ -494,8 +498,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
             if (t < T) {
-              const float4 a4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
-              const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col + 4));
+              const float4 a4 = x4(t, col), b4 = x4(t, col + 4);
               float sacc = acc[t];
               sacc = fmaf(wf[0], a4.x, sacc); sacc = fmaf(wf[1], a4.y, sacc);
               sacc = fmaf(wf[2], a4.z, sacc); sacc = fmaf(wf[3], a4.w, sacc);
@@ -1033,9 +1036,11 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   // published anything, and the next call reads it after this one has ended.  At the last tag the CTAs
   // count out instead, and the last one clears the exchange area and restarts the epoch from 0. ----
   __syncthreads();
-  if (tid == 0)
+  if (tid == 0) {
     for (int st = 0; st < NS; ++st)
       if (s_pending[st] >= 0) mbar_wait(&bars[st], (uint32_t)s_pending[st], p.status);
+    if (XS) mbar_wait(&bar_x, 0u, p.status);  // (returns at once unless its first wait failed)
+  }
   if (ep != 0xffffffffu) {
     if (tid == 0) red_max_u32(reinterpret_cast<unsigned*>(p.sync + WS_SYNC_EPOCH), ep);
     return;
