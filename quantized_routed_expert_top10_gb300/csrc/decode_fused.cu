@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ int s_pending[NS];
   __shared__ float s_inv[TT];
   __shared__ float s_ssq[DF_NW];
+  __shared__ float s_ssqt[DF_NW][TT];  // per warp and token (two or more tokens)
   __shared__ float s_dot[ROWS_MAX][TT];
   __shared__ __align__(16) int s_ids[(TT * K + 3) / 4 * 4];
   __shared__ float s_w[TT * K];
@@ -288,8 +289,9 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   // up to four tokens: every token's x (fp32) into the ring (idle until the units) with bulk copies,
   // read from there by the staging, the router rows and the lookahead
   constexpr bool XS = TT <= 4;
+  constexpr int XSTR = H + 4;  // token stride of the ring copy (floats): rows start 4 banks apart
   const float* xs32 = reinterpret_cast<const float*>(ring + 8192);  // after the top-k scratch
-  static_assert(!XS || 8192 + sizeof(float) * TT * H <= (size_t)NS * DF_UNIT, "x fits the ring");
+  static_assert(!XS || 8192 + sizeof(float) * TT * XSTR <= (size_t)NS * DF_UNIT, "x fits the ring");
   static_assert(sizeof(TopKScratch) * DF_NW <= 8192, "top-k scratch before x");
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     if (XS) {
       mbar_expect_tx(&bar_x, (uint32_t)(sizeof(float) * T * H));
       for (int t = 0; t < T; ++t)
-        bulk_g2s(ring + 8192 + sizeof(float) * t * H, p.x + (size_t)t * H, (uint32_t)(sizeof(float) * H), &bar_x);
+        bulk_g2s(ring + 8192 + sizeof(float) * t * XSTR, p.x + (size_t)t * H, (uint32_t)(sizeof(float) * H), &bar_x);
     }
     // the router words this CTA will poll into L2 now, so the publishers' stores and the polls meet
     // in L2 instead of each paying a miss later
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   }
   // x of token t at column col: the ring copy (up to four tokens) or global memory
   auto x4 = [&](int t, int col) {
-    return XS ? *reinterpret_cast<const float4*>(xs32 + (size_t)t * H + col)
+    return XS ? *reinterpret_cast<const float4*>(xs32 + (size_t)t * XSTR + col)
               : __ldg(reinterpret_cast<const float4*>(p.x + (size_t)t * H + col));
   };
   __syncthreads();  // the barriers are initialised before anyone waits on them
@@ -384,33 +386,40 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     if (lane == 0) s_ssq[warp] = ss;
     quantise_half_block(v, amax, live, hb, p.q2_offset, sqx + b);
   } else {
-    // fp16 x in fragment order, xs[16-group][token][16 halves]; warp w takes tokens w, w + 4, lane
-    // the 16-groups lane + 32 i
-    for (int t = warp; t < T; t += DF_NW) {
-      float4 a[H / 16 / 32][4];
+    // fp16 x in fragment order, xs[16-group][token][16 halves]: item = (16-group g, token t) with t
+    // fastest, so consecutive threads write consecutive 32-byte fragments (conflict-free); thread tid
+    // keeps token tid % TT throughout (256 is a multiple of TT), and each token's sum of squares is
+    // reduced in a fixed order (lanes, then warps)
+    static_assert(DF_THREADS % TT == 0, "a thread stays on one token");
+    float ss = 0.f;
 #pragma unroll
-      for (int i = 0; i < H / 16 / 32; ++i)
+    for (int k = 0; k < (H / 16 * TT + DF_THREADS - 1) / DF_THREADS; ++k) {
+      const int idx = tid + DF_THREADS * k, g = idx / TT, t = idx % TT;
+      if (g < H / 16 && t < T) {
+        float f[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          a[i][q] = x4(t, 16 * (lane + 32 * i) + 4 * q);
-      float ss = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const float4 a = x4(t, 16 * g + 4 * q);
+          f[4 * q] = a.x; f[4 * q + 1] = a.y; f[4 * q + 2] = a.z; f[4 * q + 3] = a.w;
+        }
 #pragma unroll
-      for (int i = 0; i < H / 16 / 32; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          ss += a[i][q].x * a[i][q].x + a[i][q].y * a[i][q].y + a[i][q].z * a[i][q].z + a[i][q].w * a[i][q].w;
-      ss = warp_sum(ss);
-      if (lane == 0) s_inv[t] = p.residual ? 1.f / sqrtf(ss / (float)H + 1e-6f) : 1.f;
-#pragma unroll
-      for (int i = 0; i < H / 16 / 32; ++i) {
-        const float f[16] = {a[i][0].x, a[i][0].y, a[i][0].z, a[i][0].w, a[i][1].x, a[i][1].y, a[i][1].z, a[i][1].w,
-                             a[i][2].x, a[i][2].y, a[i][2].z, a[i][2].w, a[i][3].x, a[i][3].y, a[i][3].z, a[i][3].w};
+        for (int i = 0; i < 16; ++i) ss = fmaf(f[i], f[i], ss);
         uint32_t hq[8];
         to_fragment_order(f, hq);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sqx) + ((size_t)(lane + 32 * i) * T + t) * 32);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sqx) + ((size_t)g * T + t) * 32);
         dst[0] = make_uint4(hq[0], hq[1], hq[2], hq[3]);
         dst[1] = make_uint4(hq[4], hq[5], hq[6], hq[7]);
       }
+    }
+#pragma unroll
+    for (int o = TT; o < 32; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane < TT) s_ssqt[warp][lane] = ss;
+    __syncthreads();
+    if (tid < T) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < DF_NW; ++w) tot += s_ssqt[w][tid];
+      s_inv[tid] = p.residual ? 1.f / sqrtf(tot / (float)H + 1e-6f) : 1.f;
     }
   }
 #pragma unroll
