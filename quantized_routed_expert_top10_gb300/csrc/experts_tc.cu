@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
                                                          TcTile* __restrict__ half_tiles, int32_t* __restrict__ counts,
                                                          int max_tiles, int max_half_tiles, int* __restrict__ status) {
-  __shared__ int s_pad[EMAX], s_nt[EMAX], s_nh[EMAX], s_scratch[32];
+  __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_nh[EMAX], s_scratch[32];
   const int i = threadIdx.x;
   const int na = max(0, min(*n_active, E));
   int e = 0, q0 = 0, n = 0;
@@ -69,17 +69,30 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
     }
   }
   s_pad[i] = (i < na) ? (n + 7) / 8 * 8 : 0;
-  s_nt[i] = (i < na) ? (n + TCN - 1) / TCN : 0;
+  // gate/up tiles in three classes -- full (TCN tokens), other wide (> TCN_HALF), narrow -- listed in
+  // that order, so each CTA's run of items changes between both-halves and one-half TMEM use once
+  const int rem = n % TCN;
+  s_full[i] = (i < na) ? n / TCN : 0;
+  s_wide[i] = (i < na && rem > TCN_HALF) ? 1 : 0;
+  s_narrow[i] = (i < na && rem > 0 && rem <= TCN_HALF) ? 1 : 0;
   s_nh[i] = (i < na) ? (n + TCN_HALF - 1) / TCN_HALF : 0;
   __syncthreads();
   const int ppad = cta_exclusive_scan(s_pad, s_pad, EMAX, s_scratch);
-  const int ntiles = cta_exclusive_scan(s_nt, s_nt, EMAX, s_scratch);
+  const int nfull = cta_exclusive_scan(s_full, s_full, EMAX, s_scratch);
+  const int nwide = cta_exclusive_scan(s_wide, s_wide, EMAX, s_scratch);
+  const int nnarrow = cta_exclusive_scan(s_narrow, s_narrow, EMAX, s_scratch);
+  const int ntiles = nfull + nwide + nnarrow;
   const int nhalf = cta_exclusive_scan(s_nh, s_nh, EMAX, s_scratch);
   if (i < na) {
     exps[i] = TcExpert{e, q0, n, s_pad[i]};
-    for (int t = 0; t * TCN < n; ++t) {
-      const int idx = s_nt[i] + t;
-      if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t * TCN, min(TCN, n - t * TCN), s_pad[i] + t * TCN};
+    for (int t = 0; t < n / TCN; ++t) {
+      const int idx = s_full[i] + t;
+      if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t * TCN, TCN, s_pad[i] + t * TCN};
+    }
+    if (rem > 0) {
+      const int t0 = n / TCN * TCN;
+      const int idx = rem > TCN_HALF ? nfull + s_wide[i] : nfull + nwide + s_narrow[i];
+      if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t0, rem, s_pad[i] + t0};
     }
     for (int t = 0; t * TCN_HALF < n; ++t) {
       const int idx = s_nh[i] + t;
