@@ -36,6 +36,7 @@ constexpr int DF_GU = N_SLAB;                  // 40 gate/up units (slabs) per e
 constexpr int DF_DN = RT_D;                    // 20 down units per expert
 constexpr int DF_MAXD = DECODE_T_MAX * K;      // at most 80 distinct experts
 constexpr int DF_THREADS = 256;
+constexpr int DF_EARLY = 1;                    // unit copies issued as soon as routing is known
 constexpr int DF_NW = DF_THREADS / 32;         // 8 warps
 constexpr int DF_KG = DF_NW;                   // k-block groups per gate/up unit (one token: a warp each)
 constexpr int DF_KBG = KB_GU / DF_KG;          // 5 k-blocks per group
@@ -666,9 +667,11 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       mbar_expect_tx(&bars[st], DF_UNIT);
       bulk_g2s_stream(ring + (size_t)st * DF_UNIT, src, DF_UNIT, &bars[st], pol);
     };
-    // only the first unit's copy now: issued alone, it is not queued behind every CTA's later stages,
-    // so the first unit starts computing while the rest streams in (issued once it has arrived)
-    if (tid == 0 && c < n_units) issue(c, 0);
+    // the first DF_EARLY units' copies now, the rest once the first has arrived: not queued behind
+    // every CTA's later stages, the first units start computing while the rest streams in
+    if (tid == 0)
+      for (int k = 0; k < DF_EARLY; ++k)
+        if (c + G * k < n_units) issue(c + G * k, k);
 
     int i = 0;
     for (int u = c; u < n_units; u += G, ++i) {
@@ -687,7 +690,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         if (tid == 0) {
           s_pending[st] = -1;
           if (i == 0)
-            for (int k = 1; k < NS; ++k)
+            for (int k = DF_EARLY; k < NS; ++k)
               if (c + G * k < n_units) issue(c + G * k, k);
         }
         if constexpr (MMA) {
@@ -876,7 +879,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         if (tid == 0) {
           s_pending[st] = -1;
           if (i == 0)
-            for (int k = 1; k < NS; ++k)
+            for (int k = DF_EARLY; k < NS; ++k)
               if (c + G * k < n_units) issue(c + G * k, k);
         }
         if constexpr (MMA) {
