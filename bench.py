@@ -173,8 +173,8 @@ NCU_TRAFFIC = {
     # 29,630,976 B read, 6,912 / 0 / 0 B written)
     ("verify_4tok_1layer", "DECODE_LAYER"): (29636011, "2fa0582a05568b3a"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (281075968 + 12581632, "48d549082ee35f29"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (122246656 + 146020608, "48d549082ee35f29"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (288993280 + 9800448, "0b10e817eb9b44a3"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (121902848 + 145785856, "0b10e817eb9b44a3"),
 }
 
 
