@@ -5,12 +5,13 @@
 // (momoyeyu.github.io "ai-infra-strata", "提示词处理": one weight read serves every token routed to an
 // expert), the Q2_0 SwiGLU experts (ai.thesatyajit.com "Strata engine", "The CPU kernels": codes
 // {0,1,2,3} = {-1,0,1,2} x d with the offset removed once per block) and the weighted combine -- runs
-// as one cooperative launch of two 128-thread CTAs per SM:
-//   1. every CTA stages all tokens' activations in shared memory (16-bit integer blocks for one
-//      token, fp16 in MMA fragment order for more) with their rmsnorm, then computes a few router
-//      rows and publishes them;
+// as one cooperative launch of two 256-thread CTAs per SM:
+//   1. every CTA stages all tokens' activations in shared memory (up to four tokens' x arrive by
+//      bulk copy; 16-bit integer blocks for one token, fp16 in MMA fragment order for more) with
+//      their rmsnorm, then computes a few router rows and publishes them;
 //   2. every CTA polls all router dot products and redundantly computes the top-10 of all tokens
-//      and the grouping (identical results everywhere);
+//      and the grouping (identical results everywhere); in a decode stack its idle warps meanwhile
+//      compute its rows of the next layer's router (the lookahead, step 5);
 //   3. the expert bytes are cut into equal 23,040-byte units -- gate/up units (expert, slab of 16
 //      rows, all 40 k-blocks: contiguous in the packed blob) and down units (expert, 128-row tile,
 //      all 10 k-blocks) -- dealt round robin to the CTAs, gate/up units first.  Each CTA streams its
@@ -18,7 +19,10 @@
 //      routing is known.  A gate/up unit publishes h = silu(g) * u of its 16 rows; a down unit polls
 //      the h of its expert's tokens and publishes its 128 output rows per pair;
 //   4. the CTA of down unit (expert slot j, row tile r) then polls the outputs of every pair for
-//      share j of tile r's rows and writes their weighted sum in k order (+ the residual).
+//      share j of tile r's rows and writes their weighted sum in k order (+ the residual);
+//   5. decode stacks: the last CTA takes the next layer's predicted top-10 (its router on this
+//      layer's input) and publishes the distinct experts; at its start the next layer's CTAs
+//      prefetch their share of those experts' units into L2 (a hint; results never depend on it).
 // Every exchanged value travels as one 64-bit word (value bits, call tag) in the workspace's decode
 // exchange area: a reader polls the words it needs until all carry this call's tag, so learning
 // that a value is ready and fetching it take one round trip.  When the output aliases the input,
