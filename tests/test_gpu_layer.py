@@ -120,3 +120,26 @@ def test_repeat_calls_are_deterministic(layer0):
     b = run_layer(blobs, wr, bias, x)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+def test_epoch_wrap_clears_the_exchange_area(layer0):
+    """The decode layer tags its exchange words with a call epoch kept in the workspace header (the
+    int32 at byte 4096 + 4 * 32).  The call that takes the last tag, 0xFFFFFFFF, counts its CTAs out,
+    clears the exchange area and restarts the epoch from 0; results stay the same throughout."""
+    blobs, _ = layer0
+    T = 4
+    x = gen.verify_window(0, T)
+    wr = gen.router_weights(0, 0)
+    ref_out, ref_ids, _ = run_layer(blobs, wr, None, x)
+    ws = workspace(T)
+    epoch = ws[4224:4228]
+    epoch.copy_(torch.tensor(np.array([0xFFFFFFFE], dtype=np.uint32).view(np.uint8), device=DEV))
+    out, ids, _ = run_layer(blobs, wr, None, x, ws=ws)
+    np.testing.assert_array_equal(out, ref_out)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert int(epoch.cpu().numpy().view(np.uint32)[0]) == 0
+    area = ws[12288:12288 + 16 * 8 * 512 * 8]  # router words: cleared with the rest of the area
+    assert int(torch.count_nonzero(area)) == 0
+    out, ids, _ = run_layer(blobs, wr, None, x, ws=ws)
+    np.testing.assert_array_equal(out, ref_out)
+    assert int(epoch.cpu().numpy().view(np.uint32)[0]) == 1
