@@ -83,33 +83,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   return true;
 }
 
-// Orders this thread's earlier (generic-proxy) view of global memory before its later async-proxy
-// accesses (cp.async.bulk reads of data that other threads wrote and released).
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-// Release reduction (fire and forget): every write this thread has observed -- its own, and the CTA's
-// ordered before it by a barrier -- is visible device-wide before the add.
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 // Relaxed max with no reply.
 __device__ __forceinline__ void red_max_u32(unsigned* p, unsigned v) {
   asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Acquire-release add returning the old value.
-__device__ __forceinline__ int atom_acq_rel_add(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void st_relaxed(int* p, int v) {
-  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
 }
 __device__ __forceinline__ int ld_relaxed(const int* p) {
   int v;
@@ -117,41 +93,6 @@ __device__ __forceinline__ int ld_relaxed(const int* p) {
   return v;
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
-// Bounded wait (one thread) until all G CTAs of the grid have arrived on the N counters at base
-// (stride words apart; CTA c adds 1 to counter c % N): counter i reaches the number of c < G with
-// c % N == i.  The counters are polled with relaxed loads, all N in flight at once; the fence after
-// the last reads makes them acquires.  False and ST_TIMEOUT if the grid never completes.
-template <int N>
-__device__ __forceinline__ bool spin_grid_arrivals(const int* base, int stride, int G, int* status) {
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    bool all = true;
-#pragma unroll
-    for (int i = 0; i < N; ++i) all &= ld_relaxed(base + stride * i) >= (G - i + N - 1) / N;
-    if (all) break;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      set_status(status, ST_TIMEOUT);
-      return false;
-    }
-  }
-  fence_acq_rel_gpu();
-  return true;
-}
-
-// Bounded spin until *p >= target (one thread); false and ST_TIMEOUT if it never got there.
-__device__ __forceinline__ bool spin_until_geq(const int* p, int target, int* status) {
-  if (ld_acquire(p) >= target) return true;
-  const unsigned long long t0 = globaltimer();
-  while (ld_acquire(p) < target) {
-    __nanosleep(64);
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      set_status(status, ST_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
