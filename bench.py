@@ -194,6 +194,22 @@ def ncu_traffic(workload, kernel):
     return rec[0]
 
 
+def max_over_ranks(ms, device):
+    """The slowest rank's time, on every rank (all-reduce MAX, then a barrier): replicas run the same
+    work, so the job's time is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_step, steps, world, total_ms):
+    """Tokens per second of the whole job: every rank processes tokens_per_step per step."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 def measure_gb300(args, rank, world, local_rank):
     import torch
 
@@ -307,16 +323,13 @@ def measure_gb300(args, rank, world, local_rank):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = float(np.sum(step_ms))
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        torch.distributed.barrier()
+        total_ms = max_over_ranks(total_ms, dev)
     st = qre.strata_poll_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
     ids_h = ids.cpu().numpy()
     ids_all_h = ids_all.cpu().numpy() if L > 1 else None
-    value = world * T * K / (total_ms / 1e3)
+    value = whole_job_rate(T, K, world, total_ms)
 
     # ---- dominant kernel ----
     roof = kernel_roofline(cfg, kernel_ms, K, ids_all_h if L > 1 else ids_h[None],
