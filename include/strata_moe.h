@@ -165,6 +165,34 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
                                int32_t n_layers, float* x, int32_t T, int32_t* ids, float* weights,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* strata_moe_layer for activations in HOST memory: x_host (host, fp32 [T][2560]) is copied into the
+ * workspace's I/O area, the layer runs there exactly as strata_moe_layer runs it (same kernels, same
+ * results bit for bit), the output is copied to out_host (host, fp32 [T][2560]), and the call returns
+ * after synchronising `stream`, so out_host holds the result on return.  ids / weights (nullable) are
+ * DEVICE arrays as for strata_moe_layer.  x_host and out_host must not overlap (STRATA_E_INVAL).
+ *   - When x_host and out_host are page-locked (cudaHostAlloc / cudaHostRegister) and `stream` is not
+ *     the legacy default stream, the first call captures copy-in, layer and copy-out as one CUDA graph
+ *     and later calls with the same arguments (every pointer and size, flags, stream, current device
+ *     and the fields of *ex) replay it: one graph launch per call.  Up to 16 graphs are kept per
+ *     process, the least recently used dropped.  Otherwise (pageable buffers, the default stream, or
+ *     event timing armed by strata_moe_profile_arm) the steps are enqueued one by one.
+ *   - The host buffers are read and written by the GPU during the call only; their contents may
+ *     change freely between calls, as may every device array's contents.
+ *   - Must not be called while `stream` is being captured: returns STRATA_E_INVAL.
+ *   - Workspace as for strata_moe_layer (strata_moe_workspace_bytes includes the I/O area); calls
+ *     sharing a workspace must not overlap in time. */
+strata_status strata_moe_layer_host(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
+                                    const float* x_host, int32_t T, int32_t flags, float* out_host, int32_t* ids,
+                                    float* weights, void* ws, size_t ws_bytes, void* stream);
+
+/* strata_moe_stack for activations in HOST memory: x_host (host, fp32 [T][2560]) is copied in, the
+ * n_layers residual layers run as in strata_moe_stack, the result is copied back into x_host, and the
+ * call returns after synchronising `stream`.  Graph capture and replay, workspace and errors as for
+ * strata_moe_layer_host (the key includes all n_layers descriptors of ex). */
+strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
+                                    int32_t n_layers, float* x_host, int32_t T, int32_t* ids, float* weights,
+                                    void* ws, size_t ws_bytes, void* stream);
+
 /* Canonical -> packed blob layout, host memory (host pointers), n_blobs consecutive blobs of
  * STRATA_MOE_BLOB_BYTES each.  Pure byte permutation; src and dst must not overlap. */
 strata_status strata_pack_q2_0(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs);

@@ -40,6 +40,7 @@ EXPORTS = (
     "strata_moe_workspace_bytes", "strata_moe_workspace_init", "strata_moe_route", "strata_moe_group",
     "strata_moe_group_noalloc",
     "strata_moe_experts", "strata_moe_combine", "strata_moe_layer", "strata_moe_stack",
+    "strata_moe_layer_host", "strata_moe_stack_host",
     "strata_pack_q2_0", "strata_unpack_q2_0", "strata_pack_q2_0_device", "strata_poll_status",
     "strata_clear_status", "strata_status_str", "strata_moe_launch_count", "strata_moe_profile_arm",
     "strata_moe_profile_recorded",
@@ -84,6 +85,10 @@ def lib():
                                                 _vp, _vp, _vp, _vp, _sz, _vp]),
             "strata_moe_stack": (ctypes.c_int, [ctypes.POINTER(strata_experts_t), _vp, _vp, _i32, _vp, _i32,
                                                 _vp, _vp, _vp, _sz, _vp]),
+            "strata_moe_layer_host": (ctypes.c_int, [ctypes.POINTER(strata_experts_t), _vp, _vp, _vp, _i32, _i32,
+                                                     _vp, _vp, _vp, _vp, _sz, _vp]),
+            "strata_moe_stack_host": (ctypes.c_int, [ctypes.POINTER(strata_experts_t), _vp, _vp, _i32, _vp, _i32,
+                                                     _vp, _vp, _vp, _sz, _vp]),
             "strata_pack_q2_0": (ctypes.c_int, [_vp, _vp, _i64]),
             "strata_unpack_q2_0": (ctypes.c_int, [_vp, _vp, _i64]),
             "strata_pack_q2_0_device": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i64, _vp]),
@@ -186,6 +191,23 @@ def strata_moe_stack(ex_layers, w_router, bias, n_layers, x, T, ids, weights, ws
     arr = (strata_experts_t * max(1, n_layers))(*ex_layers)
     _check("strata_moe_stack", lib().strata_moe_stack(arr, _p(w_router), _p(bias), n_layers, _p(x), T, _p(ids),
                                                       _p(weights), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def strata_moe_layer_host(ex, w_router, bias, x_host, T, flags, out_host, ids, weights, ws, ws_bytes=None,
+                          stream=None):
+    """x_host / out_host: host arrays (CPU tensors or numpy, fp32 [T][2560]); returns with out_host written."""
+    _check("strata_moe_layer_host", lib().strata_moe_layer_host(ctypes.byref(ex), _p(w_router), _p(bias), _p(x_host),
+                                                                T, flags, _p(out_host), _p(ids), _p(weights), _p(ws),
+                                                                _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def strata_moe_stack_host(ex_layers, w_router, bias, n_layers, x_host, T, ids, weights, ws, ws_bytes=None,
+                          stream=None):
+    """x_host: host array (fp32 [T][2560]) updated in place; returns with the result in it."""
+    arr = (strata_experts_t * max(1, n_layers))(*ex_layers)
+    _check("strata_moe_stack_host", lib().strata_moe_stack_host(arr, _p(w_router), _p(bias), n_layers, _p(x_host), T,
+                                                                _p(ids), _p(weights), _p(ws), _nbytes(ws, ws_bytes),
+                                                                _s(stream)))
 
 
 def strata_pack_q2_0(canonical, packed, n_blobs):

@@ -97,6 +97,22 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
 
 }  // namespace
 
+// The checks strata_moe_layer / strata_moe_stack make before enqueueing anything, for the host-buffer
+// calls to make before they touch the device (n_ex descriptors, all with the same expert count).
+strata_status strata::check_layer_args(const strata_experts_t* ex, int n_ex, const uint16_t* w_router,
+                                       const float* bias, int32_t flags, int32_t T, const void* ws,
+                                       size_t ws_bytes) {
+  STRATA_TRY(check_T(T));
+  if (!ex || n_ex < 0 || !w_router) return STRATA_E_INVAL;
+  for (int l = 0; l < n_ex; ++l) {
+    STRATA_TRY(check_experts(&ex[l]));
+    if (ex[l].n_expert != ex[0].n_expert) return STRATA_E_INVAL;
+  }
+  if (flags & ~STRATA_MOE_RESIDUAL_RMSNORM) return STRATA_E_INVAL;
+  if (!aligned(w_router, 16) || (bias && !aligned(bias, 4))) return STRATA_E_ALIGN;
+  return check_ws(ws, ws_bytes, T);
+}
+
 extern "C" {
 
 size_t strata_moe_workspace_bytes(int32_t T) {

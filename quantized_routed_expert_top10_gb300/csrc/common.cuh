@@ -108,6 +108,7 @@ struct WsLayout {
   size_t xg;          // tensor-core expert path: gathered fp16 tokens [KB_GU][rows][128 B]
   size_t hg;          //                                      fp16 h [KB_D][rows][128 B]
   size_t tcmeta;      //                                      expert ranges, tiles, counts
+  size_t io;          // fp32 [2][T][H]: device copies of a host-buffer call's input and output
   size_t total;
   int max_tiles;
   int n_chunks;
@@ -156,6 +157,7 @@ inline WsLayout ws_layout(int T) {
   L.xg = take(tc_xg_bytes(T));
   L.hg = take(tc_hg_bytes(T));
   L.tcmeta = take(tc_meta_bytes(T));
+  L.io = take(sizeof(float) * 2 * (size_t)T * H);
   L.total = T > 0 ? o : WS_HEADER;
   return L;
 }
@@ -267,6 +269,17 @@ enum KernelId : int {
 };
 void kernel_begin(int kid, cudaStream_t s);
 void kernel_end(int kid, cudaStream_t s);
+// Argument checks of a layer / stack call with n_ex expert descriptors (abi.cu).
+strata_status check_layer_args(const strata_experts_t* ex, int n_ex, const uint16_t* w_router, const float* bias,
+                               int32_t flags, int32_t T, const void* ws, size_t ws_bytes);
+// True while the calling thread has event timing armed for some kernel (its launches must then be
+// enqueued one by one, not replayed from a graph).
+bool profiling_armed();
+// Counts n launches made by replaying a graph that holds n of the library's kernels (n may wrap to
+// take back launches that a capture counted).
+void count_launches(unsigned long long n);
+// Launch sites the calling thread has passed so far (captured ones included).
+unsigned long long launches_this_thread();
 #define STRATA_LAUNCH(kid, s, ...) \
   do {                             \
     kernel_begin((kid), (s));      \

@@ -21,6 +21,7 @@ static_assert(KID_DECODE_LAYER == STRATA_KERNEL_DECODE_LAYER && KID_ROUTE_DECODE
               "kernel ids of the ABI and the library differ");
 
 std::atomic<unsigned long long> g_launches{0};
+thread_local unsigned long long t_launches = 0;  // launches made by the calling thread
 
 struct Armed {
   cudaEvent_t const* start = nullptr;
@@ -40,6 +41,7 @@ void kernel_begin(int kid, cudaStream_t s) {
 
 void kernel_end(int kid, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  ++t_launches;
   Armed& a = t_armed[kid];
   if (a.skip > 0) {
     --a.skip;
@@ -48,6 +50,16 @@ void kernel_end(int kid, cudaStream_t s) {
     ++a.used;
   }
 }
+
+bool profiling_armed() {
+  for (int k = 0; k < KID_COUNT; ++k)
+    if (t_armed[k].used < t_armed[k].n) return true;
+  return false;
+}
+
+void count_launches(unsigned long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+unsigned long long launches_this_thread() { return t_launches; }
 
 }  // namespace strata
 

@@ -31,7 +31,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 18
+    assert len(names) == 20
     assert sorted(names) == sorted(qre.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -133,6 +133,27 @@ def test_host_argument_checks(lib):
     assert lib.strata_pack_q2_0_device(A, qre.BLOB_BYTES, A + 16, qre.BLOB_BYTES, 1, None) == -2
     assert lib.strata_moe_workspace_init(A + 8, 4096, None) == -2
     assert lib.strata_moe_workspace_init(A, 100, None) == -6
+    # host-buffer calls: the same checks, made before the device is touched
+    hx = np.zeros((4, 2560), dtype=np.float32)
+    ho = np.zeros((4, 2560), dtype=np.float32)
+    xp, op = hx.ctypes.data, ho.ctypes.data
+    lh, sh = lib.strata_moe_layer_host, lib.strata_moe_stack_host
+    assert lh(ctypes.byref(ex), A, None, xp, -1, 0, op, None, None, A, ws_big, None) == -1
+    assert lh(ctypes.byref(ex), A, None, None, 4, 0, op, None, None, A, ws_big, None) == -1
+    assert lh(ctypes.byref(ex), A, None, xp, 4, 0, None, None, None, A, ws_big, None) == -1
+    assert lh(ctypes.byref(ex), A, None, xp, 4, 0, xp + 4096, None, None, A, ws_big, None) == -1  # overlap
+    assert lh(ctypes.byref(ex), A, None, xp, 4, 2, op, None, None, A, ws_big, None) == -1         # flags
+    assert lh(ctypes.byref(bad_off), A, None, xp, 4, 0, op, None, None, A, ws_big, None) == -1
+    assert lh(ctypes.byref(bad_align), A, None, xp, 4, 0, op, None, None, A, ws_big, None) == -2
+    assert lh(ctypes.byref(ex), A + 2, None, xp, 4, 0, op, None, None, A, ws_big, None) == -2
+    assert lh(ctypes.byref(ex), A, None, xp, 16, 0, op, None, None, A, 4096, None) == -6
+    assert lh(ctypes.byref(ex), A, None, xp, 0, 0, op, None, None, A, ws_big, None) == 0
+    exs = (qre.strata_experts_t * 2)(ex, bad_e)
+    assert sh(exs, A, None, 2, xp, 4, None, None, A, ws_big, None) == -1
+    assert sh(exs, A, None, -1, xp, 4, None, None, A, ws_big, None) == -1
+    assert sh(exs, A, None, 1, None, 4, None, None, A, ws_big, None) == -1
+    assert sh(exs, A, None, 1, xp, 4, None, None, A, 1024, None) == -6
+    assert sh(exs, A, None, 0, xp, 4, None, None, A, ws_big, None) == 0
     # empty calls are valid and enqueue nothing
     assert lib.strata_moe_route(A, 0, A, None, 512, A, A, None, A, ws_big, None) == 0
     assert lib.strata_moe_layer(ctypes.byref(ex), A, None, A, 0, 0, A, None, None, A, ws_big, None) == 0

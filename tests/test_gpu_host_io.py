@@ -1,0 +1,144 @@
+"""GPU tests of the host-buffer calls (strata_moe_layer_host / strata_moe_stack_host): the same results,
+bit for bit, as the device-buffer calls on the same inputs, through the graph path (page-locked buffers
+on a side stream, first call captured, later calls replayed) and the direct path (pageable buffers or
+the default stream); and the oracle on the host path's output."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import quantized_routed_expert_top10_gb300 as qre
+from gpu_common import DEV, BlobCache, check_close, check_routing, device_packed_layer, to_dev, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def layers():
+    """Seed-0 experts of layers 0-2 packed on the device, and the host blob cache for the oracle."""
+    blobs = [device_packed_layer(0, l) for l in range(3)]
+    yield blobs, BlobCache(0)
+    del blobs
+    torch.cuda.empty_cache()
+
+
+def device_call(ex, wr, bias, x, flags, ws, stream):
+    out = torch.empty(x.shape, dtype=torch.float32, device=DEV)
+    with torch.cuda.stream(stream):
+        qre.strata_moe_layer(ex, wr, bias, to_dev(x), x.shape[0], flags, out, None, None, ws, stream=stream)
+    stream.synchronize()
+    return out.cpu().numpy()
+
+
+def host_buffers(T, pinned):
+    if pinned:
+        return (torch.empty(T, qre.H, dtype=torch.float32).pin_memory(),
+                torch.empty(T, qre.H, dtype=torch.float32).pin_memory())
+    return np.empty((T, qre.H), dtype=np.float32), np.empty((T, qre.H), dtype=np.float32)
+
+
+def fill(buf, x):
+    if isinstance(buf, torch.Tensor):
+        buf.copy_(torch.from_numpy(x))
+    else:
+        buf[...] = x
+
+
+def as_np(buf):
+    return buf.numpy().copy() if isinstance(buf, torch.Tensor) else buf.copy()
+
+
+@pytest.mark.parametrize("T,flags,pinned", [(1, 0, True), (4, 0, True), (4, 1, False), (8, 1, True),
+                                            (64, 0, True), (300, 1, False)])
+def test_layer_host_matches_device_call(layers, T, flags, pinned):
+    blobs, _ = layers
+    ex = qre.experts(blobs[0])
+    wr = to_dev(gen.router_weights(0, 0))
+    bias = to_dev(gen.zipf_bias(0, 0))
+    ws = workspace(T)
+    s = torch.cuda.Stream()
+    hx, ho = host_buffers(T, pinned)
+    before = qre.strata_moe_launch_count()
+    for it in range(3):  # the first call captures, the next two replay (pinned); new x every call
+        x = (gen.activations_fast(40 + it, T) * (2.0 if flags else 1.0)).astype(np.float32)
+        fill(hx, x)
+        qre.strata_moe_layer_host(ex, wr, bias, hx, T, flags, ho, None, None, ws, stream=s)
+        got = as_np(ho)
+        want = device_call(ex, wr, bias, x, flags, ws, s)
+        np.testing.assert_array_equal(got, want)
+    assert qre.strata_poll_status(ws) == 0
+    # three host calls and three device calls, each the same kernels
+    per_call = (qre.strata_moe_launch_count() - before) // 6
+    assert per_call >= 1
+    assert qre.strata_moe_launch_count() - before == 6 * per_call
+
+
+def test_layer_host_on_default_stream(layers):
+    blobs, _ = layers
+    ex = qre.experts(blobs[0])
+    wr = to_dev(gen.router_weights(0, 0))
+    T = 4
+    ws = workspace(T)
+    hx, ho = host_buffers(T, True)
+    x = gen.verify_window(0, T)
+    fill(hx, x)
+    qre.strata_moe_layer_host(ex, wr, None, hx, T, 0, ho, None, None, ws, stream=0)
+    np.testing.assert_array_equal(as_np(ho), device_call(ex, wr, None, x, 0, ws, torch.cuda.Stream()))
+
+
+def test_layer_host_parity_with_oracle(layers):
+    """The verify window through the host path against the oracle (routing up to ties, outputs to 2e-3)."""
+    blobs, cache = layers
+    T = 4
+    x = gen.verify_window(0, T)
+    wr_h = gen.router_weights(0, 0)
+    ws = workspace(T)
+    ids = torch.empty(T, qre.K, dtype=torch.int32, device=DEV)
+    hx, ho = host_buffers(T, True)
+    fill(hx, x)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        qre.strata_moe_layer_host(qre.experts(blobs[0]), to_dev(wr_h), None, hx, T, 0, ho, ids, None, ws, stream=s)
+    ids_h = ids.cpu().numpy()
+    ref_r = oracle.route(x, wr_h, None, residual=False)
+    check_routing(ids_h, ref_r["ids"], ref_r["logits"])
+    ref = oracle.moe_layer(x, wr_h, None, cache.layer_list(0, ids_h, 512), ids_in=ids_h)
+    check_close(as_np(ho), ref["out"], "host-buffer layer output")
+
+
+@pytest.mark.parametrize("T,pinned", [(1, True), (4, False), (20, True)])
+def test_stack_host_matches_device_call(layers, T, pinned):
+    blobs, _ = layers
+    L = 3
+    exs = [qre.experts(b) for b in blobs]
+    wr = to_dev(np.concatenate([gen.router_weights(0, l) for l in range(L)]))
+    bias = to_dev(np.concatenate([gen.zipf_bias(0, l) for l in range(L)]))
+    ws = workspace(T)
+    s = torch.cuda.Stream()
+    hx, _ = host_buffers(T, pinned)
+    for it in range(2):
+        x = gen.activations_fast(60 + it, T)
+        fill(hx, x)
+        qre.strata_moe_stack_host(exs, wr, bias, L, hx, T, None, None, ws, stream=s)
+        xd = to_dev(x)
+        with torch.cuda.stream(s):
+            qre.strata_moe_stack(exs, wr, bias, L, xd, T, None, None, ws, stream=s)
+        s.synchronize()
+        np.testing.assert_array_equal(as_np(hx), xd.cpu().numpy())
+    assert qre.strata_poll_status(ws) == 0
+
+
+def test_host_call_refused_inside_capture(layers):
+    blobs, _ = layers
+    T = 4
+    ws = workspace(T)
+    hx, ho = host_buffers(T, True)
+    ex = qre.experts(blobs[0])
+    wr = to_dev(gen.router_weights(0, 0))
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(qre.StrataError):
+        with torch.cuda.graph(g, stream=s):
+            qre.strata_moe_layer_host(ex, wr, None, hx, T, 0, ho, None, None, ws, stream=s)
