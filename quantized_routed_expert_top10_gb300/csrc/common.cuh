@@ -265,7 +265,8 @@ namespace strata {
 // it and record the caller's armed timing events around it.  Ids equal the ABI's STRATA_KERNEL_*.
 enum KernelId : int {
   KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_ROUTER_PREP, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
-  KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_COUNT
+  KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_HOST_COPY,
+  KID_COUNT
 };
 void kernel_begin(int kid, cudaStream_t s);
 void kernel_end(int kid, cudaStream_t s);

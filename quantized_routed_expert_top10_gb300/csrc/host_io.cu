@@ -4,7 +4,10 @@
 //
 // With page-locked host buffers and a non-default stream the three steps are captured once as a CUDA
 // graph and replayed by later calls with the same arguments, so a call costs one graph launch and one
-// synchronisation on the host instead of a copy, a launch per kernel and a copy.
+// synchronisation on the host instead of a copy, a launch per kernel and a copy.  Small activations
+// (decode and verify windows) move by a short kernel through the host buffers' device mappings: a
+// copy-engine transfer of a few KB costs several microseconds of latency on the call's path.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -15,13 +18,56 @@ using namespace strata;
 
 namespace {
 
-inline bool page_locked(const void* p) {
+#define STRATA_TRY_HOST(expr)              \
+  do {                                     \
+    const strata_status _st = (expr);      \
+    if (_st != STRATA_OK) return _st;      \
+  } while (0)
+
+// A host-buffer call synchronises its stream, so it cannot be part of a capture.
+strata_status not_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return STRATA_E_CUDA;
+  return cs == cudaStreamCaptureStatusNone ? STRATA_OK : STRATA_E_INVAL;
+}
+
+// The device address of page-locked host memory at p, or nullptr when p is pageable (or unmapped).
+inline void* mapped(const void* p) {
   cudaPointerAttributes a{};
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();  // an unregistered pointer may leave an error behind on older drivers
-    return false;
+    return nullptr;
   }
-  return a.type == cudaMemoryTypeHost;
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Activations up to this size move between host and device by host_copy_kernel (latency-bound: one
+// short kernel on the graph's path instead of a copy-engine transfer); larger ones by the copy engines.
+constexpr size_t kKernelCopyMax = 4u << 20;
+
+// dst[i] = src[i], 16-byte words; one side is page-locked host memory reached through its device
+// mapping, the other the workspace's I/O area.
+__global__ void __launch_bounds__(256) host_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                        size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+// Copy `bytes` from src to dst on s: the kernel when the mapped side `map` (the device address of the
+// host buffer) is usable, else a copy-engine transfer of the host pointer `host`.
+strata_status copy_host(void* dst, const void* src, size_t bytes, const void* map, bool to_device, const void* host,
+                        cudaStream_t s) {
+  const bool aligned16 = ((uintptr_t)map & 15) == 0 && (bytes & 15) == 0;
+  if (map && aligned16 && bytes <= kKernelCopyMax) {
+    const size_t n = bytes / 16;
+    const int blocks = (int)std::min<size_t>((n + 255) / 256, 8 * 152);
+    STRATA_LAUNCH(KID_HOST_COPY, s,
+                  host_copy_kernel<<<blocks, 256, 0, s>>>((const uint4*)src, (uint4*)dst, n));
+    return cudaGetLastError() == cudaSuccess ? STRATA_OK : STRATA_E_CUDA;
+  }
+  const cudaError_t e = to_device ? cudaMemcpyAsync(dst, host, bytes, cudaMemcpyHostToDevice, s)
+                                  : cudaMemcpyAsync((void*)host, src, bytes, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? STRATA_OK : STRATA_E_CUDA;
 }
 
 // Everything a captured graph depends on: the pointers it copies from and to, the sizes, the
@@ -34,6 +80,8 @@ struct HostKey {
   const void* bias = nullptr;
   const void* x_host = nullptr;
   const void* out_host = nullptr;
+  const void* x_map = nullptr;    // their device mappings (a re-registered buffer may map elsewhere)
+  const void* out_map = nullptr;
   const void* ids = nullptr;
   const void* weights = nullptr;
   const void* ws = nullptr;
@@ -43,7 +91,8 @@ struct HostKey {
 
   bool operator==(const HostKey& o) const {
     if (kind != o.kind || device != o.device || T != o.T || flags != o.flags || n_layers != o.n_layers ||
-        w_router != o.w_router || bias != o.bias || x_host != o.x_host || out_host != o.out_host || ids != o.ids ||
+        w_router != o.w_router || bias != o.bias || x_host != o.x_host || out_host != o.out_host ||
+        x_map != o.x_map || out_map != o.out_map || ids != o.ids ||
         weights != o.weights || ws != o.ws || ws_bytes != o.ws_bytes || stream != o.stream || ex.size() != o.ex.size())
       return false;
     for (size_t i = 0; i < ex.size(); ++i)
@@ -114,12 +163,8 @@ cudaGraphExec_t graph_for(const HostKey& key, cudaStream_t s, Enqueue enqueue, s
 // Runs `enqueue` (copy in, compute, copy out on s) from a cached graph when it can, else directly,
 // then synchronises s.
 template <typename Enqueue>
-strata_status run_host_call(const HostKey& key, cudaStream_t s, const void* a, const void* b, Enqueue enqueue) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return STRATA_E_CUDA;
-  if (cs != cudaStreamCaptureStatusNone) return STRATA_E_INVAL;  // a synchronising call cannot be captured
-  const bool graphable = s != nullptr && s != cudaStreamLegacy && page_locked(a) && page_locked(b) &&
-                         !profiling_armed();
+strata_status run_host_call(const HostKey& key, cudaStream_t s, bool page_locked, Enqueue enqueue) {
+  const bool graphable = s != nullptr && s != cudaStreamLegacy && page_locked && !profiling_armed();
   if (graphable) {
     std::lock_guard<std::mutex> lock(g_mu);
     strata_status st = STRATA_OK;
@@ -156,6 +201,9 @@ strata_status strata_moe_layer_host(const strata_experts_t* ex, const uint16_t* 
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STRATA_E_CUDA;
+  STRATA_TRY_HOST(not_capturing(s));
+  const void* xm = mapped(x_host);
+  const void* om = mapped(out_host);
   HostKey key;
   key.kind = 0;
   key.device = dev;
@@ -165,20 +213,24 @@ strata_status strata_moe_layer_host(const strata_experts_t* ex, const uint16_t* 
   key.bias = bias;
   key.x_host = x_host;
   key.out_host = out_host;
+  key.x_map = xm;
+  key.out_map = om;
   key.ids = ids;
   key.weights = weights;
   key.ws = ws;
   key.ws_bytes = ws_bytes;
   key.stream = stream;
   key.ex.assign(ex, ex + 1);
+  // small outputs are written by the layer itself straight into out_host's mapping (both paths only
+  // store to out, once per element), which saves the copy-out step
+  const bool direct_out = om && ((uintptr_t)om & 15) == 0 && bytes <= kKernelCopyMax;
   auto enqueue = [&]() -> strata_status {
-    if (cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return STRATA_E_CUDA;
-    const strata_status st = strata_moe_layer(ex, w_router, bias, dx, T, flags, dout, ids, weights, ws, ws_bytes, stream);
-    if (st != STRATA_OK) return st;
-    return cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? STRATA_OK
-                                                                                             : STRATA_E_CUDA;
+    STRATA_TRY_HOST(copy_host(dx, xm, bytes, xm, true, x_host, s));
+    STRATA_TRY_HOST(strata_moe_layer(ex, w_router, bias, dx, T, flags, direct_out ? (float*)om : dout, ids, weights,
+                                     ws, ws_bytes, stream));
+    return direct_out ? STRATA_OK : copy_host((void*)om, dout, bytes, om, false, out_host, s);
   };
-  return run_host_call(key, s, x_host, out_host, enqueue);
+  return run_host_call(key, s, xm && om, enqueue);
 }
 
 strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
@@ -194,6 +246,8 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STRATA_E_CUDA;
+  STRATA_TRY_HOST(not_capturing(s));
+  const void* xm = mapped(x_host);
   HostKey key;
   key.kind = 1;
   key.device = dev;
@@ -203,6 +257,8 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
   key.bias = bias;
   key.x_host = x_host;
   key.out_host = x_host;
+  key.x_map = xm;
+  key.out_map = xm;
   key.ids = ids;
   key.weights = weights;
   key.ws = ws;
@@ -210,13 +266,11 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
   key.stream = stream;
   key.ex.assign(ex, ex + n_layers);
   auto enqueue = [&]() -> strata_status {
-    if (cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return STRATA_E_CUDA;
-    const strata_status st = strata_moe_stack(ex, w_router, bias, n_layers, dx, T, ids, weights, ws, ws_bytes, stream);
-    if (st != STRATA_OK) return st;
-    return cudaMemcpyAsync(x_host, dx, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? STRATA_OK
-                                                                                         : STRATA_E_CUDA;
+    STRATA_TRY_HOST(copy_host(dx, xm, bytes, xm, true, x_host, s));
+    STRATA_TRY_HOST(strata_moe_stack(ex, w_router, bias, n_layers, dx, T, ids, weights, ws, ws_bytes, stream));
+    return copy_host((void*)xm, dx, bytes, xm, false, x_host, s);
   };
-  return run_host_call(key, s, x_host, x_host, enqueue);
+  return run_host_call(key, s, xm != nullptr, enqueue);
 }
 
 }  // extern "C"
