@@ -73,7 +73,7 @@ typedef enum strata_status {
   STRATA_OK = 0,
   STRATA_E_INVAL = -1,       /* null pointer, size out of range, bad enum value */
   STRATA_E_ALIGN = -2,       /* a pointer or stride breaks the alignment rule of its argument */
-  STRATA_E_UNSUPPORTED = -3, /* a shape this build does not implement */
+  STRATA_E_UNSUPPORTED = -3, /* a shape the library does not implement */
   STRATA_E_CUDA = -4,        /* a CUDA runtime call (launch, copy) failed */
   STRATA_E_TIMEOUT = -5,     /* a bounded device-side wait expired (device status) */
   STRATA_E_WORKSPACE = -6,   /* ws_bytes smaller than strata_moe_workspace_bytes(T) */
