@@ -169,12 +169,12 @@ KERNEL_SOURCES = {
 # workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
 # sources at capture time: once a source changes the figure no longer describes the kernel (null).
 NCU_TRAFFIC = {
-    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,599,744 / 29,604,864 /
-    # 29,608,704 B read, 12,032 / 0 / 2,048 B written)
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29609131, "b9b2ef5b98d875c0"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,619,712 / 29,608,960 /
+    # 29,635,584 B read, 7,424 / 0 / 0 B written)
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29623893, "91c80c06f5525bb8"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (288985344 + 9696512, "fdbe05773e591a24"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (121753600 + 145805824, "fdbe05773e591a24"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (288917504 + 9676544, "bc56cfd6b207b2bb"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (121634304 + 145833216, "bc56cfd6b207b2bb"),
 }
 
 

@@ -77,6 +77,26 @@ def test_layer_host_matches_device_call(layers, T, flags, pinned):
     assert qre.strata_poll_status(ws) == 0
 
 
+def test_layer_host_at_the_largest_chunk(layers):
+    """T = 8,192 (the ABI's maximum): page-locked buffers of 84 MB each way through the mapped path."""
+    blobs, _ = layers
+    T = 8192
+    ex = qre.experts(blobs[1])
+    wr = to_dev(gen.router_weights(0, 1))
+    bias = to_dev(gen.zipf_bias(0, 1))
+    ws = workspace(T)
+    s = torch.cuda.Stream()
+    hx, ho = host_buffers(T, True)
+    x = gen.activations_fast(90, T)
+    fill(hx, x)
+    for _ in range(2):
+        qre.strata_moe_layer_host(ex, wr, bias, hx, T, 1, ho, None, None, ws, stream=s)
+    np.testing.assert_array_equal(as_np(ho), device_call(ex, wr, bias, x, 1, ws, s))
+    assert qre.strata_poll_status(ws) == 0
+    del ws
+    torch.cuda.empty_cache()
+
+
 def test_prepared_calls_repeat_the_call(layers):
     blobs, _ = layers
     T = 4
