@@ -169,12 +169,12 @@ KERNEL_SOURCES = {
 # workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
 # sources at capture time: once a source changes the figure no longer describes the kernel (null).
 NCU_TRAFFIC = {
-    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,619,712 / 29,608,960 /
-    # 29,635,584 B read, 7,424 / 0 / 0 B written)
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29623893, "91c80c06f5525bb8"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,610,496 / 29,605,376 /
+    # 29,609,984 B read, 8,192 / 0 / 512 B written)
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29611520, "8da5f57911afa7cb"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (288917504 + 9676544, "bc56cfd6b207b2bb"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (121634304 + 145833216, "bc56cfd6b207b2bb"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (288850432 + 9672704, "674fec59ed54a97f"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (122005504 + 145927424, "674fec59ed54a97f"),
 }
 
 

@@ -198,6 +198,16 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
                                     int32_t n_layers, float* x_host, int32_t T, int32_t* ids, float* weights,
                                     void* ws, size_t ws_bytes, void* stream);
 
+/* Failure-detection self-test (no counterpart on the pages).  Every wait in the library's kernels is
+ * bounded: past a limit (2 s) it records STRATA_E_TIMEOUT in the workspace's status word and the
+ * kernel returns instead of hanging.  This call runs the decode layer's two kinds of wait -- a poll of
+ * an exchange word for a tag, and an mbarrier phase -- in one CTA on conditions that never hold, with
+ * the limit limit_ns (in [1000, 2e9]), so both expire: afterwards strata_poll_status returns
+ * STRATA_E_TIMEOUT, strata_clear_status clears it, and the context stays usable.  Uses the first 8
+ * bytes of the workspace's logits area as the never-written word (set to 0 first); ws as for T = 1.
+ * Enqueued on stream; takes about 2 x limit_ns on the device. */
+strata_status strata_moe_wait_selftest(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream);
+
 /* Canonical -> packed blob layout, host memory (host pointers), n_blobs consecutive blobs of
  * STRATA_MOE_BLOB_BYTES each.  Pure byte permutation; src and dst must not overlap. */
 strata_status strata_pack_q2_0(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs);
@@ -238,7 +248,8 @@ const char* strata_status_str(strata_status s);
 #define STRATA_KERNEL_COMBINE 12
 #define STRATA_KERNEL_PACK 13
 #define STRATA_KERNEL_HOST_COPY 14     /* copy between page-locked host memory and the workspace (host-buffer calls) */
-#define STRATA_KERNEL_COUNT 15
+#define STRATA_KERNEL_WAIT_SELFTEST 15 /* strata_moe_wait_selftest */
+#define STRATA_KERNEL_COUNT 16
 
 /* Number of kernels this process has launched through the library so far (all threads). */
 uint64_t strata_moe_launch_count(void);

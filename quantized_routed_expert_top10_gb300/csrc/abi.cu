@@ -235,6 +235,18 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
   return STRATA_OK;
 }
 
+strata_status strata_moe_wait_selftest(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream) {
+  STRATA_TRY(check_ws(ws, ws_bytes, 1));
+  if (limit_ns < 1000 || limit_ns > 2000000000ull) return STRATA_E_INVAL;
+  const WsLayout L = ws_layout(1);
+  uint64_t* word = (uint64_t*)((char*)ws + L.logits);
+  STRATA_CUDA(cudaMemsetAsync(word, 0, sizeof(uint64_t), (cudaStream_t)stream));
+  // tag 0xA5A5A5A5: the word holds tag 0 and nothing writes it during the call
+  STRATA_CUDA(launch_wait_selftest(word, 0xA5A5A5A5u, (unsigned long long)limit_ns, (int*)((char*)ws + L.status),
+                                   (cudaStream_t)stream));
+  return STRATA_OK;
+}
+
 strata_status strata_pack_q2_0(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs) {
   if (!canonical || !packed || n_blobs < 0) return STRATA_E_INVAL;
   const uint8_t* c_end = canonical + n_blobs * BLOB;

@@ -266,7 +266,7 @@ namespace strata {
 enum KernelId : int {
   KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_ROUTER_PREP, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
   KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_HOST_COPY,
-  KID_COUNT
+  KID_WAIT_SELFTEST, KID_COUNT
 };
 void kernel_begin(int kid, cudaStream_t s);
 void kernel_end(int kid, cudaStream_t s);
@@ -288,6 +288,9 @@ unsigned long long launches_this_thread();
     kernel_end((kid), (s));        \
   } while (0)
 
+// The decode layer's bounded waits on conditions that never hold, with limit_ns (decode_fused.cu).
+cudaError_t launch_wait_selftest(const uint64_t* word, uint32_t tag, unsigned long long limit_ns, int* status,
+                                 cudaStream_t s);
 cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const uint16_t* w_router,
                                 const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
                                 float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);

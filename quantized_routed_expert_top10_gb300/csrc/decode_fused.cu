@@ -97,10 +97,11 @@ __device__ __forceinline__ float tagged_value(uint64_t w) { return __uint_as_flo
 // the ones still missing, all in flight at once, until every entry of the CTA carries `tag`.  The
 // verdicts are CTA-wide (barrier reductions), so every thread leaves on the same pass.  Between
 // passes the CTA sleeps, 64 ns doubling up to 512 ns: a spinning CTA would take issue slots from the
-// other CTA on its SM.  False (and ST_TIMEOUT) once the wait limit has passed.
+// other CTA on its SM.  False (and ST_TIMEOUT) once limit_ns has passed (the layer uses the library's
+// limit; the wait self-test passes a short one).
 template <int KMAX, typename Map>
 __device__ __forceinline__ bool poll_tagged(const uint64_t* src, Map map, int count, uint32_t tag, float* dst,
-                                            int* status) {
+                                            int* status, unsigned long long limit_ns = kWaitLimitNs) {
   static_assert(KMAX <= 64, "one mask bit per entry");
   const int tid = threadIdx.x;
   uint64_t missing = 0;
@@ -121,7 +122,7 @@ __device__ __forceinline__ bool poll_tagged(const uint64_t* src, Map map, int co
         missing &= ~(1ull << k);
       }
     if (__syncthreads_and(missing == 0 ? 1 : 0)) return true;
-    if (__syncthreads_or(globaltimer() - t0 > kWaitLimitNs ? 1 : 0)) {
+    if (__syncthreads_or(globaltimer() - t0 > limit_ns ? 1 : 0)) {
       if (tid == 0) set_status(status, ST_TIMEOUT);
       return false;
     }
@@ -1111,7 +1112,29 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
   return err;
 }
 
+// Wait self-test: one CTA of the layer's shape runs the layer's two bounded waits on conditions that
+// never hold -- a poll of an exchange word for a tag nothing writes, and an mbarrier phase nothing
+// completes -- with a short limit; each expires, records ST_TIMEOUT in the status word and returns.
+__global__ void __launch_bounds__(DF_THREADS) wait_selftest_kernel(const uint64_t* word, uint32_t tag,
+                                                                   unsigned long long limit_ns, int* status) {
+  __shared__ float s_dst[DF_THREADS];
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  poll_tagged<1>(word, [](int) { return 0; }, 1, tag, s_dst, status, limit_ns);
+  if (threadIdx.x == 0) mbar_wait(&bar, 0u, status, limit_ns);  // no arrival ever comes
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(const uint64_t* word, uint32_t tag, unsigned long long limit_ns, int* status,
+                                 cudaStream_t s) {
+  STRATA_LAUNCH(KID_WAIT_SELFTEST, s, wait_selftest_kernel<<<1, DF_THREADS, 0, s>>>(word, tag, limit_ns, status));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_router, const float* bias,
                                 const float* x, int T, int residual, int alias, float* out, int32_t* ids, float* weights,

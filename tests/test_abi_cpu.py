@@ -31,7 +31,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 20
+    assert len(names) == 21
     assert sorted(names) == sorted(qre.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -154,6 +154,13 @@ def test_host_argument_checks(lib):
     assert sh(exs, A, None, 1, None, 4, None, None, A, ws_big, None) == -1
     assert sh(exs, A, None, 1, xp, 4, None, None, A, 1024, None) == -6
     assert sh(exs, A, None, 0, xp, 4, None, None, A, ws_big, None) == 0
+    # the wait self-test: workspace and limit checked before the device is touched
+    ws1 = qre.strata_moe_workspace_bytes(1)
+    assert lib.strata_moe_wait_selftest(None, ws1, 10000, None) == -1
+    assert lib.strata_moe_wait_selftest(A + 16, ws1, 10000, None) == -2
+    assert lib.strata_moe_wait_selftest(A, 1024, 10000, None) == -6
+    assert lib.strata_moe_wait_selftest(A, ws1, 999, None) == -1
+    assert lib.strata_moe_wait_selftest(A, ws1, 2000000001, None) == -1
     # empty calls are valid and enqueue nothing
     assert lib.strata_moe_route(A, 0, A, None, 512, A, A, None, A, ws_big, None) == 0
     assert lib.strata_moe_layer(ctypes.byref(ex), A, None, A, 0, 0, A, None, None, A, ws_big, None) == 0
