@@ -169,12 +169,12 @@ KERNEL_SOURCES = {
 # workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
 # sources at capture time: once a source changes the figure no longer describes the kernel (null).
 NCU_TRAFFIC = {
-    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,610,496 / 29,605,376 /
-    # 29,609,984 B read, 8,192 / 0 / 512 B written)
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29611520, "8da5f57911afa7cb"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,614,848 / 29,607,680 /
+    # 29,626,880 B read, 8,448 / 0 / 0 B written)
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29619285, "5ad4c6c9dc1077e8"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (288850432 + 9672704, "674fec59ed54a97f"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (122005504 + 145927424, "674fec59ed54a97f"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (288977408 + 9764096, "08f79a4ce57ba945"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (121604096 + 145818880, "08f79a4ce57ba945"),
 }
 
 

@@ -208,6 +208,18 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
  * Enqueued on stream; takes about 2 x limit_ns on the device. */
 strata_status strata_moe_wait_selftest(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream);
 
+/* Blob checksums, for verifying an upload or a device pack against the bytes it came from.
+ * zwxr.cn news/242664, section "与静态 offload 方案的本质差异": every expert slot is read back and
+ * checked after it is filled, and the engine refuses to run when a check fails.  The checksum is the
+ * common CRC-32 (IEEE 802.3 polynomial, reflected, preset and final inversion all ones: the value
+ * zlib's crc32 gives) of each blob's STRATA_MOE_BLOB_BYTES bytes; blob j starts at blobs + j*stride,
+ * stride >= STRATA_MOE_BLOB_BYTES.  Host: blobs and crc [n_blobs] are host memory.  Device: blobs in
+ * device memory (256-byte aligned, stride a multiple of 256), crc a device array [n_blobs] written
+ * on stream, one CTA per blob.  n_blobs == 0 is an empty call. */
+strata_status strata_blob_crc32(const uint8_t* blobs, int64_t stride, int64_t n_blobs, uint32_t* crc);
+strata_status strata_blob_crc32_device(const void* blobs, int64_t stride, int64_t n_blobs, uint32_t* crc,
+                                       void* stream);
+
 /* Canonical -> packed blob layout, host memory (host pointers), n_blobs consecutive blobs of
  * STRATA_MOE_BLOB_BYTES each.  Pure byte permutation; src and dst must not overlap. */
 strata_status strata_pack_q2_0(const uint8_t* canonical, uint8_t* packed, int64_t n_blobs);
@@ -249,7 +261,8 @@ const char* strata_status_str(strata_status s);
 #define STRATA_KERNEL_PACK 13
 #define STRATA_KERNEL_HOST_COPY 14     /* copy between page-locked host memory and the workspace (host-buffer calls) */
 #define STRATA_KERNEL_WAIT_SELFTEST 15 /* strata_moe_wait_selftest */
-#define STRATA_KERNEL_COUNT 16
+#define STRATA_KERNEL_BLOB_CRC32 16    /* strata_blob_crc32_device */
+#define STRATA_KERNEL_COUNT 17
 
 /* Number of kernels this process has launched through the library so far (all threads). */
 uint64_t strata_moe_launch_count(void);

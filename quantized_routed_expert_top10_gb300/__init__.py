@@ -40,7 +40,8 @@ EXPORTS = (
     "strata_moe_workspace_bytes", "strata_moe_workspace_init", "strata_moe_route", "strata_moe_group",
     "strata_moe_group_noalloc",
     "strata_moe_experts", "strata_moe_combine", "strata_moe_layer", "strata_moe_stack",
-    "strata_moe_layer_host", "strata_moe_stack_host", "strata_moe_wait_selftest",
+    "strata_moe_layer_host", "strata_moe_stack_host", "strata_moe_wait_selftest", "strata_blob_crc32",
+    "strata_blob_crc32_device",
     "strata_pack_q2_0", "strata_unpack_q2_0", "strata_pack_q2_0_device", "strata_poll_status",
     "strata_clear_status", "strata_status_str", "strata_moe_launch_count", "strata_moe_profile_arm",
     "strata_moe_profile_recorded",
@@ -90,6 +91,8 @@ def lib():
             "strata_moe_stack_host": (ctypes.c_int, [ctypes.POINTER(strata_experts_t), _vp, _vp, _i32, _vp, _i32,
                                                      _vp, _vp, _vp, _sz, _vp]),
             "strata_moe_wait_selftest": (ctypes.c_int, [_vp, _sz, ctypes.c_uint64, _vp]),
+            "strata_blob_crc32": (ctypes.c_int, [_vp, _i64, _i64, _vp]),
+            "strata_blob_crc32_device": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
             "strata_pack_q2_0": (ctypes.c_int, [_vp, _vp, _i64]),
             "strata_unpack_q2_0": (ctypes.c_int, [_vp, _vp, _i64]),
             "strata_pack_q2_0_device": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i64, _vp]),
@@ -248,6 +251,17 @@ def strata_moe_wait_selftest(ws, limit_ns, ws_bytes=None, stream=None):
                                                                       _s(stream)))
 
 
+def strata_blob_crc32(blobs, n_blobs, crc, stride=BLOB_BYTES):
+    """CRC-32 (zlib's) of each packed blob in host memory into crc (host uint32 [n_blobs])."""
+    _check("strata_blob_crc32", lib().strata_blob_crc32(_p(blobs), stride, n_blobs, _p(crc)))
+
+
+def strata_blob_crc32_device(blobs, n_blobs, crc, stride=BLOB_BYTES, stream=None):
+    """The same checksums of blobs in device memory into crc (device uint32 [n_blobs]), enqueued."""
+    _check("strata_blob_crc32_device", lib().strata_blob_crc32_device(_p(blobs), stride, n_blobs, _p(crc),
+                                                                      _s(stream)))
+
+
 def strata_pack_q2_0(canonical, packed, n_blobs):
     _check("strata_pack_q2_0", lib().strata_pack_q2_0(_p(canonical), _p(packed), n_blobs))
 
@@ -277,7 +291,7 @@ def strata_status_str(status: int) -> str:
 # kernel ids of strata_moe_profile_arm (STRATA_KERNEL_* of the header)
 KERNELS = ("DECODE_LAYER", "ROUTE_DECODE", "ROUTER_PREP", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN",
            "GROUP_SCATTER", "TC_PREPARE", "TC_GATHER",
-           "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK", "HOST_COPY", "WAIT_SELFTEST")
+           "TC_GATEUP", "TC_DOWN", "COMBINE", "PACK", "HOST_COPY", "WAIT_SELFTEST", "BLOB_CRC32")
 KERNEL_ID = {name: i for i, name in enumerate(KERNELS)}
 
 

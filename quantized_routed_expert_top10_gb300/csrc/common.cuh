@@ -266,7 +266,7 @@ namespace strata {
 enum KernelId : int {
   KID_DECODE_LAYER = 0, KID_ROUTE_DECODE, KID_ROUTER_PREP, KID_ROUTER_TC, KID_TOP_K, KID_GROUP_HIST, KID_GROUP_SCAN,
   KID_GROUP_SCATTER, KID_TC_PREPARE, KID_TC_GATHER, KID_TC_GATEUP, KID_TC_DOWN, KID_COMBINE, KID_PACK, KID_HOST_COPY,
-  KID_WAIT_SELFTEST, KID_COUNT
+  KID_WAIT_SELFTEST, KID_BLOB_CRC32, KID_COUNT
 };
 void kernel_begin(int kid, cudaStream_t s);
 void kernel_end(int kid, cudaStream_t s);
@@ -288,6 +288,9 @@ unsigned long long launches_this_thread();
     kernel_end((kid), (s));        \
   } while (0)
 
+// CRC-32 of packed blobs (checksum.cu): on the host, and one CTA per blob on the device.
+uint32_t blob_crc32_host(const uint8_t* data, int64_t n);
+cudaError_t launch_blob_crc32(const uint8_t* blobs, int64_t stride, int64_t n_blobs, uint32_t* crc, cudaStream_t s);
 // The decode layer's bounded waits on conditions that never hold, with limit_ns (decode_fused.cu).
 cudaError_t launch_wait_selftest(const uint64_t* word, uint32_t tag, unsigned long long limit_ns, int* status,
                                  cudaStream_t s);

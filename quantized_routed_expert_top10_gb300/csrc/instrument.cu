@@ -18,6 +18,7 @@ static_assert(KID_DECODE_LAYER == STRATA_KERNEL_DECODE_LAYER && KID_ROUTE_DECODE
                   KID_TC_GATEUP == STRATA_KERNEL_TC_GATEUP && KID_TC_DOWN == STRATA_KERNEL_TC_DOWN &&
                   KID_COMBINE == STRATA_KERNEL_COMBINE && KID_PACK == STRATA_KERNEL_PACK &&
                   KID_HOST_COPY == STRATA_KERNEL_HOST_COPY && KID_WAIT_SELFTEST == STRATA_KERNEL_WAIT_SELFTEST &&
+                  KID_BLOB_CRC32 == STRATA_KERNEL_BLOB_CRC32 &&
                   KID_COUNT == STRATA_KERNEL_COUNT,
               "kernel ids of the ABI and the library differ");
 

@@ -31,7 +31,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 21
+    assert len(names) == 23
     assert sorted(names) == sorted(qre.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -81,6 +81,20 @@ def test_pack_round_trip_and_documented_layout(lib):
             chunk = 921600 + ((nr // 128) * 10 + kb) * 2304
             np.testing.assert_array_equal(p[chunk + 16 * (nr % 128): chunk + 16 * (nr % 128) + 16], blk[2:])
             np.testing.assert_array_equal(p[chunk + 2048 + 2 * (nr % 128): chunk + 2048 + 2 * (nr % 128) + 2], blk[:2])
+
+
+def test_blob_crc32_host_is_zlibs(lib):
+    import zlib
+    n, stride = 3, qre.BLOB_BYTES + 256
+    buf = np.random.default_rng(5).integers(0, 256, n * stride, dtype=np.uint8)
+    crc = np.zeros(n, dtype=np.uint32)
+    qre.strata_blob_crc32(buf, n, crc, stride=stride)
+    for j in range(n):
+        assert int(crc[j]) == zlib.crc32(buf[j * stride: j * stride + qre.BLOB_BYTES].tobytes())
+    buf[stride + 12345] ^= 1  # one flipped bit in blob 1 changes only its checksum
+    crc2 = np.zeros(n, dtype=np.uint32)
+    qre.strata_blob_crc32(buf, n, crc2, stride=stride)
+    assert crc2[0] == crc[0] and crc2[2] == crc[2] and crc2[1] != crc[1]
 
 
 def test_pack_rejects_overlap_and_null(lib):
@@ -161,6 +175,17 @@ def test_host_argument_checks(lib):
     assert lib.strata_moe_wait_selftest(A, 1024, 10000, None) == -6
     assert lib.strata_moe_wait_selftest(A, ws1, 999, None) == -1
     assert lib.strata_moe_wait_selftest(A, ws1, 2000000001, None) == -1
+    # blob checksums: sizes, pointers and alignment checked first
+    assert lib.strata_blob_crc32(None, qre.BLOB_BYTES, 1, A) == -1
+    assert lib.strata_blob_crc32(A, qre.BLOB_BYTES - 1, 1, A) == -1
+    assert lib.strata_blob_crc32(A, qre.BLOB_BYTES, -1, A) == -1
+    assert lib.strata_blob_crc32(None, qre.BLOB_BYTES, 0, None) == 0
+    assert lib.strata_blob_crc32_device(A, qre.BLOB_BYTES, -1, A, None) == -1
+    assert lib.strata_blob_crc32_device(None, qre.BLOB_BYTES, 2, A, None) == -1
+    assert lib.strata_blob_crc32_device(A + 16, qre.BLOB_BYTES, 2, A, None) == -2
+    assert lib.strata_blob_crc32_device(A, qre.BLOB_BYTES + 16, 2, A, None) == -2
+    assert lib.strata_blob_crc32_device(A, qre.BLOB_BYTES, 2, A + 2, None) == -2
+    assert lib.strata_blob_crc32_device(A, qre.BLOB_BYTES, 0, A, None) == 0
     # empty calls are valid and enqueue nothing
     assert lib.strata_moe_route(A, 0, A, None, 512, A, A, None, A, ws_big, None) == 0
     assert lib.strata_moe_layer(ctypes.byref(ex), A, None, A, 0, 0, A, None, None, A, ws_big, None) == 0
@@ -186,6 +211,6 @@ def test_profile_arm_argument_checks(lib):
 
 def test_kernel_ids_match_header():
     src = open(HEADER).read()
-    ids = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"#define STRATA_KERNEL_([A-Z_]+) (\d+)", src))
+    ids = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"#define STRATA_KERNEL_([A-Z0-9_]+) (\d+)", src))
     assert ids.pop("COUNT") == len(qre.KERNELS)
     assert ids == qre.KERNEL_ID
