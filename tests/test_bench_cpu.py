@@ -1,0 +1,42 @@
+"""The benchmark's JSON contract, checked on the CPU: the reference arm (the oracle on the host cores)
+runs without a GPU, and its one JSON line carries the keys and types the contract names."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, stdout=subprocess.PIPE,
+                       stderr=subprocess.PIPE, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout  # exactly one JSON line
+    return json.loads(lines[0])
+
+
+def test_reference_arm_json_line():
+    d = run_bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert d["impl"] == "reference"
+    for key, typ in (("metric", str), ("value", float), ("unit", str), ("steps", int), ("warmup", int),
+                     ("ms_per_step", float), ("higher_is_better", bool), ("scaling", str), ("dtype", str),
+                     ("data", str), ("config", dict), ("cpu_baseline", dict), ("e2e", dict)):
+        assert isinstance(d[key], typ), key
+    assert d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["config"]["workload"] == "verify_4tok_1layer"  # the default workload, the same as the GPU arm's
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_whole_job_rate():
+    # tokens per step x steps x ranks / total seconds
+    assert bench.whole_job_rate(4, 10, 2, 100.0) == 4 * 10 * 2 / 0.1
