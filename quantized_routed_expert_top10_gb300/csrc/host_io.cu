@@ -42,6 +42,16 @@ inline void* mapped(const void* p) {
   return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
+// The device address of the page-locked host buffer [p, p + bytes), or nullptr: its first and last
+// bytes must both be page-locked and mapped the same distance apart (the buffer lies in one allocation
+// or registration, as the header requires); anything else takes the copy engines.
+inline void* mapped_range(const void* p, size_t bytes) {
+  void* m0 = mapped(p);
+  if (!m0 || bytes == 0) return m0;
+  void* m1 = mapped((const char*)p + bytes - 1);
+  return m1 == (char*)m0 + (bytes - 1) ? m0 : nullptr;
+}
+
 // dst[i] = src[i], 16-byte words; one side is page-locked host memory reached through its device
 // mapping, the other the workspace's I/O area.
 __global__ void __launch_bounds__(256) host_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
@@ -203,8 +213,8 @@ strata_status strata_moe_layer_host(const strata_experts_t* ex, const uint16_t* 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STRATA_E_CUDA;
   STRATA_TRY_HOST(not_capturing(s));
-  const void* xm = mapped(x_host);
-  const void* om = mapped(out_host);
+  const void* xm = mapped_range(x_host, bytes);
+  const void* om = mapped_range(out_host, bytes);
   HostKey key;
   key.kind = 0;
   key.device = dev;
@@ -248,7 +258,7 @@ strata_status strata_moe_stack_host(const strata_experts_t* ex, const uint16_t* 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STRATA_E_CUDA;
   STRATA_TRY_HOST(not_capturing(s));
-  const void* xm = mapped(x_host);
+  const void* xm = mapped_range(x_host, bytes);
   HostKey key;
   key.kind = 1;
   key.device = dev;
