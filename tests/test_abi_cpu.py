@@ -37,6 +37,27 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_prepared_calls_marshal_and_report_errors(lib):
+    """The binding's prepared host calls pass their fixed arguments on every call; a call the library
+    rejects before touching the device raises each time it is repeated."""
+    A = 1 << 20
+    ex = qre.experts(A, 512, 1)
+    hx = np.zeros((4, 2560), dtype=np.float32)
+    ho = np.zeros((4, 2560), dtype=np.float32)
+    ws_big = qre.strata_moe_workspace_bytes(4)
+    bad = qre.prepare_layer_host(ex, A, None, hx, 4, 2, ho, None, None, A, ws_bytes=ws_big, stream=0)  # flags
+    for _ in range(2):
+        with pytest.raises(qre.StrataError) as e:
+            bad()
+        assert e.value.status == -1
+    empty = qre.prepare_layer_host(ex, A, None, hx, 0, 0, ho, None, None, A, ws_bytes=ws_big, stream=0)
+    empty()  # T = 0: valid, nothing enqueued
+    bad_stack = qre.prepare_stack_host([ex, qre.experts(A, 100, 1)], A, None, 2, hx, 4, None, None, A,
+                                       ws_bytes=ws_big, stream=0)
+    with pytest.raises(qre.StrataError):
+        bad_stack()
+
+
 def test_status_strings(lib):
     for code, name in qre.STATUS.items():
         assert qre.strata_status_str(code).startswith(name)
