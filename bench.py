@@ -1,17 +1,25 @@
 """Benchmark of the GB300 routed-expert MoE block (one JSON line on stdout).
 
-Default workload: the 4-token verify window (one MoE layer, 512 Q2_0 experts, top-10, inputs
-x_j = x_0 + 0.3 N(0,1), seed 0).  A step is one strata_moe_layer call (router GEMV, top-10,
-grouping, Q2_0 SwiGLU experts, combine) on inputs resident in HBM; the step's working set fits in
-the 129 MB L2, so a 256 MB buffer is written between timed steps (flush excluded from the step
-time, which is taken with CUDA events around each step on the launching stream).
+Headline workload (the default): the long prefill, 8,192 tokens through 48 residual MoE layers
+(512 Q2_0 experts per layer, 33,973,862,400 bytes of blobs resident in HBM, top-10 routing with a
+Zipf prior reseeded per layer, seed 0).  A step is one strata_moe_stack call over the chunk (router
+GEMM, top-10, grouping, Q2_0 SwiGLU experts on the tensor cores, combine, rmsnorm + residual, for
+every layer) on inputs resident in HBM; the step streams far more than the 129 MB L2, so no flush is
+needed.  The line's "configs" record measures the other workloads of the block the same way, each with
+its own roofline, end-to-end figure and oracle baseline:
+  0  one token, one layer            (HBM-bound decode; L2 flushed between steps)
+  1  4-token verify window, one layer (HBM-bound decode; L2 flushed between steps)
+  2  one token through 48 layers      (HBM-bound decode stack)
+  3  2,048 tokens, one layer          (tensor-core prefill; reports the per-expert load)
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+                  [--no-cpu-baseline] [--no-subconfigs] [--layers L]
 
---config 0..4 selects the other workloads of the block (decode 1 token; verify window; 48-layer
-decode stack; 2,048-token prefill; 8,192-token x 48-layer prefill).  --impl reference times the
-CPU oracle (plain C, double precision) on the host cores on a bounded sample of the same workload.
-Under torchrun each rank runs an independent replica (the block shards by requests; no collective).
+--config picks the headline workload (default 4); --impl reference times the CPU oracle (plain C,
+double precision) on the host cores on a bounded sample of the headline workload; --layers limits a
+stack workload to its first L layers (for profiling one layer's kernels; such a line is not a bench
+figure).  Under torchrun each rank runs an independent replica (the block shards by requests; no
+collective on the data path).
 """
 from __future__ import annotations
 
@@ -32,23 +40,31 @@ import gen  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) / TC util (prefill)"
 E = 512
+H = 2560
 BLOB = 1382400
-ROUTER_BYTES = 512 * 2560 * 2
+ROUTER_BYTES = E * H * 2
+HEADLINE = 4
+SUBCONFIGS = (0, 1, 2, 3)
+# timed steps per workload: the headline's default, and the sub-records' (each about a second or less)
+DEFAULT_STEPS = {0: 2000, 1: 2000, 2: 100, 3: 50, 4: 10}
+SUB_STEPS = {0: 1000, 1: 1000, 2: 60, 3: 30, 4: 3}
+# expert FLOPs per (token, expert) pair: gate/up two 640 x 2560 products, down one 2560 x 640
+FLOPS_PER_PAIR = {"TC_GATEUP": 2 * 2 * 2560 * 640, "TC_DOWN": 2 * 640 * 2560}
+ROUTER_FLOPS_PER_TOKEN = 2 * E * H
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=HEADLINE)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
-
-
-DEFAULT_STEPS = {0: 4000, 1: 4000, 2: 100, 3: 50, 4: 3}
+    ap.add_argument("--no-subconfigs", action="store_true")
+    ap.add_argument("--layers", type=int, default=None)
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -119,28 +135,29 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # workload set-up
 # ------------------------------------------------------------------------------------------------
-def setup_device(cfg_id, seed, dev):
-    import torch
+class Arena:
+    """Packed blobs of layers 0..n_layers-1 (seed `seed`), generated and packed on the device, shared by
+    every workload (they all draw layer l's experts from the same seed)."""
 
-    import quantized_routed_expert_top10_gb300 as qre
-    cfg = gen.config_inputs(cfg_id, seed)
-    L, T = cfg["L"], cfg["T"]
-    table = torch.from_numpy(gen.SCALE_TABLE.view(np.int16)).to(dev)
-    arena = torch.empty(L * E * BLOB, dtype=torch.uint8, device=dev)
-    tmp = torch.empty(E * BLOB, dtype=torch.uint8, device=dev)
-    s = torch.cuda.current_stream().cuda_stream
-    for l in range(L):
-        gen.device_canonical_blobs(seed, l, 0, E, table.data_ptr(), tmp.data_ptr(), BLOB, s)
-        qre.strata_pack_q2_0_device(tmp, BLOB, arena[l * E * BLOB:], BLOB, E)
-    del tmp
-    wr = torch.from_numpy(np.stack(cfg["wr"]).view(np.int16)).to(dev)
-    bias = None
-    if cfg["bias"][0] is not None:
-        bias = torch.from_numpy(np.stack(cfg["bias"])).to(dev)
-    exs = [qre.experts(arena[l * E * BLOB:], E, 1) for l in range(L)]
-    x_host = cfg["x"]
-    torch.cuda.synchronize()
-    return cfg, arena, wr, bias, exs, x_host
+    def __init__(self, qre, seed, dev, n_layers):
+        import torch
+        self.n_layers = n_layers
+        table = torch.from_numpy(gen.SCALE_TABLE.view(np.int16)).to(dev)
+        self.blobs = torch.empty(n_layers * E * BLOB, dtype=torch.uint8, device=dev)
+        tmp = torch.empty(E * BLOB, dtype=torch.uint8, device=dev)
+        s = torch.cuda.current_stream().cuda_stream
+        for l in range(n_layers):
+            gen.device_canonical_blobs(seed, l, 0, E, table.data_ptr(), tmp.data_ptr(), BLOB, s)
+            qre.strata_pack_q2_0_device(tmp, BLOB, self.blobs[l * E * BLOB:], BLOB, E)
+        del tmp
+        torch.cuda.synchronize()
+        self.exs = [qre.experts(self.blobs[l * E * BLOB:], E, 1) for l in range(n_layers)]
+
+
+def workload(cfg_id, seed, layers=None):
+    c = gen.CONFIGS[cfg_id]
+    L = c["L"] if layers is None or c["L"] == 1 else min(layers, c["L"])
+    return gen.config_inputs(cfg_id, seed, L=L)
 
 
 def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws):
@@ -154,27 +171,24 @@ def run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws):
     return x_work
 
 
-# Kernels timed with the library's own event hooks inside the timed region: the whole decode layer for
-# T <= 8; for prefill every kernel of the step (the dominant one is picked by total time).
+# Kernels timed with the library's own event hooks: the whole decode layer for T <= 8; for prefill
+# every kernel of the step (the dominant one is picked by total time).
 PREFILL_KERNELS = ("ROUTER_PREP", "ROUTER_TC", "TOP_K", "GROUP_HIST", "GROUP_SCAN", "GROUP_SCATTER", "TC_PREPARE",
                    "TC_GATHER", "TC_GATEUP", "TC_DOWN", "COMBINE")
-FLOPS_PER_PAIR = {"TC_GATEUP": 2 * 2 * 2560 * 640, "TC_DOWN": 2 * 640 * 2560}
 CSRC = os.path.join(ROOT, "quantized_routed_expert_top10_gb300", "csrc")
 KERNEL_SOURCES = {
     "DECODE_LAYER": ("decode_fused.cu", "common.cuh", "device_common.cuh"),
     "TC_GATEUP": ("experts_tc.cu", "tc_common.cuh", "common.cuh", "device_common.cuh"),
     "TC_DOWN": ("experts_tc.cu", "tc_common.cuh", "common.cuh", "device_common.cuh"),
 }
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture of the
-# workload (summaries under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's
-# sources at capture time: once a source changes the figure no longer describes the kernel (null).
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture (summaries
+# under profiles/), keyed by (workload, kernel), with the SHA-256 of the kernel's sources at capture
+# time: once a source changes the figure no longer describes the kernel (null).  A stack workload's
+# per-launch figure is one layer's launch, captured on its first layer (--layers 1).
 NCU_TRAFFIC = {
     # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,614,848 / 29,607,680 /
     # 29,626,880 B read, 8,448 / 0 / 0 B written)
     ("verify_4tok_1layer", "DECODE_LAYER"): (29619285, "5ad4c6c9dc1077e8"),
-    # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (288977408 + 9764096, "08f79a4ce57ba945"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (121604096 + 145818880, "08f79a4ce57ba945"),
 }
 
 
@@ -187,8 +201,8 @@ def source_digest(kernel):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, kernel):
-    rec = NCU_TRAFFIC.get((workload, kernel))
+def ncu_traffic(workload_name, kernel):
+    rec = NCU_TRAFFIC.get((workload_name, kernel))
     if rec is None or rec[1] != source_digest(kernel):
         return None
     return rec[0]
@@ -210,55 +224,46 @@ def whole_job_rate(tokens_per_step, steps, world, total_ms):
     return world * tokens_per_step * steps / (total_ms / 1e3)
 
 
-def measure_gb300(args, rank, world, local_rank):
+def measure_workload(qre, arena, cfg_id, args, K, W, world, dev, local_rank, e2e_calls):
+    """Time K steps of one workload (after W warm-up steps) and return its record."""
     import torch
-
-    import quantized_routed_expert_top10_gb300 as qre
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    cfg_id = args.config
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg_id]
-    W = max(3, args.warmup)
-    cfg, arena, wr, bias, exs, x_host = setup_device(cfg_id, args.seed, dev)
+    cfg = workload(cfg_id, args.seed, args.layers)
     T, L = cfg["T"], cfg["L"]
+    wr = torch.from_numpy(np.stack(cfg["wr"]).view(np.int16)).to(dev)
+    bias = None if cfg["bias"][0] is None else torch.from_numpy(np.stack(cfg["bias"])).to(dev)
+    exs = arena.exs[:L]
+    x_host = cfg["x"]
     x_in = torch.from_numpy(x_host).to(dev)
     x_work = torch.empty_like(x_in)
     out = torch.empty_like(x_in)
     ids = torch.empty(T, 10, dtype=torch.int32, device=dev)
     ids_all = torch.empty(L, T, 10, dtype=torch.int32, device=dev) if L > 1 else None
-    ws_bytes = qre.strata_moe_workspace_bytes(T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.empty(qre.strata_moe_workspace_bytes(T), dtype=torch.uint8, device=dev)
     qre.strata_moe_workspace_init(ws)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    need_flush = L == 1 and cfg_id in (0, 1)  # working set < L2; the stacks and prefill stream > L2
+    need_flush = L == 1 and T <= 8  # one decode layer's working set fits the L2; everything else streams past it
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if need_flush else None
     stream = torch.cuda.current_stream()
+    step_args = (qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
 
     for _ in range(W):
-        run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
+        run_step(*step_args)
     torch.cuda.synchronize()
-    st = qre.strata_poll_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
+    check_status(qre, ws)
 
-    # Decode steps (T <= 8: one cooperative launch per layer) would be bound by the host's launch
-    # rate, so the step is captured once in a CUDA graph and replayed; prefill steps run eagerly.
+    # Decode steps (T <= 8: one cooperative launch per layer) would be bound by the host's launch rate,
+    # so the step is captured once in a CUDA graph and replayed; prefill steps run eagerly.
     graph, graph_launches, graph_note = None, None, "eager launches"
     if T <= 8:
         try:
             n0 = qre.strata_moe_launch_count()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
+                run_step(*step_args)
             graph_launches = qre.strata_moe_launch_count() - n0
             for _ in range(W):
                 graph.replay()
             torch.cuda.synchronize()
-            st = qre.strata_poll_status(ws)
-            if st != 0:
-                raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
+            check_status(qre, ws)
             graph_note = "CUDA graph replay of the step"
         except Exception as exc:  # capture refused: fall back to eager launches, and say so
             graph, graph_launches = None, None
@@ -268,10 +273,10 @@ def measure_gb300(args, rank, world, local_rank):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     # Dominant-kernel timing inside the timed region: T <= 8 and one layer -> the step is exactly one
-    # launch of the decode layer kernel (its events are the step's); T <= 8 stacks -> replayed as a
-    # graph: the step time over its L launches (an upper bound on the kernel's duration), or, run
-    # eagerly, library event hooks around one layer per step; prefill -> every launch of the two
-    # tensor-core expert kernels.
+    # launch of the decode layer kernel (its events are the step's); T <= 8 stacks replayed as a graph ->
+    # the step time over its L launches (an upper bound on the kernel's duration), or, run eagerly,
+    # library event hooks around one layer per step; prefill -> every launch of the two tensor-core
+    # expert kernels.
     timed = () if (T <= 8 and (L == 1 or graph is not None)) else ("DECODE_LAYER",) if T <= 8 \
         else ("TC_GATEUP", "TC_DOWN")
     per_step = 1 if T <= 8 else L
@@ -303,7 +308,7 @@ def measure_gb300(args, rank, world, local_rank):
         if graph is not None:
             graph.replay()
         else:
-            run_step(qre, cfg, exs, wr, bias, x_in, x_work, out, ids, ids_all, ws)
+            run_step(*step_args)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -313,63 +318,52 @@ def measure_gb300(args, rank, world, local_rank):
         kernel_ms[k] = [a.elapsed_time(b) for a, b in zip(*kev[k])]
         qre.strata_moe_profile_arm(k, [], [])
     del armed
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if T <= 8 and L == 1:
-        kernel_ms["DECODE_LAYER"] = step_ms_list(starts, ends)
+        kernel_ms["DECODE_LAYER"] = list(step_ms)
     elif T <= 8 and graph is not None:
-        kernel_ms["DECODE_LAYER"] = [m / L for m in step_ms_list(starts, ends) for _ in range(L)]
+        kernel_ms["DECODE_LAYER"] = [m / L for m in step_ms for _ in range(L)]
     if wall < 1.0:
         time.sleep(0.3)
     clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = float(np.sum(step_ms))
     if world > 1:
         total_ms = max_over_ranks(total_ms, dev)
-    st = qre.strata_poll_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
-    ids_h = ids.cpu().numpy()
-    ids_all_h = ids_all.cpu().numpy() if L > 1 else None
-    value = whole_job_rate(T, K, world, total_ms)
+    check_status(qre, ws)
+    ids_layers = ids_all.cpu().numpy() if L > 1 else ids.cpu().numpy()[None]
 
-    # ---- dominant kernel ----
-    roof = kernel_roofline(cfg, kernel_ms, K, ids_all_h if L > 1 else ids_h[None],
-                           graph_stack=T <= 8 and L > 1 and graph is not None)
-    if T > 8:
-        roof["kernel_ms_per_step"] = step_breakdown(qre, run_step, (qre, cfg, exs, wr, bias, x_in, x_work, out, ids,
-                                                                   ids_all, ws), stream, L)
-
-    # ---- end to end through the public API with host buffers ----
-    e2e = measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush if need_flush else None, dev,
-                      max(20, min(K, 500)), world)
-
-    result = {
-        "metric": METRIC,
-        "value": value,
+    roof = kernel_roofline(cfg, kernel_ms, ids_layers, graph_stack=T <= 8 and L > 1 and graph is not None)
+    rec = {
+        "value": whole_job_rate(T, K, world, total_ms),
         "unit": "tokens/s",
-        "n_gpus": world,
         "steps": K,
         "warmup": W,
         "ms_per_step": total_ms / K,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": path_dtype(T),
-        "data": "synthetic (seeded Philox4x32-10 inputs; random Q2_0 experts; no trained weights)",
-        "config": dict(workload_config(cfg, args.seed, world, need_flush,
-                                       int(len(np.unique(ids_h))) if L == 1 else None), launch=graph_note),
+        "config": dict(workload_config(cfg, args.seed, world, need_flush), launch=graph_note),
         "roofline": roof,
         "clocks": clk,
-        "e2e": e2e,
         "gpu_launches": n_launches,
     }
-    return result, cfg, ids_h
+    if T > 8:
+        rec["kernel_ms_per_step"] = step_breakdown(qre, step_args, stream, L)
+        rec["step_tc"] = step_tensor_fraction(cfg, total_ms / K)
+        rec["expert_load"] = expert_load(ids_layers)
+    else:
+        rec["distinct_experts_per_layer"] = float(np.mean([len(np.unique(l)) for l in ids_layers]))
+    rec["e2e"] = measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, flush, dev, e2e_calls, world)
+    del ws, flush
+    torch.cuda.empty_cache()
+    return rec
 
 
-def step_ms_list(starts, ends):
-    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+def check_status(qre, ws):
+    st = qre.strata_poll_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {qre.STATUS.get(st, st)}")
 
 
-def step_breakdown(qre, fn, args, stream, L, steps=2):
+def step_breakdown(qre, step_args, stream, L, steps=2):
     """Per-kernel device time of a step (ms), from a separate untimed pass with every prefill kernel's
     launches bracketed by events (the extra event records are kept out of the timed region)."""
     import torch
@@ -383,7 +377,7 @@ def step_breakdown(qre, fn, args, stream, L, steps=2):
     for k in PREFILL_KERNELS:
         armed[k] = qre.strata_moe_profile_arm(k, *evs[k])
     for _ in range(steps):
-        fn(*args)
+        run_step(*step_args)
     torch.cuda.synchronize()
     out = {}
     for k in PREFILL_KERNELS:
@@ -404,7 +398,7 @@ def path_dtype(T):
     return "f16 mma.sync, fp32 acc" if T <= 8 else "f16 tcgen05, fp32 acc"
 
 
-def workload_config(cfg, seed, world, need_flush, distinct):
+def workload_config(cfg, seed, world, need_flush):
     return {
         "workload": cfg["name"],
         "tokens": cfg["T"],
@@ -417,12 +411,11 @@ def workload_config(cfg, seed, world, need_flush, distinct):
         "seed": seed,
         "l2": "256 MB buffer written between timed steps (flush excluded)" if need_flush
         else "working set larger than L2 (no flush)",
-        "distinct_experts_last_step": distinct,
         "parallelism": f"replicas x{world}",
     }
 
 
-def kernel_roofline(cfg, kernel_ms, K, ids_layers, graph_stack=False):
+def kernel_roofline(cfg, kernel_ms, ids_layers, graph_stack=False):
     """Roofline of the dominant kernel from the per-launch event times taken in the timed region.
 
     decode layer (T <= 8): HBM-bound; algorithmic bytes per launch = router rows (512 x 2560 bf16) +
@@ -450,25 +443,59 @@ def kernel_roofline(cfg, kernel_ms, K, ids_layers, graph_stack=False):
                 "algorithmic_bytes_per_launch": per_launch, "distinct_experts_per_layer": float(np.mean(d)),
                 "avg_launch_ms": avg_ms, "launches_timed": len(ms),
                 "timing": "step events (one launch per step)" if L == 1 else
-                "step events / 48 (graph replay of the 48 launches; includes the gaps between them)"
-                if graph_stack else "library event hooks around one layer per step (layer = step % 48)"}
+                "step events / layers (graph replay of the layer launches; includes the gaps between them)"
+                if graph_stack else "library event hooks around one layer per step (layer = step % layers)"}
     peak = tc_burst if L == 1 else tc_sust
     flops = T * 10 * FLOPS_PER_PAIR[dom]
     achieved = flops / (avg_ms / 1e3) / 1e12
     other = "TC_DOWN" if dom == "TC_GATEUP" else "TC_GATEUP"
     o_ms = float(np.mean(kernel_ms[other])) if kernel_ms.get(other) else None
-    return {"kernel": f"tc_expert_kernel ({'gate/up + SwiGLU' if dom == 'TC_GATEUP' else 'down'}, tcgen05 fp16)",
+    return {"kernel": f"tc_expert_kernel ({'gate/up + SwiGLU' if dom == 'TC_GATEUP' else 'down + combine'}, "
+                      f"tcgen05 fp16)",
             "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "frac_of": f"{'bf16_tflops' if L == 1 else 'bf16_tflops_sustained'}, {src}",
             "traffic": ncu_traffic(cfg["name"], dom), "algorithmic_flops_per_launch": flops,
             "avg_launch_ms": avg_ms, "launches_timed": len(ms),
             "other_expert_kernel": None if o_ms is None else {
                 "kernel": other, "avg_launch_ms": o_ms,
-                "achieved_tflops": T * 10 * FLOPS_PER_PAIR[other] / (o_ms / 1e3) / 1e12},
+                "achieved_tflops": T * 10 * FLOPS_PER_PAIR[other] / (o_ms / 1e3) / 1e12,
+                "frac": T * 10 * FLOPS_PER_PAIR[other] / (o_ms / 1e3) / 1e12 / peak},
             "timing": "library event hooks around every launch of the two expert kernels"}
 
 
-def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, world):
+def step_tensor_fraction(cfg, step_ms):
+    """The whole step's algorithmic tensor work (expert gate/up and down, and the router GEMM) over the
+    step time, against the same peak as the dominant kernel."""
+    _, tc_burst, tc_sust, how = load_peaks()
+    T, L = cfg["T"], cfg["L"]
+    flops = L * T * (10 * (FLOPS_PER_PAIR["TC_GATEUP"] + FLOPS_PER_PAIR["TC_DOWN"]) + ROUTER_FLOPS_PER_TOKEN)
+    peak = tc_burst if L == 1 else tc_sust
+    achieved = flops / (step_ms / 1e3) / 1e12
+    return {"flops_per_step": flops, "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "frac_of": f"{'bf16_tflops' if L == 1 else 'bf16_tflops_sustained'}, {how}"}
+
+
+def expert_load(ids_layers):
+    """Tokens per expert of each layer's routing: experts touched (U), the largest and the mean load
+    over the touched experts, their ratio (the load imbalance) and, for one layer, the whole sorted
+    histogram."""
+    counts = [np.bincount(l.reshape(-1), minlength=E) for l in ids_layers]
+    U = [int(np.count_nonzero(c)) for c in counts]
+    mx = [int(c.max()) for c in counts]
+    mean = [float(c[c > 0].mean()) for c in counts]
+    rec = {"experts_touched": U[0] if len(U) == 1 else float(np.mean(U)),
+           "max_tokens_per_expert": mx[0] if len(mx) == 1 else float(np.mean(mx)),
+           "mean_tokens_per_touched_expert": mean[0] if len(mean) == 1 else float(np.mean(mean)),
+           "max_over_mean": float(np.mean([a / b for a, b in zip(mx, mean)]))}
+    if len(counts) == 1:
+        c = counts[0]
+        rec["tokens_per_expert_sorted"] = sorted((int(v) for v in c[c > 0]), reverse=True)
+    else:
+        rec["per_layer"] = "mean over layers"
+    return rec
+
+
+def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, flush, dev, n, world):
     """The user's call: strata_moe_layer_host / strata_moe_stack_host on page-locked host buffers, on a
     stream of its own.  Each call copies the step's input in, runs it, copies the result out and
     returns after synchronising, so the host wall clock around the call is the whole step."""
@@ -504,61 +531,146 @@ def measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, stream, flush, dev, n, worl
 # ------------------------------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ------------------------------------------------------------------------------------------------
-def oracle_sample(cfg_id, seed, budget_s=12.0, max_reps=None):
-    """Time the oracle on a bounded sample of the workload; returns (tokens/s, threads, description)."""
-    import oracle
-    cfg = gen.config_inputs(cfg_id, seed, L=1 if cfg_id in (2, 4) else None)
-    x = cfg["x"]
-    T = x.shape[0]
-    tok = T if T <= 4 else 4
-    xs = x[:tok]
-    wr, bias = cfg["wr"][0], cfg["bias"][0]
-    residual = cfg["residual"]
-    r = oracle.route(xs, wr, bias, residual=residual)
-    blobs = [None] * E
-    for e in np.unique(r["ids"]):
-        blobs[int(e)] = gen.canonical_blob(seed, 0, int(e))
-    threads = max(1, min(os.cpu_count() or 1, tok))
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.moe_layer(xs, wr, bias, blobs, residual=residual, n_threads=threads)
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleSample:
+    """A bounded sample of a workload for the oracle: `tokens` tokens drawn like the workload's (its
+    router, bias and layer-0 experts; for one-token and verify-window workloads, more tokens of the same
+    distribution so that every thread has one), one layer.  A 48-layer workload's per-token time is the
+    one-layer time x 48."""
+
+    def __init__(self, cfg_id, seed, tokens):
+        import oracle
+        self.oracle = oracle
+        c = gen.CONFIGS[cfg_id]
+        cfg = gen.config_inputs(cfg_id, seed, T=tokens, L=1)
+        self.name = c["name"]
+        self.layers = c["L"]
+        self.x = np.ascontiguousarray(cfg["x"][:tokens])
+        self.tokens = self.x.shape[0]
+        self.wr, self.bias, self.residual = cfg["wr"][0], cfg["bias"][0], cfg["residual"]
+        r = oracle.route(self.x, self.wr, self.bias, residual=self.residual)
+        self.blobs = [None] * E
+        for e in np.unique(r["ids"]):
+            self.blobs[int(e)] = gen.canonical_blob(seed, 0, int(e))
+
+    def run(self, threads):
+        t0 = time.perf_counter()
+        self.oracle.moe_layer(self.x, self.wr, self.bias, self.blobs, residual=self.residual, n_threads=threads)
+        return time.perf_counter() - t0
+
+    def rate(self, seconds):
+        """Tokens of the workload per second, from one layer's time over the sample."""
+        return self.tokens / seconds / self.layers
+
+    def describe(self, reps, seconds, threads):
+        return (f"{self.tokens} token(s) x 1 layer of {self.name} on {threads} thread(s), repeated {reps}x in "
+                f"{seconds:.1f} s" + (f", per-token time x{self.layers} layers" if self.layers > 1 else ""))
+
+
+def oracle_baseline(cfg_id, seed, budget_s, single_thread=False):
+    """The oracle timed on every host core (threads = cores, one token per thread at least), repeated
+    until budget_s; with single_thread also one token on one thread."""
+    cores = host_cores()
+    smp = OracleSample(cfg_id, seed, cores)
+    reps, el = 0, 0.0
+    while el < budget_s or reps == 0:
+        el += smp.run(cores)
         reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or (max_reps and reps >= max_reps):
-            break
-    layers = cfg_id in (2, 4)
-    tps = tok * reps / el
-    if layers:
-        tps /= 48.0  # one layer timed; a token of the workload passes 48 layers
-    desc = (f"{tok} token(s) x 1 layer of {cfg['name']}, repeated {reps}x in {el:.1f} s"
-            + (", per-token time x48 layers" if layers else ""))
-    return tps, threads, desc, el / reps
+    rec = {"value": smp.rate(el / reps), "unit": "tokens/s", "cores": cores, "threads": cores, "host_cores": cores,
+           "kind": "oracle", "sample": smp.describe(reps, el, cores)}
+    if single_thread:
+        one = OracleSample(cfg_id, seed, 1)
+        r1, e1 = 0, 0.0
+        while e1 < budget_s / 3 or r1 == 0:
+            e1 += one.run(1)
+            r1 += 1
+        rec["single_thread"] = {"value": one.rate(e1 / r1), "unit": "tokens/s", "threads": 1,
+                                "sample": one.describe(r1, e1, 1)}
+    return rec
 
 
 def reference_arm(args, rank):
+    """--impl reference: the oracle on the host cores, each step one bounded sample of the headline
+    workload (one token per core, one layer; x48 for a 48-layer workload)."""
     if rank != 0:
         return None
     cfg_id = args.config
     K = args.steps if args.steps is not None else 5
     W = args.warmup
-    cfg = gen.CONFIGS[cfg_id]
+    cores = host_cores()
+    smp = OracleSample(cfg_id, args.seed, cores)
     for _ in range(min(W, 1)):
-        oracle_sample(cfg_id, args.seed, budget_s=0.0, max_reps=1)
-    step_s = []
-    threads = 1
-    desc = ""
-    for _ in range(K):
-        tps, threads, desc, per = oracle_sample(cfg_id, args.seed, budget_s=0.0, max_reps=1)
-        step_s.append(per)
-    tok = min(cfg["T"], 4)
-    value = tok * K / float(np.sum(step_s)) / (48.0 if cfg_id in (2, 4) else 1.0)
-    cpu = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        smp.run(cores)
+    step_s = [smp.run(cores) for _ in range(K)]
+    value = smp.rate(float(np.mean(step_s)))
+    cfg = gen.CONFIGS[cfg_id]
+    conf = workload_config(dict(name=cfg["name"], T=cfg["T"], L=cfg["L"]), args.seed, 1, cfg["L"] == 1 and cfg["T"] <= 8)
+    cpu = {"value": value, "unit": "tokens/s", "cores": cores, "threads": cores, "host_cores": cores,
+           "kind": "oracle", "sample": smp.describe(K, float(np.sum(step_s)), cores)}
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
             "steps": K, "warmup": W, "ms_per_step": 1e3 * float(np.mean(step_s)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(cfg, args.seed, 1, cfg_id in (0, 1), None),
-            "cpu_baseline": cpu,
+            "config": conf, "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------------------------------
+def measure_gb300(args, rank, world, local_rank):
+    import torch
+
+    import quantized_routed_expert_top10_gb300 as qre
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    head = args.config
+    subs = () if args.no_subconfigs else tuple(c for c in SUBCONFIGS if c != head)
+    n_layers = max(workload(c, args.seed, args.layers)["L"] for c in (head,) + subs)
+    arena = Arena(qre, args.seed, dev, n_layers)
+    W = max(3, args.warmup)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[head]
+    rec = measure_workload(qre, arena, head, args, K, W, world, dev, local_rank,
+                           e2e_calls=max(20, min(K, 500)) if gen.CONFIGS[head]["T"] <= 8 else max(3, min(K, 20)))
+    sub = {}
+    for c in subs:
+        r = measure_workload(qre, arena, c, args, SUB_STEPS[c], W, world, dev, local_rank,
+                             e2e_calls=200 if gen.CONFIGS[c]["T"] <= 8 else 10)
+        sub[str(c)] = r
+    result = {
+        "metric": METRIC,
+        "value": rec["value"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": rec["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": rec["dtype"],
+        "data": "synthetic (seeded Philox4x32-10 inputs; random Q2_0 experts; no trained weights)",
+        "config": rec["config"],
+        "roofline": rec["roofline"],
+        "clocks": rec["clocks"],
+        "e2e": rec["e2e"],
+        "gpu_launches": rec["gpu_launches"],
+    }
+    for key in ("step_tc", "kernel_ms_per_step", "expert_load", "distinct_experts_per_layer"):
+        if key in rec:
+            result[key] = rec[key]
+    if sub:
+        result["configs"] = sub
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
 
 
 def main():
@@ -569,16 +681,15 @@ def main():
         if res is not None:
             print(json.dumps(res), flush=True)
         return
-    res, cfg, ids = measure_gb300(args, rank, world, local_rank)
+    res = measure_gb300(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            tps, threads, desc, _ = oracle_sample(args.config, args.seed)
-            res["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                   "sample": desc}
+            res["cpu_baseline"] = oracle_baseline(args.config, args.seed, budget_s=15.0,
+                                                  single_thread=gen.CONFIGS[args.config]["T"] <= 8)
+            for c, r in res.get("configs", {}).items():
+                r["cpu_baseline"] = oracle_baseline(int(c), args.seed, budget_s=4.0,
+                                                    single_thread=int(c) in (0, 1))
         print(json.dumps(res), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

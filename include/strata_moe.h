@@ -140,8 +140,11 @@ strata_status strata_moe_group_noalloc(const int32_t* ids, int32_t T, int32_t n_
  * expert that owns p.  x fp32 [T][2560]; grouping arrays as strata_moe_group writes them; parts
  * fp32 [T][10][2560].  Weights are the packed blobs of ex (host pointer to the struct).  Computed
  * as grouped tensor-core GEMMs (x rounded to fp16, fp32 accumulation) for every T.  The grouping
- * arrays are checked on the device: an expert id outside [0, n_expert), a slot range outside
- * [0, T*10) or a pair number outside [0, T*10) sets STRATA_E_CORRUPT and that entry is skipped. */
+ * arrays are checked on the device before any expert work: an active entry naming an expert outside
+ * [0, n_expert) or a slot range outside [0, T*10), or active entries that are not strictly increasing
+ * or whose slot ranges are out of order or overlap, set STRATA_E_CORRUPT and the call computes nothing
+ * (parts keeps its contents); a pair number outside [0, T*10) sets STRATA_E_CORRUPT and that slot is
+ * skipped. */
 strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int32_t T,
                                  const int32_t* expert_off, const int32_t* pair, const int32_t* active,
                                  const int32_t* n_active, float* parts, void* ws, size_t ws_bytes,

@@ -43,30 +43,54 @@ struct TcExpert { int32_t e, q0, n, q0pad; };    // grouping slots [q0, q0+n), p
 struct TcTile { int32_t e, q0, n, q0pad; };      // <= 128 tokens of one expert
 
 // ---------------------------------------------------------------------------------------------
-// Tile lists: experts' padded row ranges (multiples of 8) and tiles of at most 128 tokens.  An expert
-// entry outside [0, E) or a slot range outside [0, P) sets ST_CORRUPT and contributes no tile.
+// Tile lists: experts' padded row ranges (multiples of 8) and tiles of at most 128 tokens.  The
+// grouping may come from the caller, so it is checked before any tile is listed: every active entry
+// must name an expert in [0, E) whose slot range lies in [0, P), the entries must be strictly
+// increasing and their ranges in the same order without overlap (so the padded rows of all experts fit
+// rows_cap).  Anything else sets ST_CORRUPT and lists no tile at all: the expert kernels then do
+// nothing and every workspace offset they would derive stays unused.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restrict__ expert_off,
                                                          const int32_t* __restrict__ active,
                                                          const int32_t* __restrict__ n_active, int E, int P,
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
                                                          TcTile* __restrict__ half_tiles, int32_t* __restrict__ counts,
-                                                         int max_tiles, int max_half_tiles, int* __restrict__ status) {
+                                                         int max_tiles, int max_half_tiles, int64_t rows_cap,
+                                                         int* __restrict__ status) {
   __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_nh[EMAX], s_scratch[32];
+  __shared__ int s_e[EMAX], s_end[EMAX];
+  __shared__ int s_bad;
   const int i = threadIdx.x;
+  if (i == 0) s_bad = 0;
   const int na = max(0, min(*n_active, E));
-  int e = 0, q0 = 0, n = 0;
-  if (i < na) {  // the grouping may come from the caller: a bad entry is reported and skipped
+  int e = -1, q0 = 0, n = 0;
+  bool bad = false;
+  if (i < na) {
     e = active[i];
     if (e >= 0 && e < E) {
-      q0 = expert_off[e];
-      n = expert_off[e + 1] - q0;
+      const int first = expert_off[e], end = expert_off[e + 1];
+      if (first >= 0 && end >= first && end <= P) {
+        q0 = first;
+        n = end - first;
+      } else {
+        bad = true;
+      }
+    } else {
+      bad = true;
     }
-    if (e < 0 || e >= E || q0 < 0 || n < 0 || q0 + n > P) {
+  }
+  s_e[i] = e;
+  s_end[i] = q0 + n;
+  __syncthreads();
+  if (i < na && i > 0 && (s_e[i - 1] >= e || s_end[i - 1] > q0)) bad = true;
+  if (bad) s_bad = 1;
+  __syncthreads();
+  if (s_bad) {  // uniform over the CTA
+    if (i == 0) {
       set_status(status, ST_CORRUPT);
-      q0 = 0;
-      n = 0;
+      counts[0] = counts[1] = counts[2] = counts[3] = 0;
     }
+    return;
   }
   s_pad[i] = (i < na) ? (n + 7) / 8 * 8 : 0;
   // gate/up tiles in three classes -- full (TCN tokens), other wide (> TCN_HALF), narrow -- listed in
@@ -83,6 +107,13 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   const int nnarrow = cta_exclusive_scan(s_narrow, s_narrow, EMAX, s_scratch);
   const int ntiles = nfull + nwide + nnarrow;
   const int nhalf = cta_exclusive_scan(s_nh, s_nh, EMAX, s_scratch);
+  if ((int64_t)ppad + TCN > rows_cap) {  // cannot happen once the ranges are disjoint; kept as a bound
+    if (i == 0) {
+      set_status(status, ST_CORRUPT);
+      counts[0] = counts[1] = counts[2] = counts[3] = 0;
+    }
+    return;
+  }
   if (i < na) {
     exps[i] = TcExpert{e, q0, n, s_pad[i]};
     for (int t = 0; t < n / TCN; ++t) {
@@ -513,7 +544,8 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
-                                                    half_tiles, counts, max_tiles, max_half, status));
+                                                    half_tiles, counts, max_tiles, max_half, rows_cap,
+                                                    status));
   STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, T * K, exps, counts, xg,
                                                                                    rows_cap, status));
   cudaError_t err = cudaGetLastError();

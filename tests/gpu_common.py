@@ -84,6 +84,12 @@ class BlobCache:
 
     def layer_list(self, layer, ids, E=512):
         need = set(np.unique(ids).tolist())
+        missing = [e for e in need if (layer, e) not in self.cache]
+        if len(missing) > 16:  # many blobs: draw the whole layer with the device generator (same bits)
+            canon = device_canonical(self.seed, layer, 0, E).cpu().numpy().reshape(E, B)
+            for e in missing:
+                self.cache[(layer, e)] = canon[e].copy()
+            del canon
         return [self.get(layer, e) if e in need else None for e in range(E)]
 
 
@@ -133,3 +139,57 @@ def run_layer(blobs, wr, bias, x, flags=0, q2_offset=1, E=512, ws=None):
     st = qre.strata_poll_status(ws)
     assert st == 0, qre.STATUS.get(st, st)
     return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+# Tile widths of the prefill expert kernels: gate/up tiles hold up to 256 tokens of one expert (a
+# remainder above 128 is a "wide" tile, one of at most 128 a "narrow" one); down tiles up to 128.
+GU_TILE = 256
+DOWN_TILE = 128
+
+
+def tile_tokens(ids: np.ndarray, E: int = 512):
+    """The prefill tiles a routing produces, as (class, expert, first token, last token): per expert the
+    gate/up tiles of 256 slots ('full', then the remainder as 'wide' or 'narrow') and the down tiles of
+    128 slots ('down'), slots in grouping order (ascending pair number)."""
+    off, pair, active = oracle.group(ids, E)
+    out = []
+    for e in active:
+        q0, n = int(off[e]), int(off[e + 1] - off[e])
+        for width, kind in ((GU_TILE, "gu"), (DOWN_TILE, "down")):
+            for t0 in range(0, n, width):
+                m = min(width, n - t0)
+                cls = "down" if kind == "down" else ("full" if m == GU_TILE else "wide" if m > DOWN_TILE else "narrow")
+                out.append((cls, int(e), int(pair[q0 + t0]) // 10, int(pair[q0 + t0 + m - 1]) // 10))
+    return out
+
+
+def stratified_sample(ids: np.ndarray, budget=None, rotate: int = 0, E: int = 512):
+    """Tokens whose outputs a full-size parity check compares: the first and last token of tiles of
+    every class, then of every expert's tiles, so a tile-schedule mistake on any expert shows.  With a
+    budget, the classes' first and last tiles come first, then the experts in an order rotated by
+    `rotate` (so successive layers of a stack cover different experts).  Returns (tokens, experts
+    covered, tiles covered per class)."""
+    tiles = tile_tokens(ids, E)
+    order = []
+    for cls in ("full", "wide", "narrow", "down"):
+        of = [t for t in tiles if t[0] == cls]
+        if of:
+            order += [of[0], of[-1]]
+    experts = sorted({t[1] for t in tiles})
+    if experts:
+        r = rotate % len(experts)
+        rank = {e: i for i, e in enumerate(experts[r:] + experts[:r])}
+        order += sorted(tiles, key=lambda t: (rank[t[1]], t[0]))
+    pick, covered, cls_count = [], set(), {}
+    seen = set()
+    for cls, e, a, b in order:
+        new = [t for t in (a, b) if t not in seen]
+        if budget is not None and len(pick) + len(new) > budget:
+            continue
+        for t in new:
+            seen.add(t)
+            pick.append(t)
+        if (cls, e, a, b) not in covered:
+            covered.add((cls, e, a, b))
+            cls_count[cls] = cls_count.get(cls, 0) + 1
+    return np.array(sorted(pick), dtype=np.int64), len({c[1] for c in covered}), cls_count

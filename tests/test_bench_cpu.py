@@ -5,6 +5,8 @@ import os
 import subprocess
 import sys
 
+import numpy as np
+
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -29,9 +31,11 @@ def test_reference_arm_json_line():
     assert d["steps"] == 1 and d["warmup"] == 3
     assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
-    assert d["config"]["workload"] == "verify_4tok_1layer"  # the default workload, the same as the GPU arm's
+    # the default workload, the same as the GPU arm's headline
+    assert d["config"]["workload"] == "prefill_8192tok_48layer_stack"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["cores"] == cb["threads"] == bench.host_cores()
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
@@ -40,3 +44,22 @@ def test_reference_arm_json_line():
 def test_whole_job_rate():
     # tokens per step x steps x ranks / total seconds
     assert bench.whole_job_rate(4, 10, 2, 100.0) == 4 * 10 * 2 / 0.1
+
+
+def test_oracle_baseline_uses_every_core_and_one_thread():
+    rec = bench.oracle_baseline(0, 0, budget_s=0.0, single_thread=True)
+    assert rec["cores"] == rec["threads"] == rec["host_cores"] == bench.host_cores()
+    assert rec["value"] > 0 and rec["single_thread"]["threads"] == 1 and rec["single_thread"]["value"] > 0
+
+
+def test_expert_load_record():
+    ids = np.array([[[0, 1], [0, 2], [0, 1]]], dtype=np.int32)  # one layer, 3 tokens, top-2
+    rec = bench.expert_load(ids)
+    assert rec["experts_touched"] == 3 and rec["max_tokens_per_expert"] == 3
+    assert rec["mean_tokens_per_touched_expert"] == 2.0 and rec["max_over_mean"] == 1.5
+    assert rec["tokens_per_expert_sorted"] == [3, 2, 1]
+
+
+def test_step_tensor_fraction_counts_expert_and_router_flops():
+    rec = bench.step_tensor_fraction({"T": 8192, "L": 48}, 100.0)
+    assert rec["flops_per_step"] == 48 * 8192 * (10 * 9830400 + 2 * 512 * 2560)

@@ -13,8 +13,8 @@ import torch
 import gen
 import oracle
 import quantized_routed_expert_top10_gb300 as qre
-from gpu_common import (W_TOL, DEV, B, BlobCache, check_close, check_routing, device_packed_layer, run_layer, to_dev,
-                        workspace)
+from gpu_common import (W_TOL, DEV, B, BlobCache, check_close, check_routing, device_packed_layer, run_layer,
+                        stratified_sample, to_dev, workspace)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 L = 48
@@ -81,15 +81,19 @@ def test_config2_decode_stack_48_layers(arena):
 
 
 def test_config3_prefill_2048(arena):
+    """All 2,048 tokens' routing; outputs of the first and last token of every prefill tile of every
+    expert (every gate/up tile class and every down tile)."""
     cfg = gen.config_inputs(3)
     x, wr, bias = cfg["x"], cfg["wr"][0], cfg["bias"][0]
     out, ids, w = run_layer(arena[:E * B], wr, bias, x)
     r = oracle.route(x, wr, bias)
     ties = check_routing(ids, r["ids"], r["logits"])
     counts = np.bincount(ids.reshape(-1), minlength=E)
+    sample, n_exp, per_cls = stratified_sample(ids)
     print(f"config 3: {ties} tie tokens; experts touched {np.count_nonzero(counts)}; "
-          f"max/mean load {counts.max()}/{counts[counts > 0].mean():.1f}")
-    sample = np.random.default_rng(3).choice(2048, 48, replace=False)
+          f"max/mean load {counts.max()}/{counts[counts > 0].mean():.1f}; outputs checked for {sample.size} tokens "
+          f"covering {n_exp} experts and tiles {per_cls}")
+    assert n_exp == np.count_nonzero(counts)
     cache = BlobCache(0)
     ref = oracle.moe_layer(x[sample], wr, bias, cache.layer_list(0, ids[sample]), ids_in=ids[sample])
     check_close(out[sample], ref["out"], "config 3 sampled outputs")
@@ -97,26 +101,58 @@ def test_config3_prefill_2048(arena):
 
 
 def test_config4_prefill_8192_stack_sampled(arena):
+    """Every layer: routing of 256 random tokens, and outputs of 64 tokens chosen from the layer's own
+    tiles (the first and last tile of each class, then experts in an order rotated per layer), with
+    the GPU's own layer inputs."""
     T = 8192
     cfg = gen.config_inputs(4)
     rng = np.random.default_rng(4)
-    route_sample = np.sort(rng.choice(T, 64, replace=False))
-    out_sample = route_sample[:4]
+    route_sample = np.sort(rng.choice(T, 256, replace=False))
+    rs = torch.from_numpy(route_sample).to(DEV)
     ws = workspace(T)
     xl = to_dev(cfg["x"])
     idl = torch.empty(T, 10, dtype=torch.int32, device=DEV)
     cache = BlobCache(0)
-    ties = 0
+    ties, n_checked, experts_seen = 0, 0, set()
     for l in range(L):
-        x_in = xl[torch.from_numpy(route_sample).to(DEV)].cpu().numpy()
+        x_before = xl.clone()
         qre.strata_moe_layer(layer_experts(arena, l), to_dev(cfg["wr"][l]), to_dev(cfg["bias"][l]), xl, T,
                              qre.RESIDUAL_RMSNORM, xl, idl, None, ws)
-        x_out = xl[torch.from_numpy(route_sample).to(DEV)].cpu().numpy()
-        ids = idl[torch.from_numpy(route_sample).to(DEV)].cpu().numpy()
-        r = oracle.route(x_in, cfg["wr"][l], cfg["bias"][l], residual=True)
-        ties += check_routing(ids, r["ids"], r["logits"])
-        ref = oracle.moe_layer(x_in[:4], cfg["wr"][l], cfg["bias"][l], cache.layer_list(l, ids[:4]),
-                               residual=True, ids_in=ids[:4])
-        check_close(x_out[:4] - x_in[:4], ref["out"] - x_in[:4].astype(np.float64), f"layer {l}")
+        ids_all = idl.cpu().numpy()
+        r = oracle.route(x_before[rs].cpu().numpy(), cfg["wr"][l], cfg["bias"][l], residual=True)
+        ties += check_routing(ids_all[route_sample], r["ids"], r["logits"])
+        sample, _, _ = stratified_sample(ids_all, budget=64, rotate=37 * l)
+        st = torch.from_numpy(sample).to(DEV)
+        x_in, x_out = x_before[st].cpu().numpy(), xl[st].cpu().numpy()
+        ids = ids_all[sample]
+        experts_seen.update((l, int(e)) for e in np.unique(ids))
+        ref = oracle.moe_layer(x_in, cfg["wr"][l], cfg["bias"][l], cache.layer_list(l, ids), residual=True,
+                               ids_in=ids)
+        check_close(x_out - x_in, ref["out"] - x_in.astype(np.float64), f"layer {l}")
+        n_checked += sample.size
+        for key in [k for k in cache.cache if k[0] == l]:
+            del cache.cache[key]
     assert qre.strata_poll_status(ws) == 0
-    print(f"config 4: {ties} tie tokens among {64 * L} checked token-layers")
+    print(f"config 4: {ties} tie tokens among {256 * L} routed token-layers; outputs of {n_checked} token-layers "
+          f"checked, {len(experts_seen)} (layer, expert) pairs")
+
+
+@pytest.mark.parametrize("T,n_layers", [(300, 3), (8192, 2)])
+def test_prefill_stack_equals_layer_chain(arena, T, n_layers):
+    """strata_moe_stack for a prefill chunk (the call the long-prefill benchmark times) gives the same
+    bits as the same layers run one strata_moe_layer call at a time."""
+    cfg = gen.config_inputs(4, T=T, L=n_layers)
+    wr_d, bias_d = to_dev(np.stack(cfg["wr"])), to_dev(np.stack(cfg["bias"]))
+    exs = [layer_experts(arena, l) for l in range(n_layers)]
+    ws = workspace(T)
+    xs = to_dev(cfg["x"])
+    ids_s = torch.empty(n_layers, T, 10, dtype=torch.int32, device=DEV)
+    qre.strata_moe_stack(exs, wr_d, bias_d, n_layers, xs, T, ids_s, None, ws)
+    assert qre.strata_poll_status(ws) == 0
+    xl = to_dev(cfg["x"])
+    idl = torch.empty(T, 10, dtype=torch.int32, device=DEV)
+    for l in range(n_layers):
+        qre.strata_moe_layer(exs[l], wr_d[l], bias_d[l], xl, T, qre.RESIDUAL_RMSNORM, xl, idl, None, ws)
+        np.testing.assert_array_equal(ids_s[l].cpu().numpy(), idl.cpu().numpy())
+    assert qre.strata_poll_status(ws) == 0
+    np.testing.assert_array_equal(xs.cpu().numpy(), xl.cpu().numpy())

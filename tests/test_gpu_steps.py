@@ -110,6 +110,37 @@ def layer0():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("bad", ["duplicate_active", "overlapping_ranges", "descending_active"])
+def test_experts_reject_inconsistent_grouping(layer0, bad):
+    """A caller's grouping whose active list repeats an expert, runs backwards, or whose slot ranges
+    overlap would make the tile list run past the workspace's padded rows: the device check finds it
+    before any expert work, sets STRATA_E_CORRUPT and the call leaves parts untouched."""
+    blobs, _ = layer0
+    T = 12
+    ids = _random_ids(T, 7, skew=False)
+    off, pair, active = oracle.group(ids, 512)
+    off, active = off.copy(), active.copy()
+    na = active.size
+    if bad == "duplicate_active":
+        active = np.concatenate([active[:1], active])[:512].astype(np.int32)
+        na = min(na + 1, 512)
+    elif bad == "descending_active":
+        active = active[::-1].copy()
+    else:  # an active expert's range is stretched into the next active expert's
+        i = int(np.flatnonzero(np.diff(active) > 1)[0])
+        off[int(active[i]) + 1] = off[int(active[i + 1])] + 1
+    ws = workspace(T)
+    parts = torch.full((T, 10, qre.H), 3.5, dtype=torch.float32, device=DEV)
+    act = torch.zeros(512, dtype=torch.int32, device=DEV)
+    act[:active.size] = to_dev(active.astype(np.int32))
+    qre.strata_moe_experts(qre.experts(blobs), to_dev(gen.activations_fast(3, T)), T, to_dev(off), to_dev(pair), act,
+                           to_dev(np.array([na], dtype=np.int32)), parts, ws)
+    assert qre.strata_poll_status(ws) == -7
+    assert bool(torch.all(parts == 3.5))
+    qre.strata_clear_status(ws)
+    assert qre.strata_poll_status(ws) == 0
+
+
 @pytest.mark.parametrize("T", [4, 37])
 def test_experts_and_combine_steps(layer0, T):
     blobs, cache = layer0

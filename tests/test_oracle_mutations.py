@@ -70,6 +70,12 @@ MUTATIONS = [
     ("router_on_raw_input",
      "oracle_router_logits(xn, H, E, j->w_router, j->bias, logits);\n  if (j->ids_in)",
      "oracle_router_logits(xin, H, E, j->w_router, j->bias, logits);\n  if (j->ids_in)"),
+    ("route_tokens_rmsnorm_dropped",
+     "if (j->residual) oracle_rmsnorm(xn, j->H, 1e-6, xn);",
+     "(void)0;"),
+    ("route_tokens_bias_dropped",
+     "oracle_router_logits(xn, j->H, j->E, j->w_router, j->bias, logits);\n    oracle_top_k",
+     "oracle_router_logits(xn, j->H, j->E, j->w_router, NULL, logits);\n    oracle_top_k"),
     ("combine_unweighted",
      "for (int h = 0; h < H; ++h) acc[h] += w[k] * y[h];",
      "for (int h = 0; h < H; ++h) acc[h] += y[h];"),

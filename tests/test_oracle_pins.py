@@ -277,6 +277,73 @@ def test_weights_for_ids_matches_top_k():
     np.testing.assert_allclose(oracle.weights_for_ids(l, perm), w[::-1], rtol=1e-15)
 
 
+def _dense_route(x, wr, bias, residual, K):
+    """Independent route: rmsnorm and logits with numpy in float64, then a stable descending argsort of
+    the softmax (the first K), renormalised."""
+    xd = x.astype(np.float64)
+    if residual:
+        xd = xd / np.sqrt(np.mean(xd * xd, axis=1, keepdims=True) + 1e-6)
+    l = xd @ gen.bf16_bits_to_f32(wr).astype(np.float64).T
+    if bias is not None:
+        l = l + bias.astype(np.float64)
+    p = np.exp(l - l.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    ids = np.argsort(-p, axis=1, kind="stable")[:, :K]
+    w = np.take_along_axis(p, ids, axis=1)
+    return ids, w / w.sum(axis=1, keepdims=True), l
+
+
+@pytest.mark.parametrize("residual", [False, True])
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("H,E,K,T", [(64, 8, 2, 6), (2560, 512, 10, 2)])
+def test_route_tokens_against_numpy(H, E, K, T, residual, with_bias):
+    """oracle.route (the routing every GPU check compares with): rmsnorm on residual layers, the bias
+    added, and the top-K of the softmax, against a dense numpy evaluation.  x is scaled by 3 so a
+    dropped rmsnorm changes the logits."""
+    x = (3.0 * gen.activations(H + T, T, H_=H)).astype(np.float32)
+    wr = gen.router_weights(1, 0, E_=E, H_=H)
+    bias = gen.zipf_bias(1, 0, E_=E) if with_bias else None
+    r = oracle.route(x, wr, bias, residual=residual, K=K)
+    ids, w, l = _dense_route(x, wr, bias, residual, K)
+    np.testing.assert_allclose(r["logits"], l, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(r["ids"], ids)
+    np.testing.assert_allclose(r["w"], w, rtol=1e-12)
+
+
+@pytest.mark.parametrize("residual", [False, True])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_route_tokens_equal_the_layer_routing(residual, with_bias):
+    """oracle.route and the routing inside oracle.moe_layer are separate code: the same bits."""
+    H, E, FF, K, T = 64, 8, 16, 2, 7
+    x, wr, blobs = _tiny_layer_inputs(T)
+    x = (2.5 * x).astype(np.float32)
+    bias = gen.zipf_bias(0, 0, E_=E) if with_bias else None
+    r = oracle.route(x, wr, bias, residual=residual, K=K)
+    m = oracle.moe_layer(x, wr, bias, blobs, K=K, residual=residual)
+    np.testing.assert_array_equal(r["ids"], m["ids"])
+    np.testing.assert_array_equal(r["w"], m["w"])
+    np.testing.assert_array_equal(r["logits"], m["logits"])
+
+
+def test_route_one_hot_gives_the_router_column_plus_bias():
+    wr = gen.router_weights(0, 0, E_=64, H_=128)
+    bias = gen.zipf_bias(0, 0, E_=64)
+    x = np.zeros((3, 128), dtype=np.float32)
+    cols = (0, 77, 127)
+    for t, h in enumerate(cols):
+        x[t, h] = 1.0
+    r = oracle.route(x, wr, bias, K=10)
+    for t, h in enumerate(cols):
+        want = gen.bf16_bits_to_f32(wr[:, h]).astype(np.float64) + bias.astype(np.float64)
+        np.testing.assert_array_equal(r["logits"][t], want)
+    # residual: rmsnorm of a one-hot vector is the one-hot vector times 1/sqrt(1/H + 1e-6)
+    r = oracle.route(x, wr, None, residual=True, K=10)
+    s = 1.0 / math.sqrt(1.0 / 128 + 1e-6)
+    for t, h in enumerate(cols):
+        np.testing.assert_allclose(r["logits"][t], gen.bf16_bits_to_f32(wr[:, h]).astype(np.float64) * s,
+                                   rtol=1e-14, atol=0)
+
+
 # ---------------------------------------------------------------------------------------------
 # grouping
 # ---------------------------------------------------------------------------------------------
