@@ -157,7 +157,12 @@ strata_status strata_moe_combine(const float* parts, const float* weights, int32
 
 /* Steps 1-5 for one layer. flags = 0: out = moe(x); flags = STRATA_MOE_RESIDUAL_RMSNORM: out =
  * x + moe(rmsnorm(x)) with router and experts both reading rmsnorm(x).  out may alias x.  ids /
- * weights (nullable) receive the routing.  Workspace as for any call with T tokens. */
+ * weights (nullable) receive the routing.  Workspace as for any call with T tokens.
+ * Summation order: for T <= 8 the ten weighted expert outputs of a token are added in k order and
+ * repeated calls give the same bits.  For T > 8 the combine is fused into the down projection: out is
+ * first set to x (residual layers) or 0, and each expert's weighted output is added into it with fp32
+ * atomic additions as the expert finishes, so the order of a token's ten additions -- and the last
+ * bits of out -- can differ from call to call (the routing, computed before, does not). */
 strata_status strata_moe_layer(const strata_experts_t* ex, const uint16_t* w_router, const float* bias,
                                const float* x, int32_t T, int32_t flags, float* out, int32_t* ids,
                                float* weights, void* ws, size_t ws_bytes, void* stream);
@@ -251,7 +256,9 @@ const char* strata_status_str(strata_status s);
  * Kernel ids (every kernel the library launches): */
 #define STRATA_KERNEL_DECODE_LAYER 0   /* whole layer for T <= 8, one cooperative launch */
 #define STRATA_KERNEL_ROUTE_DECODE 1   /* router GEMV + top-10 + grouping, T <= 8 (strata_moe_route) */
-#define STRATA_KERNEL_ROUTER_PREP 2    /* bf16 hi/lo copies of x for the router GEMM (and 1/rms), T > 8 */
+#define STRATA_KERNEL_ROUTER_PREP 2    /* bf16 hi/lo copies of x for the router GEMM (and 1/rms), T > 8; in a layer call
+                                          also the experts' fp16 token copy and the output's initial value
+                                          (strata_moe_experts: the fp16 token copy alone) */
 #define STRATA_KERNEL_ROUTER_TC 3      /* router GEMM on the tensor cores, T > 8 */
 #define STRATA_KERNEL_TOP_K 4
 #define STRATA_KERNEL_GROUP_HIST 5
@@ -260,8 +267,8 @@ const char* strata_status_str(strata_status s);
 #define STRATA_KERNEL_TC_PREPARE 8     /* tile list of the tensor-core expert path */
 #define STRATA_KERNEL_TC_GATHER 9      /* fp16 token gather per expert */
 #define STRATA_KERNEL_TC_GATEUP 10     /* Q2_0 gate/up + SwiGLU grouped GEMM (tcgen05) */
-#define STRATA_KERNEL_TC_DOWN 11       /* Q2_0 down grouped GEMM (tcgen05) */
-#define STRATA_KERNEL_COMBINE 12
+#define STRATA_KERNEL_TC_DOWN 11       /* Q2_0 down grouped GEMM (tcgen05); in a layer call also the combine */
+#define STRATA_KERNEL_COMBINE 12       /* strata_moe_combine */
 #define STRATA_KERNEL_PACK 13
 #define STRATA_KERNEL_HOST_COPY 14     /* copy between page-locked host memory and the workspace (host-buffer calls) */
 #define STRATA_KERNEL_WAIT_SELFTEST 15 /* strata_moe_wait_selftest */

@@ -47,16 +47,18 @@ strata_status check_experts(const strata_experts_t* ex) {
 
 // Steps 1-3 for T tokens into the workspace (ids/weights to the given pointers). Also leaves the
 // quantised expert input in ws.qx.  Reads x (rmsnorm applied first when `norm`).
+// For a prefill layer (T > DECODE_T_MAX) the router's prep pass also writes the expert path's fp16 token
+// copy and initialises out (x for residual layers, else zeros) for the fused combine.
 strata_status route_and_group(const float* x, int T, int norm, const uint16_t* w_router, const float* bias, int E,
                               int q2_offset, int32_t* ids, float* weights, float* logits_user,
-                              const WsLayout& L, char* ws, cudaStream_t s) {
+                              const WsLayout& L, char* ws, cudaStream_t s, float* out = nullptr) {
   if (T <= DECODE_T_MAX) {
     STRATA_CUDA(launch_route_decode(x, T, norm, w_router, bias, E, q2_offset, ids, weights, logits_user, L, ws, s));
     return STRATA_OK;
   }
   float* lparts = (float*)(ws + L.logits);
   STRATA_CUDA(launch_router_tc(x, norm ? (float*)(ws + L.inv_rms) : nullptr, T, w_router, E, ws + L.xbf, lparts,
-                               (int*)(ws + L.status), s));
+                               (int*)(ws + L.status), s, out ? (uint8_t*)(ws + L.x16) : nullptr, out));
   STRATA_CUDA(launch_top_k(lparts, T, E, bias, logits_user, ids, weights, s));
   STRATA_CUDA(launch_group(ids, T, E, (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair),
                            (int32_t*)(ws + L.active), nullptr, L, ws, s));
@@ -84,14 +86,13 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
     STRATA_CUDA(launch_decode_fused(*ex, w_router, bias, x, T, norm, alias, out, ids_d, wts_d, next, L, w, s));
     return STRATA_OK;
   }
-  STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s));
-  float* parts = (float*)(w + L.parts);
-  const float* inv = norm ? (const float*)(w + L.inv_rms) : nullptr;
-  STRATA_CUDA(launch_experts_tc(*ex, x, inv, T, (const int32_t*)(w + L.expert_off), (const int32_t*)(w + L.pair),
-                                (const int32_t*)(w + L.active), (const int32_t*)(w + L.n_active), parts,
-                                (uint8_t*)(w + L.xg), (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta),
-                                (int*)(w + L.status), s));
-  STRATA_CUDA(launch_combine(parts, wts_d, T, norm ? x : nullptr, out, s));
+  STRATA_TRY(route_and_group(x, T, norm, w_router, bias, ex->n_expert, ex->q2_offset, ids_d, wts_d, nullptr, L, w, s,
+                             out));
+  STRATA_CUDA(launch_experts_tc(*ex, (const uint8_t*)(w + L.x16), T, (const int32_t*)(w + L.expert_off),
+                                (const int32_t*)(w + L.pair), (const int32_t*)(w + L.active),
+                                (const int32_t*)(w + L.n_active), nullptr, wts_d, out, (uint8_t*)(w + L.xg),
+                                (uint8_t*)(w + L.hg),
+                                (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
   return STRATA_OK;
 }
 
@@ -180,8 +181,10 @@ strata_status strata_moe_experts(const strata_experts_t* ex, const float* x, int
   const WsLayout L = ws_layout(T);
   char* w = (char*)ws;
   cudaStream_t s = (cudaStream_t)stream;
-  STRATA_CUDA(launch_experts_tc(*ex, x, nullptr, T, expert_off, pair, active, n_active, parts, (uint8_t*)(w + L.xg),
-                                (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
+  STRATA_CUDA(launch_x16(x, nullptr, T, (uint8_t*)(w + L.x16), s));
+  STRATA_CUDA(launch_experts_tc(*ex, (const uint8_t*)(w + L.x16), T, expert_off, pair, active, n_active, parts,
+                                nullptr, nullptr, (uint8_t*)(w + L.xg), (uint8_t*)(w + L.hg), (uint8_t*)(w + L.tcmeta),
+                                (int*)(w + L.status), s));
   return STRATA_OK;
 }
 

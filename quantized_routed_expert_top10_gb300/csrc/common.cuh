@@ -104,9 +104,9 @@ struct WsLayout {
   size_t chunk_cnt;   // int32 [n_chunks][EMAX]
   size_t qx;          // QBlock [T][KB_GU] quantised layer input (T <= DECODE_T_MAX routing kernel)
   size_t xpp;         // fp32 [T][H] (T <= DECODE_T_MAX): the other buffer of a decode stack's ping-pong
-  size_t parts;       // fp32 [T*K][H]
-  size_t xg;          // tensor-core expert path: gathered fp16 tokens [KB_GU][rows][128 B]
-  size_t hg;          //                                      fp16 h [KB_D][rows][128 B]
+  size_t x16;         // tensor-core expert path: fp16 token copy [KB_GU][T][128 B]
+  size_t xg;          //                          the same per padded slot, swizzled [KB_GU][rows][128 B]
+  size_t hg;          //                          fp16 h per padded slot, swizzled [KB_D][rows][128 B]
   size_t tcmeta;      //                                      expert ranges, tiles, counts
   size_t io;          // fp32 [2][T][H]: device copies of a host-buffer call's input and output
   size_t total;
@@ -126,6 +126,7 @@ inline int max_tiles_for(int T) {
 
 // Sizes of the tensor-core path's buffers (experts_tc.cu).
 int64_t tc_rows_cap(int T);
+size_t tc_x16_bytes(int T);
 size_t tc_xg_bytes(int T);
 size_t tc_hg_bytes(int T);
 size_t tc_meta_bytes(int T);
@@ -153,7 +154,7 @@ inline WsLayout ws_layout(int T) {
   L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.n_chunks * EMAX);
   L.qx = take(sizeof(QBlock) * (size_t)T * KB_GU);
   L.xpp = take(T <= DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);
-  L.parts = take(sizeof(float) * (size_t)P * H);
+  L.x16 = take(tc_x16_bytes(T));
   L.xg = take(tc_xg_bytes(T));
   L.hg = take(tc_hg_bytes(T));
   L.tcmeta = take(tc_meta_bytes(T));
@@ -298,17 +299,29 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
                                 const float* bias, int E, int q2_offset, int32_t* ids, float* weights,
                                 float* logits_out, const WsLayout& L, char* ws, cudaStream_t s);
 // Router logits of a prefill chunk: bf16 hi/lo copies of x (times 1/rms, written to inv_rms, when it is
-// non-null) in xbf, then the tensor-core GEMM into the partial-logit slices.
+// non-null) in xbf, then the tensor-core GEMM into the partial-logit slices.  A layer call also passes
+// x16 (receives the expert path's fp16 token copy, with the same 1/rms) and out (receives x when inv_rms
+// is non-null -- the residual -- else zeros, for the down kernel to add the experts' outputs into).
 cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16_t* w_router, int E, void* xbf,
-                             float* parts, int* status, cudaStream_t s);
+                             float* parts, int* status, cudaStream_t s, uint8_t* x16 = nullptr,
+                             float* out = nullptr);
 cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, float* logits_out, int32_t* ids,
                          float* weights, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, int32_t* pair,
                          int32_t* active, int32_t* n_active, const WsLayout& L, char* ws, cudaStream_t s);
-cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
-                              const int32_t* expert_off, const int32_t* pair, const int32_t* active,
-                              const int32_t* n_active, float* parts,
-                              uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s);
+// A 2-D tensor map (CUtensorMap, 64-byte aligned storage) over a row-major matrix of `rows` rows of
+// `inner` elements of CUtensorMapDataType `dtype`, rows row_stride bytes apart; boxes of box_inner x
+// box_rows elements, 128-byte swizzle, out-of-range elements read as zeros.  False if encoding fails.
+bool make_tensor_map_2d(void* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                        uint32_t box_inner, uint32_t box_rows);
+// fp16 token copy X16 of x (times inv_rms[t] when non-null) for the tensor-core expert path.
+cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s);
+// Tile lists, then the gate/up and down kernels over the grouping.  out == null: y of every pair into
+// parts [T*K][H]; otherwise out[t] += weights[t][k] * y (out already holds the residual or zeros).
+cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, int T, const int32_t* expert_off,
+                              const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
+                              const float* weights, float* out, uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status,
+                              cudaStream_t s);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
 // The next layer of a decode stack, for the lookahead (its router on this layer's input predicts its

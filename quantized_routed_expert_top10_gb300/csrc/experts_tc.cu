@@ -3,29 +3,33 @@
 // momoyeyu.github.io "ai-infra-strata", section "提示词处理": a prompt is cut into chunks, tokens are
 // gathered per expert so one weight read serves all of them (W x becomes W X), and the kernel fuses
 // the dequantisation with the matrix product.  ai.thesatyajit.com "Strata engine", "The CPU kernels":
-// Q2_0 codes {0,1,2,3} mean {-1,0,1,2} x the block scale.
+// Q2_0 codes {0,1,2,3} mean {-1,0,1,2} x the block scale.  zwxr.cn news/242664, "一次路由的完整旅程":
+// moe_combine adds the experts' outputs weighted by the router weights.
 //
 // Per expert e with n_e tokens (its slots in the grouping), two grouped GEMMs with the weights as the
 // M = 128 operand ("swap AB") and the expert's tokens as N (up to 256 per tile):
 //   gate/up:  [g; u] (2 x 128 rows x N) = [G_rt; U_rt] (128 x 2560) * X_e^T, h = silu(g) * u -> Hg (fp16)
-//   down:     [y_2rp; y_2rp+1] (2 x 128 rows x N) = [D_2rp; D_2rp+1] (128 x 640 each) * H_e^T
-//             -> parts[pair][row] (fp32); two row tiles per item so each token tile is read half as often
+//   down:     [y_2rp; y_2rp+1] (2 x 128 rows x N) = [D_2rp; D_2rp+1] (128 x 640 each) * H_e^T; two row
+//             tiles per item so each token tile is read half as often.  In a layer call the epilogue
+//             adds w[t][k] * y into the layer output (fp32 reductions: the combine step, fused), so no
+//             per-pair output is stored; strata_moe_experts stores y per pair instead.
 // Warp roles in each persistent CTA (one per SM; work items = (tile, 128-row tile of the weights)):
-//   warp 0      streams the token tile and the Q2_0 code chunk of each 64-wide k-block with
-//               cp.async.bulk into a 4-stage (gate/up) or 6-stage (down) ring;
+//   warp 0      streams the token tile (gate/up: from Xg, the tokens copied once per layer into padded-slot
+//               order by tc_gather_kernel; down: from Hg) and the Q2_0 code chunk of each 64-wide
+//               k-block with cp.async.bulk into a 4-stage (gate/up) or 6-stage (down) ring;
+//   warp 2      owns the TMEM allocation;
 //   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
 //               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
 //               exact) in a 2-stage ring of weight tiles;
 //   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (one half for a tile of up to 128
 //               tokens, both for a wider one) and commits to the stages' "empty" mbarriers;
 //   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
-//               epilogue while the next item accumulates into the other buffer;
-//   warp 2      owns the TMEM allocation.
+//               epilogue while the next item accumulates into the other buffer.
 // Every wait is bounded (STRATA_E_TIMEOUT).
 //
 // In-block order: the dequantiser emits the 64 weights of a block in the order pi (per 16 weights:
 // 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15), which is what one LOP3 per half2 produces from the packed
-// codes; the gathered tokens Xg and h (Hg) are stored in the same order, so every dot product is the
+// codes; the token copy X16 and h (Hg) are stored in the same order, so every dot product is the
 // same sum.
 #include "tc_common.cuh"
 
@@ -139,60 +143,64 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   }
 }
 
+// X16 (see x16_store_chunk) of x for strata_moe_experts, times inv_rms[t] when given: one warp per
+// token row.  A layer call gets X16 from the router's prep pass instead.
 // ---------------------------------------------------------------------------------------------
-// Xg[kb][row][128 B]: row = padded slot; fp16 x of the slot's token (times its 1/rms for residual
-// layers) in pi order, swizzled by row % 8; rows past an expert's tokens are zero.  One warp per
-// padded row (the expert found by binary search over the experts' first rows, staged in shared
-// memory); lane = (k-block within a group of 4, 16-byte chunk), so a warp reads 1 KB of x contiguously.
-// Chunk c of a 64-block holds weights {0,8,1,9,2,10,3,11} (c even) or {4,12,5,13,6,14,7,15} (c odd)
-// of the block's 16-group c / 2: two float4 loads.
+__global__ void __launch_bounds__(256) tc_x16_kernel(const float* __restrict__ x, const float* __restrict__ inv_rms,
+                                                     int T, uint8_t* __restrict__ x16) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
+  const float sc = inv_rms ? __ldg(inv_rms + t) : 1.f;
+#pragma unroll 4
+  for (int i = 0; i < H / 128; ++i) tc::x16_store_chunk(__ldg(xr + lane + 32 * i), i, sc, t, T, x16);
+}
+
+// Xg[kb][row][128 B]: the padded-slot copy of the tokens the gate/up kernel bulk-copies its token tiles
+// from (one contiguous run of rows per tile and k-block): row q0pad(e) + s of expert e holds X16 row
+// (kb, token of the expert's slot s), its 16-byte chunks swizzled by row % 8 (the tensor core's 128B
+// K-major layout, so a bulk copy of a row range is an MMA operand as it lands).  One warp per slot (the
+// expert found by binary search over the experts' first slots, staged in shared memory); lane = (k-block
+// within a group of 4, chunk), so a warp moves four whole 128-byte rows per instruction.  Rows of the
+// 8-row padding between experts are not written: they only feed MMA columns the epilogues discard.
 // ---------------------------------------------------------------------------------------------
 constexpr int GATHER_THREADS = 256;
-constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over rows; 4 CTAs per SM of a 152-SM GB300
-__global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const float* __restrict__ x,
-                                                                   const float* __restrict__ inv_rms,
+constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over slots; 4 CTAs per SM of a 152-SM GB300
+__global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t* __restrict__ x16, int T,
                                                                    const int32_t* __restrict__ pair, int P,
                                                                    const TcExpert* __restrict__ exps,
                                                                    const int32_t* __restrict__ counts,
                                                                    uint8_t* __restrict__ xg, int64_t rows_cap,
                                                                    int* __restrict__ status) {
-  __shared__ int s_row0[EMAX];
-  const int na = counts[0], ppad = counts[2];
-  for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_row0[i] = exps[i].q0pad;
+  __shared__ int s_q0[EMAX];
+  const int na = counts[0];
+  for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_q0[i] = exps[i].q0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (GATHER_THREADS / 32);
-  for (int r = blockIdx.x * (GATHER_THREADS / 32) + (threadIdx.x >> 5); r < ppad && r < rows_cap; r += warps) {
-    int lo = 0, hi = na - 1;  // last expert whose first row is <= r
+  const int nslots = na > 0 ? exps[na - 1].q0 + exps[na - 1].n : 0;
+  for (int j = blockIdx.x * (GATHER_THREADS / 32) + (threadIdx.x >> 5); j < nslots; j += warps) {
+    int lo = 0, hi = na - 1;  // last expert whose first slot is <= j
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_row0[mid] <= r) lo = mid;
+      if (s_q0[mid] <= j) lo = mid;
       else hi = mid - 1;
     }
     const TcExpert ex = exps[lo];
-    const int s = r - ex.q0pad;
-    int t = -1;
-    if (s < ex.n) {
-      const int pr = pair[ex.q0 + s];
-      if (pr >= 0 && pr < P) t = pr / K;
-      else if (lane == 0) set_status(status, ST_CORRUPT);  // a caller's bad pair: zero row, no write
+    const int64_t row = ex.q0pad + (j - ex.q0);
+    if (j - ex.q0 >= ex.n || row >= rows_cap) continue;  // cannot happen for a checked grouping
+    const int pr = pair[j];
+    if (pr < 0 || pr >= P) {  // a caller's bad pair: its row is left as it is (a wrong but finite column)
+      if (lane == 0) set_status(status, ST_CORRUPT);
+      continue;
     }
-    const float sc = (t >= 0 && inv_rms) ? __ldg(inv_rms + t) : 1.f;
-    const int c = lane & 7, odd = c & 1;
-#pragma unroll 2
-    for (int kb = lane >> 3; kb < KB_GU; kb += 4) {
-      uint4 out = make_uint4(0, 0, 0, 0);
-      if (t >= 0) {
-        const float* src = x + (size_t)t * H + kb * QK + 16 * (c >> 1) + 4 * odd;
-        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(src + 8));
-        const __half2 h0 = __floats2half2_rn(a.x * sc, b.x * sc), h1 = __floats2half2_rn(a.y * sc, b.y * sc);
-        const __half2 h2 = __floats2half2_rn(a.z * sc, b.z * sc), h3 = __floats2half2_rn(a.w * sc, b.w * sc);
-        out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
-                         *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
-      }
-      *reinterpret_cast<uint4*>(xg + ((int64_t)kb * rows_cap + r) * 128 + ((c ^ (r & 7)) << 4)) = out;
-    }
+    const int t = pr / K, c = lane & 7;
+    const uint8_t* src = x16 + (size_t)t * 128 + 16 * c;
+    uint8_t* dst = xg + row * 128 + ((c ^ (int)(row & 7)) << 4);
+#pragma unroll 5
+    for (int kb = lane >> 3; kb < KB_GU; kb += 4)
+      *reinterpret_cast<uint4*>(dst + (int64_t)kb * rows_cap * 128) =
+          __ldg(reinterpret_cast<const uint4*>(src + (size_t)kb * T * 128));
   }
 }
 
@@ -230,16 +238,19 @@ struct TcParams {
   int q2_offset;
   const TcTile* tiles;
   const int32_t* counts;
-  const uint8_t* act;   // gate/up: Xg; down: Hg
+  const uint8_t* act;   // gate/up: Xg [KB_GU][rows_cap][128 B]; down: Hg [KB_D][rows_cap][128 B]
   uint8_t* hg;          // gate/up output
   int64_t rows_cap;
-  const int32_t* pair;  // down: slot -> pair
+  const int32_t* pair;  // slot -> pair
+  int T;                // tokens
   int P;                // pairs (T * K)
-  float* parts;         // down output
+  float* parts;         // down output per pair (strata_moe_experts), or null
+  const float* wts;     // down, fused combine: router weights [T][K] (pair-indexed)
+  float* out;           //                      layer output [T][H], already holding x (residual) or 0
   int* status;
 };
 
-// Kernel geometry.  Warp 0: bulk-copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
+// Kernel geometry.  Warp 0: copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
 // dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each);
 // warps 12..15: epilogue (one TMEM lane = one weight row per thread).
 // gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
@@ -285,6 +296,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
   __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
+  __shared__ int s_ep_pair[GU ? 1 : TCN_HALF];   // down epilogue: pair of each column of the current tile
+  __shared__ float s_ep_w[GU ? 1 : TCN_HALF];     //                router weight of that pair (fused combine)
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -483,6 +496,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
           }
         }
       } else {
+        // the tile's pairs (and router weights) staged once per item by the 128 epilogue threads
+        named_barrier(2, 128);  // every epilogue thread is done with the previous item's
+        if (erow < tl.n) {
+          int pr = __ldg(p.pair + tl.q0 + erow);
+          if (pr < 0 || pr >= p.P) pr = -1;
+          s_ep_pair[erow] = pr;
+          if (p.out) s_ep_w[erow] = pr >= 0 ? __ldg(p.wts + pr) : 0.f;
+        }
+        named_barrier(2, 128);
         const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
         for (int ch = 0; ch < nrows / 16; ++ch) {
           float y0[16], y1[16];
@@ -492,11 +514,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = 16 * ch + i;
-              const int pr = col < tl.n ? p.pair[tl.q0 + col] : -1;
-              if (pr >= 0 && pr < p.P) {
-                float* dst = p.parts + (size_t)pr * H + orow;
-                dst[0] = y0[i];
-                dst[128] = y1[i];
+              const int pr = col < tl.n ? s_ep_pair[col] : -1;
+              if (pr >= 0) {
+                if (p.out) {  // fused combine: out[t] += w[t][k] * y
+                  const float w = s_ep_w[col];
+                  float* dst = p.out + (size_t)(pr / K) * H + orow;
+                  tc::red_add_f32(dst, w * y0[i]);
+                  tc::red_add_f32(dst + 128, w * y1[i]);
+                } else {
+                  float* dst = p.parts + (size_t)pr * H + orow;
+                  dst[0] = y0[i];
+                  dst[128] = y1[i];
+                }
               }
             }
           }
@@ -523,19 +552,25 @@ int g_sms[64];
 
 }  // namespace
 
-// Rows of the padded, gathered token buffers for a call with T tokens (every expert's slot range
-// rounded up to 8 rows, plus 128 rows of slack for the last tile's over-read).
+// Rows of the padded h buffer Hg for a call with T tokens (every expert's slot range rounded up to 8
+// rows, plus a tile's width of slack for the last tile's over-read).
 int64_t tc_rows_cap(int T) { return (int64_t)T * K + 8 * EMAX + TCN; }
+size_t tc_x16_bytes(int T) { return (size_t)KB_GU * T * 128; }
 size_t tc_xg_bytes(int T) { return (size_t)KB_GU * tc_rows_cap(T) * 128; }
 size_t tc_hg_bytes(int T) { return (size_t)KB_D * tc_rows_cap(T) * 128; }
 size_t tc_meta_bytes(int T) {
   return sizeof(TcExpert) * EMAX + sizeof(TcTile) * (size_t)(T * K / TCN + EMAX + T * K / TCN_HALF + EMAX) + 64;
 }
 
-cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const float* inv_rms, int T,
-                              const int32_t* expert_off,
+cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s) {
+  STRATA_LAUNCH(KID_ROUTER_PREP, s, tc_x16_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, inv_rms, T, x16));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, int T, const int32_t* expert_off,
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
-                              uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status, cudaStream_t s) {
+                              const float* weights, float* out, uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status,
+                              cudaStream_t s) {
   const int max_tiles = T * K / TCN + EMAX, max_half = T * K / TCN_HALF + EMAX;
   TcExpert* exps = reinterpret_cast<TcExpert*>(meta);
   TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * EMAX);
@@ -546,8 +581,9 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
                                                     half_tiles, counts, max_tiles, max_half, rows_cap,
                                                     status));
-  STRATA_LAUNCH(KID_TC_GATHER, s, tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x, inv_rms, pair, T * K, exps, counts, xg,
-                                                                                   rows_cap, status));
+  STRATA_LAUNCH(KID_TC_GATHER, s,
+                tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x16, T, pair, T * K, exps, counts, xg,
+                                                                          rows_cap, status));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   int dev = 0;
@@ -557,8 +593,8 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) g_sms[dev] = sms;
   }
-  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, T * K,
-              parts, status};
+  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, T,
+              T * K, nullptr, nullptr, nullptr, status};
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<true>::SMEM)) != cudaSuccess)
     return err;
@@ -567,6 +603,9 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const float* x, const 
   TcParams dp = gp;
   dp.act = hg;
   dp.tiles = half_tiles;
+  dp.parts = out ? nullptr : parts;
+  dp.wts = weights;
+  dp.out = out;
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<false>::SMEM)) != cudaSuccess)
     return err;

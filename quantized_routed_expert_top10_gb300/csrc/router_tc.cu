@@ -23,6 +23,29 @@
 #include "tc_common.cuh"
 
 namespace strata {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+bool make_tensor_map_2d(void* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                        uint32_t box_inner, uint32_t box_rows) {
+  using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_stride};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(reinterpret_cast<CUtensorMap*>(map), (CUtensorMapDataType)dtype, 2, const_cast<void*>(base), dims,
+            strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int RT_T = 128;  // tokens per tile (MMA N)
@@ -48,31 +71,36 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 // x (fp32 [T][H]) -> x_hi, x_lo (bf16 [T][H]), times 1/rms(x[t]) when inv_rms is non-null (which then
-// also receives the factors).  One warp per token row.
-__global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ x, int T,
-                                                          __nv_bfloat16* __restrict__ xh,
+// also receives the factors).  For a layer call also x16 (the expert path's fp16 token copy, same
+// scaling) and out = x (residual layers, skipped when out is x itself) or 0: the down kernel adds the
+// experts' weighted outputs into it.  One warp per token row; every read of the row precedes the
+// warp's stores to out, so out may be x.
+__global__ void __launch_bounds__(256) router_prep_kernel(const float* x, int T, __nv_bfloat16* __restrict__ xh,
                                                           __nv_bfloat16* __restrict__ xl,
-                                                          float* __restrict__ inv_rms) {
+                                                          float* __restrict__ inv_rms, uint8_t* __restrict__ x16,
+                                                          float* out) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
+  float4* orow = out ? reinterpret_cast<float4*>(out + (size_t)t * H) : nullptr;
+  const bool init_out = out && (!inv_rms || out != x);
   constexpr int PER = H / 4 / 32;  // 20 float4 per lane
-  float4 v[PER];
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    v[i] = __ldg(xr + lane + 32 * i);
-    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-  }
   float sc = 1.f;
   if (inv_rms) {
+    float ss = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < PER; ++i) {
+      const float4 v = xr[lane + 32 * i];
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
     ss = warp_sum(ss);
     sc = 1.f / sqrtf(ss / (float)H + 1e-6f);
     if (lane == 0) inv_rms[t] = sc;
   }
-#pragma unroll
+#pragma unroll 4
   for (int i = 0; i < PER; ++i) {
-    const float f[4] = {v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc};
+    const float4 v = xr[lane + 32 * i];  // read before this lane's store to the same float4 of out
+    const float f[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
     __nv_bfloat16 hi[4], lo[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -82,6 +110,8 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restric
     const size_t o = (size_t)t * H + 4 * (lane + 32 * i);
     *reinterpret_cast<uint2*>(xh + o) = *reinterpret_cast<const uint2*>(hi);
     *reinterpret_cast<uint2*>(xl + o) = *reinterpret_cast<const uint2*>(lo);
+    if (x16) tc::x16_store_chunk(v, i, sc, t, T, x16);
+    if (init_out) orow[lane + 32 * i] = inv_rms ? v : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -182,31 +212,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   }
 }
 
-using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
-EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
-  return fn;
-}
-
 // Tensor map of a row-major bf16 matrix [rows][H]: boxes of 64 columns x 128 rows, 128-byte swizzle,
 // rows past the end read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int rows) {
-  EncodeTiled fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t elem[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tensor_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, H, rows, (uint64_t)H * 2, 64, 128);
 }
 
 int g_rt_attr[64];
@@ -214,10 +223,11 @@ int g_rt_attr[64];
 }  // namespace
 
 cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16_t* w_router, int E, void* xbf,
-                             float* parts, int* status, cudaStream_t s) {
+                             float* parts, int* status, cudaStream_t s, uint8_t* x16, float* out) {
   __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xbf);
   __nv_bfloat16* xl = xh + (size_t)T * H;
-  STRATA_LAUNCH(KID_ROUTER_PREP, s, router_prep_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, xh, xl, inv_rms));
+  STRATA_LAUNCH(KID_ROUTER_PREP, s,
+                router_prep_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, xh, xl, inv_rms, x16, out));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap mh, ml, mw;

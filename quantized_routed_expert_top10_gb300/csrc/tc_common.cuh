@@ -58,6 +58,35 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// The fp16 token copy the tensor-core expert path reads its token tiles from: X16[kb][t][128 bytes] =
+// x[t][64 kb .. 64 kb + 63] times sc, as fp16, each 16-weight group in the order 0,8,1,9,..,7,15 (the
+// order one LOP3 per half2 gives the dequantised weights), chunk c (16 bytes) of a row holding
+// weights {4(c&1) .. +3} interleaved with {8 + 4(c&1) .. +3} of group c / 2.  Called by a whole warp for
+// token t with a = x[t][4 (lane + 32 i) .. +3]: the float4 8 weights further is two lanes up, so lanes
+// 4j and 4j + 1 each assemble and store one chunk.
+__device__ __forceinline__ void x16_store_chunk(const float4 a, int i, float sc, int t, int T, uint8_t* x16) {
+  const int lane = threadIdx.x & 31;
+  float4 b;
+  b.x = __shfl_down_sync(0xffffffffu, a.x, 2);
+  b.y = __shfl_down_sync(0xffffffffu, a.y, 2);
+  b.z = __shfl_down_sync(0xffffffffu, a.z, 2);
+  b.w = __shfl_down_sync(0xffffffffu, a.w, 2);
+  if ((lane & 2) == 0) {
+    const int m = lane + 32 * i;  // float4 index: 16-group m >> 2, half m & 1
+    const int kb = m >> 4, c = 2 * ((m >> 2) & 3) + (m & 1);
+    const __half2 h0 = __floats2half2_rn(a.x * sc, b.x * sc), h1 = __floats2half2_rn(a.y * sc, b.y * sc);
+    const __half2 h2 = __floats2half2_rn(a.z * sc, b.z * sc), h3 = __floats2half2_rn(a.w * sc, b.w * sc);
+    *reinterpret_cast<uint4*>(x16 + ((size_t)kb * T + t) * 128 + c * 16) =
+        make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                   *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+  }
+}
+
 // Arrive (once) on an mbarrier when every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

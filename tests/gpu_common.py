@@ -127,6 +127,19 @@ def check_close(gpu: np.ndarray, ref: np.ndarray, what: str):
     return err, bound
 
 
+# Prefill layers (T > 8) add each token's ten weighted expert outputs into the output with fp32
+# reductions whose order varies from call to call; two calls then differ by the rounding of an
+# 11-term fp32 sum in two orders: at most ~20 units of 2^-24 of the terms' magnitude.  Repeat-call
+# comparisons of prefill outputs use this bound (far inside the 2e-3 parity tolerance); routing is
+# computed before the reductions and stays bit-exact.
+SUM_ORDER_TOL = 1e-5
+
+
+def assert_equal_up_to_sum_order(a: np.ndarray, b: np.ndarray, scale: float, what: str):
+    err = float(np.abs(a.astype(np.float64) - b).max()) if a.size else 0.0
+    assert err <= SUM_ORDER_TOL * scale, f"{what}: max|diff| {err:.3e} > {SUM_ORDER_TOL * scale:.3e}"
+
+
 def run_layer(blobs, wr, bias, x, flags=0, q2_offset=1, E=512, ws=None):
     T = x.shape[0]
     ws = workspace(T) if ws is None else ws

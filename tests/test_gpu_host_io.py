@@ -1,5 +1,6 @@
-"""GPU tests of the host-buffer calls (strata_moe_layer_host / strata_moe_stack_host): the same results,
-bit for bit, as the device-buffer calls on the same inputs, through the graph path (page-locked buffers
+"""GPU tests of the host-buffer calls (strata_moe_layer_host / strata_moe_stack_host): the same results as
+the device-buffer calls on the same inputs (bit for bit for decode; for prefill up to the order of the
+fused combine's fp32 additions), through the graph path (page-locked buffers
 on a side stream, first call captured, later calls replayed) and the direct path (pageable buffers or
 the default stream), with the kernel copies (page-locked buffers) and the copy engines (pageable); and
 the oracle on the host path's output."""
@@ -10,7 +11,16 @@ import torch
 import gen
 import oracle
 import quantized_routed_expert_top10_gb300 as qre
-from gpu_common import DEV, BlobCache, check_close, check_routing, device_packed_layer, to_dev, workspace
+from gpu_common import (DEV, BlobCache, assert_equal_up_to_sum_order, check_close, check_routing,
+                        device_packed_layer, to_dev, workspace)
+
+
+def assert_same_result(got, want, T, what, layers=1):
+    """Decode (T <= 8) results repeat bit for bit; prefill results up to the fused combine's order."""
+    if T <= 8:
+        np.testing.assert_array_equal(got, want)
+    else:
+        assert_equal_up_to_sum_order(got, want, 10 * layers * np.abs(want).max(), what)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,7 +81,7 @@ def test_layer_host_matches_device_call(layers, T, flags, pinned):
         got = as_np(ho)
         want = device_call(ex, wr, bias, x, flags, ws, s)
         n2 = qre.strata_moe_launch_count()
-        np.testing.assert_array_equal(got, want)
+        assert_same_result(got, want, T, "host layer call")
         assert n2 - n1 >= 1
         assert n1 - n0 == n2 - n1 + extra  # replays count the graph's kernels
     assert qre.strata_poll_status(ws) == 0
@@ -91,7 +101,7 @@ def test_layer_host_at_the_largest_chunk(layers):
     fill(hx, x)
     for _ in range(2):
         qre.strata_moe_layer_host(ex, wr, bias, hx, T, 1, ho, None, None, ws, stream=s)
-    np.testing.assert_array_equal(as_np(ho), device_call(ex, wr, bias, x, 1, ws, s))
+    assert_same_result(as_np(ho), device_call(ex, wr, bias, x, 1, ws, s), T, "largest chunk")
     assert qre.strata_poll_status(ws) == 0
     del ws
     torch.cuda.empty_cache()
@@ -176,7 +186,7 @@ def test_stack_host_matches_device_call(layers, T, pinned):
         with torch.cuda.stream(s):
             qre.strata_moe_stack(exs, wr, bias, L, xd, T, None, None, ws, stream=s)
         s.synchronize()
-        np.testing.assert_array_equal(as_np(hx), xd.cpu().numpy())
+        assert_same_result(as_np(hx), xd.cpu().numpy(), T, "host stack call", layers=L)
     assert qre.strata_poll_status(ws) == 0
 
 
