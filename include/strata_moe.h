@@ -180,8 +180,9 @@ strata_status strata_moe_stack(const strata_experts_t* ex, const uint16_t* w_rou
  * after synchronising `stream`, so out_host holds the result on return.  ids / weights (nullable) are
  * DEVICE arrays as for strata_moe_layer.  x_host and out_host must not overlap (STRATA_E_INVAL).
  *   - Page-locked host buffers (cudaHostAlloc / cudaHostRegister) with a device mapping and 16-byte
- *     alignment are reached through that mapping: x_host is read by a copy kernel and the layer
- *     stores its output straight into out_host.  Each buffer must lie within one page-locked
+ *     alignment are reached through that mapping: x_host is read by a copy kernel, and a decode layer
+ *     (T <= 8) stores its output straight into out_host while a prefill layer computes it in the
+ *     workspace and a copy kernel writes it out.  Each buffer must lie within one page-locked
  *     allocation or registration (its first and last bytes are checked).  Pageable or unaligned
  *     buffers go through the copy engines.
  *   - When x_host and out_host are page-locked and `stream` is not the legacy default stream, the

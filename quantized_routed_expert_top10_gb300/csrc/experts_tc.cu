@@ -399,13 +399,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
           tc::fence_after_sync();
           const uint64_t bd = tc::smem_desc_sw128(smem_u32(tma_ring + (size_t)s * G::TMA_STAGE));
           const uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
+          // the two matrices' MMAs alternate, so each accumulator's next MMA never waits on its last
+          const uint64_t ad0 = tc::smem_desc_sw128(smem_u32(ast));
 #pragma unroll
-          for (int mat = 0; mat < G::NMAT; ++mat) {
-            const uint64_t ad = tc::smem_desc_sw128(smem_u32(ast + mat * A_TILE));
+          for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_f16(acc + mat * mat_cols, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          }
+            for (int mat = 0; mat < G::NMAT; ++mat)
+              tc::mma_f16(acc + mat * mat_cols, ad0 + (uint64_t)((mat * A_TILE) >> 4) + 2 * kk, bd + 2 * kk, idesc,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&empty_tma[s]);
           tc::mma_commit(&empty_a[sa]);
         }
@@ -475,22 +476,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u) + ((uint32_t)(32 * q) << 16);
       const uint32_t mat_cols = wide ? 256u : 128u;
       if (GU) {
+        // h = silu(g) * u = g u / (1 + e^-g), rounded to fp16 for the down projection: the fast exponential
+        // and division (relative error ~1e-6) stay far below that rounding (2^-11)
         const int k = rt * 128 + erow;  // h index = the down projection's contraction index
         const int kbd = k >> 6, k64 = k & 63;
         const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
+        uint8_t* hbase = p.hg + (int64_t)kbd * p.rows_cap * 128 + 2 * (pos & 7);
+        const int pc = pos >> 3;
+#pragma unroll 1
         for (int ch = 0; ch < nrows / 16; ++ch) {
-          float g[16], u[16];
-          tc::tmem_ld16(acc + 16 * ch, g);
-          tc::tmem_ld16(acc + mat_cols + 16 * ch, u);
+          uint32_t g[16], u[16];
+          tc::tmem_ld16_async(acc + 16 * ch, g);
+          tc::tmem_ld16_async(acc + mat_cols + 16 * ch, u);
+          tc::tmem_wait_ld();
           if (ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = 16 * ch + i;
               if (col < tl.n) {
-                const int64_t hrow = tl.q0pad + col;
-                __half* dst = reinterpret_cast<__half*>(p.hg + ((int64_t)kbd * p.rows_cap + hrow) * 128 +
-                                                        (((pos >> 3) ^ (hrow & 7)) << 4)) + (pos & 7);
-                *dst = __float2half_rn(silu_mul(g[i], u[i]));
+                const int hrow = tl.q0pad + col;
+                const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+                const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
+                *reinterpret_cast<__half*>(hbase + (int64_t)hrow * 128 + (((pc ^ hrow) & 7) << 4)) = __float2half_rn(h);
               }
             }
           }
@@ -506,10 +513,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         }
         named_barrier(2, 128);
         const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
+#pragma unroll 1
         for (int ch = 0; ch < nrows / 16; ++ch) {
-          float y0[16], y1[16];
-          tc::tmem_ld16(acc + 16 * ch, y0);
-          tc::tmem_ld16(acc + mat_cols + 16 * ch, y1);
+          uint32_t y0[16], y1[16];
+          tc::tmem_ld16_async(acc + 16 * ch, y0);
+          tc::tmem_ld16_async(acc + mat_cols + 16 * ch, y1);
+          tc::tmem_wait_ld();
           if (ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -519,12 +528,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
                 if (p.out) {  // fused combine: out[t] += w[t][k] * y
                   const float w = s_ep_w[col];
                   float* dst = p.out + (size_t)(pr / K) * H + orow;
-                  tc::red_add_f32(dst, w * y0[i]);
-                  tc::red_add_f32(dst + 128, w * y1[i]);
+                  tc::red_add_f32(dst, w * __uint_as_float(y0[i]));
+                  tc::red_add_f32(dst + 128, w * __uint_as_float(y1[i]));
                 } else {
                   float* dst = p.parts + (size_t)pr * H + orow;
-                  dst[0] = y0[i];
-                  dst[128] = y1[i];
+                  dst[0] = __uint_as_float(y0[i]);
+                  dst[128] = __uint_as_float(y1[i]);
                 }
               }
             }

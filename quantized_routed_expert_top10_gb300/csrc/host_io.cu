@@ -232,9 +232,11 @@ strata_status strata_moe_layer_host(const strata_experts_t* ex, const uint16_t* 
   key.ws_bytes = ws_bytes;
   key.stream = stream;
   key.ex.assign(ex, ex + 1);
-  // the layer writes its output straight into out_host's mapping (both paths only store to out, once
-  // per element), which saves the copy-out step
-  const bool direct_out = usable_map(om);
+  // a decode layer (T <= 8) stores each output element once, so it writes straight into out_host's
+  // mapping, which saves the copy-out step; a prefill layer first sets its output and then adds every
+  // expert's weighted contribution into it (fp32 reductions): those stay in device memory and the
+  // result is copied out once
+  const bool direct_out = T <= DECODE_T_MAX && usable_map(om);
   auto enqueue = [&]() -> strata_status {
     STRATA_TRY_HOST(copy_host(dx, xm, bytes, xm, true, x_host, s));
     STRATA_TRY_HOST(strata_moe_layer(ex, w_router, bias, dx, T, flags, direct_out ? (float*)om : dout, ids, weights,

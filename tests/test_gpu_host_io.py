@@ -70,8 +70,9 @@ def test_layer_host_matches_device_call(layers, T, flags, pinned):
     ws = workspace(T)
     s = torch.cuda.Stream()
     hx, ho = host_buffers(T, pinned)
-    # page-locked activations: one copy kernel in, the layer writes out_host directly
-    extra = 1 if pinned else 0
+    # page-locked activations: one copy kernel in; a decode layer writes out_host directly, a prefill
+    # layer's output is copied out by a second copy kernel
+    extra = (1 if T <= 8 else 2) if pinned else 0
     for it in range(3):  # the first call captures, the next two replay (pinned); new x every call
         x = (gen.activations_fast(40 + it, T) * (2.0 if flags else 1.0)).astype(np.float32)
         fill(hx, x)
