@@ -259,7 +259,6 @@ struct TcParams {
 // [b*256 + j*128, +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256
 // tokens, one dequantised weight tile serving all of them) takes both halves, matrix j in [j*256, +256).
 constexpr int TC_THREADS = 512;
-constexpr int NS_A = 2;    // stages of dequantised weight tiles
 template <bool GU>
 struct TcGeo {
   static constexpr int NMAT = 2;
@@ -269,11 +268,56 @@ struct TcGeo {
   static constexpr uint32_t B_TILE = (GU ? TCN : TCN_HALF) * 128;  // token rows x 64 fp16
   static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
   static constexpr int NS_TMA = GU ? 4 : 6;            // stages of (token tile, code chunks)
+  static constexpr int NS_A = 2;                       // stages of dequantised weight tiles
   static constexpr uint32_t A_STAGE = NMAT * A_TILE;
   static constexpr uint32_t TMEM_COLS = 512;           // two halves of NMAT x 128 columns
   static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
+
+// h = silu(g) * u for 16-column chunks [ch0, ch1) of a gate/up accumulator pair, by the warp of TMEM lane
+// quadrant q (one weight row per thread): g in columns [0, mat_cols) of acc, u in [mat_cols, 2 mat_cols),
+// written to Hg (fp16, the down kernel's operand layout).  The fast exponential and division (relative
+// error ~1e-6) stay far below the fp16 rounding of h (2^-11).
+__device__ __forceinline__ void swiglu_chunks(const TcParams& p, const TcTile& tl, int rt, int q, uint32_t acc,
+                                              uint32_t mat_cols, int ch0, int ch1, bool ok) {
+  const int erow = 32 * q + (threadIdx.x & 31);
+  const int k = rt * 128 + erow;  // h index = the down projection's contraction index
+  const int kbd = k >> 6, k64 = k & 63;
+  const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
+  uint8_t* hbase = p.hg + (int64_t)kbd * p.rows_cap * 128 + 2 * (pos & 7);
+  const int pc = pos >> 3;
+#pragma unroll 1
+  for (int ch = ch0; ch < ch1; ++ch) {
+    uint32_t g[16], u[16];
+    tc::tmem_ld16_async(acc + 16 * ch, g);
+    tc::tmem_ld16_async(acc + mat_cols + 16 * ch, u);
+    tc::tmem_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int col = 16 * ch + i;
+        if (col < tl.n) {
+          const int hrow = tl.q0pad + col;
+          const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+          const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
+          *reinterpret_cast<__half*>(hbase + (int64_t)hrow * 128 + (((pc ^ hrow) & 7) << 4)) = __float2half_rn(h);
+        }
+      }
+    }
+  }
+}
+
+// A 256-token gate/up tile takes both TMEM halves, so the next item's MMAs wait until its epilogue has
+// drained them; the two dequantising warps of each lane quadrant (idle then: they have prepared the next
+// item's first stages) take part of it.  Chunks of 16 columns are split in three: [0, a) for the epilogue
+// warp, [a, b) for dequantiser warp 4 + q, [b, n) for warp 8 + q.
+__device__ __forceinline__ void wide_split(int nch, int part, int& c0, int& c1) {
+  const int a = (nch + 2) / 3, b = a + (nch - a + 1) / 2;
+  c0 = part == 0 ? 0 : (part == 1 ? a : b);
+  c1 = part == 0 ? a : (part == 1 ? b : nch);
+}
+constexpr int WIDE_BAR = 3;  // named barriers 3..6: epilogue warp 12 + q with dequantiser warps 4 + q, 8 + q
 
 // Item -> (token tile, weight row tile rt).  Gate/up items take tiles of up to 256 tokens (one
 // dequantised weight tile serves all of them); down items take tiles of up to 128 tokens, so their
@@ -293,6 +337,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
   constexpr int NS_TMA = G::NS_TMA;
   constexpr uint32_t B_TILE = G::B_TILE;
   uint8_t* a_ring = smem + (size_t)NS_TMA * G::TMA_STAGE;
+  constexpr int NS_A = G::NS_A;
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
   __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
@@ -426,11 +471,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
     const int row = dt & 127, sub = dt >> 7;  // matrix of the item
     int it = 0;
     bool ok = true;
+    // gate/up: the TMEM use of every item, tracked as the issuer assigns it, so that a 256-token tile's
+    // epilogue can be joined once the next item's first NS_A stages are dequantised (or after the last item)
+    int n_small = 0, uses[2] = {0, 0};
+    struct Pending { bool wide; TcTile tl; int rt; uint32_t par0, par1; };
+    Pending pend{false, TcTile{0, 0, 0, 0}, 0, 0u, 0u};
+    auto help_wide = [&](const Pending& pd) {
+      ok = ok && mbar_wait(&tmem_full[0], pd.par0, status);
+      ok = ok && mbar_wait(&tmem_full[1], pd.par1, status);
+      tc::fence_after_sync();
+      int c0, c1;
+      wide_split((pd.tl.n + 15) / 16, warp < 8 ? 1 : 2, c0, c1);
+      swiglu_chunks(p, pd.tl, pd.rt, warp & 3, tmem + ((uint32_t)(32 * (warp & 3)) << 16), 256u, c0, c1, ok);
+      tc::fence_before_sync();
+      named_barrier(WIDE_BAR + (warp & 3), 96);
+    };
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      int rt_unused;
-      if (item_tile<GU>(p, item, rt_unused).n == 0) continue;
+      int rt_cur;
+      const TcTile tl_cur = item_tile<GU>(p, item, rt_cur);
+      if (tl_cur.n == 0) continue;
+      Pending cur{false, tl_cur, rt_cur, (uint32_t)(uses[0] & 1), (uint32_t)(uses[1] & 1)};
+      if (GU) {
+        const bool wide = (tl_cur.n + 15) / 16 * 16 > TCN_HALF;
+        const int b = wide ? 0 : (n_small++ & 1);
+        cur.wide = wide;
+        for (int h = 0; h < 2; ++h)
+          if (wide || h == b) ++uses[h];
+      }
       for (int kb = 0; kb < G::KBN; ++kb, ++it) {
         const int s = it % NS_TMA, sa = it % NS_A;
+        if (GU && kb == NS_A && pend.wide) {
+          help_wide(pend);
+          pend.wide = false;
+        }
         if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], (uint32_t)((it / NS_A - 1) & 1), status);
         ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status);
         if (ok) {
@@ -455,7 +528,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[sa]);
       }
+      if (GU) {
+        if (pend.wide) help_wide(pend);  // an item shorter than NS_A k-blocks (never for gate/up)
+        pend = cur;
+      }
     }
+    if (GU && pend.wide) help_wide(pend);
   } else if (warp >= 12) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;
@@ -476,31 +554,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
       const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u) + ((uint32_t)(32 * q) << 16);
       const uint32_t mat_cols = wide ? 256u : 128u;
       if (GU) {
-        // h = silu(g) * u = g u / (1 + e^-g), rounded to fp16 for the down projection: the fast exponential
-        // and division (relative error ~1e-6) stay far below that rounding (2^-11)
-        const int k = rt * 128 + erow;  // h index = the down projection's contraction index
-        const int kbd = k >> 6, k64 = k & 63;
-        const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
-        uint8_t* hbase = p.hg + (int64_t)kbd * p.rows_cap * 128 + 2 * (pos & 7);
-        const int pc = pos >> 3;
-#pragma unroll 1
-        for (int ch = 0; ch < nrows / 16; ++ch) {
-          uint32_t g[16], u[16];
-          tc::tmem_ld16_async(acc + 16 * ch, g);
-          tc::tmem_ld16_async(acc + mat_cols + 16 * ch, u);
-          tc::tmem_wait_ld();
-          if (ok) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int col = 16 * ch + i;
-              if (col < tl.n) {
-                const int hrow = tl.q0pad + col;
-                const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-                const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
-                *reinterpret_cast<__half*>(hbase + (int64_t)hrow * 128 + (((pc ^ hrow) & 7) << 4)) = __float2half_rn(h);
-              }
-            }
-          }
+        const int nch = nrows / 16;
+        int c0 = 0, c1 = nch;
+        if (wide) wide_split(nch, 0, c0, c1);
+        swiglu_chunks(p, tl, rt, q, acc, mat_cols, c0, c1, ok);
+        if (wide) {  // the dequantising warps of this quadrant drain the rest
+          tc::fence_before_sync();
+          named_barrier(WIDE_BAR + q, 96);
         }
       } else {
         // the tile's pairs (and router weights) staged once per item by the 128 epilogue threads
