@@ -119,9 +119,9 @@ strata_status strata_moe_group(const int32_t* ids, int32_t T, int32_t n_expert, 
  * Some callers cannot call cudaMalloc at all: code running inside an engine whose device memory
  * belongs to its own pool or to another runtime, or a process that must not grow its device
  * footprint after start-up.  This call takes the same inputs and writes the same outputs as
- * strata_moe_group (bit for bit), but its scratch -- the per-chunk expert histograms and the tile
- * list -- is a fixed array of STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES (256 KiB) in the library's own
- * device memory, so it allocates nothing and takes no ws.
+ * strata_moe_group (bit for bit), but its scratch -- the per-chunk expert histograms -- is a fixed
+ * array of STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES (256 KiB) in the library's own device memory, so it
+ * allocates nothing and takes no ws.
  *   - The array is sized for the largest T the ABI allows; T outside [0, STRATA_MOE_T_MAX] returns
  *     STRATA_E_INVAL.
  *   - Every GPU that loads the library holds the array until the process exits.  The first call on

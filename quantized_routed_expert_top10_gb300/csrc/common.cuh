@@ -33,8 +33,6 @@ constexpr int D_CHUNK = 2304;  // bytes per (rt, kb) down chunk
 constexpr int64_t D_REGION = 921600;
 constexpr int64_t BLOB = STRATA_MOE_BLOB_BYTES;
 
-// Grouping tiles (finish_grouping): up to NT slots of one expert per tile.
-constexpr int NT = 8;
 constexpr int ROUTER_KSPLIT = 2;  // prefill router: splits of the 2,560-term contraction over CTAs
 constexpr int DECODE_T_MAX = 8;  // T <= this: fused single-kernel routing (router + top-10 + grouping)
 
@@ -53,13 +51,6 @@ struct __align__(16) QBlock {
   int32_t pad[2];
 };
 static_assert(sizeof(QBlock) == 144, "QBlock layout");
-
-struct __align__(16) Tile {
-  int32_t e;   // expert id
-  int32_t q0;  // first slot (index into the sorted pair array)
-  int32_t n;   // tokens in the tile (1..NT)
-  int32_t pad;
-};
 
 // Workspace layout for a call with T tokens (byte offsets, each 256-aligned).  The first
 // WS_HEADER bytes (status word and counters) are the same for every T and are zeroed once by
@@ -99,8 +90,7 @@ struct WsLayout {
   size_t expert_off;  // int32 [EMAX + 1]
   size_t pair;        // int32 [T*K]
   size_t active;      // int32 [EMAX]
-  size_t n_active;    // int32 [4]: n_active, n_tiles
-  size_t tiles;       // Tile [max_tiles]
+  size_t n_active;    // int32 [4]: n_active
   size_t chunk_cnt;   // int32 [n_chunks][EMAX]
   size_t qx;          // QBlock [T][KB_GU] quantised layer input (T <= DECODE_T_MAX routing kernel)
   size_t xpp;         // fp32 [T][H] (T <= DECODE_T_MAX): the other buffer of a decode stack's ping-pong
@@ -110,19 +100,12 @@ struct WsLayout {
   size_t tcmeta;      //                                      expert ranges, tiles, counts
   size_t io;          // fp32 [2][T][H]: device copies of a host-buffer call's input and output
   size_t total;
-  int max_tiles;
   int n_chunks;
 };
 
 constexpr int GROUP_CHUNK = 2048;  // pairs per grouping chunk
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
-
-// Each expert's n_e pairs need ceil(n_e / NT) tiles: at most P / NT + min(P, EMAX) in all.
-inline int max_tiles_for(int T) {
-  const int P = T * K;
-  return P / NT + (P < EMAX ? P : EMAX);
-}
 
 // Sizes of the tensor-core path's buffers (experts_tc.cu).
 int64_t tc_rows_cap(int T);
@@ -134,7 +117,6 @@ size_t tc_meta_bytes(int T);
 inline WsLayout ws_layout(int T) {
   WsLayout L{};
   const int P = T * K;
-  L.max_tiles = max_tiles_for(T);
   L.n_chunks = (P + GROUP_CHUNK - 1) / GROUP_CHUNK;
   if (L.n_chunks < 1) L.n_chunks = 1;
   L.status = WS_STATUS;
@@ -150,7 +132,6 @@ inline WsLayout ws_layout(int T) {
   L.pair = take(sizeof(int32_t) * (size_t)P);
   L.active = take(sizeof(int32_t) * EMAX);
   L.n_active = take(sizeof(int32_t) * 4);
-  L.tiles = take(sizeof(Tile) * (size_t)L.max_tiles);
   L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.n_chunks * EMAX);
   L.qx = take(sizeof(QBlock) * (size_t)T * KB_GU);
   L.xpp = take(T <= DECODE_T_MAX ? sizeof(float) * (size_t)T * H : 0);

@@ -2,9 +2,9 @@
 //
 // Some callers cannot call cudaMalloc at all -- for example code running inside an engine whose
 // device memory is owned by a custom pool or by another runtime, or a process that must not grow its
-// footprint after start-up.  strata_moe_group needs a caller workspace for its per-chunk histograms
-// and tile list; this variant takes that scratch from a fixed array in this library's own device
-// memory instead, so the caller only passes its inputs and outputs.
+// footprint after start-up.  strata_moe_group needs a caller workspace for its per-chunk histograms;
+// this variant takes that scratch from a fixed array in this library's own device memory instead, so
+// the caller only passes its inputs and outputs.
 //
 // The array is a file-scope __device__ symbol of STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES, sized for
 // the largest call the ABI allows (T = 8192, 81,920 pairs).  Every GPU that loads the library holds
@@ -21,12 +21,10 @@ namespace strata {
 namespace {
 
 constexpr int64_t kNoAllocMaxPairs = (int64_t)TMAX * K;
-constexpr int kNoAllocMaxTiles = (int)(kNoAllocMaxPairs / NT + EMAX);
 constexpr int kNoAllocMaxChunks = (int)((kNoAllocMaxPairs + GROUP_CHUNK - 1) / GROUP_CHUNK);
 constexpr size_t kOffStatus = 0;
 constexpr size_t kOffNActive = 256;
-constexpr size_t kOffTiles = 512;
-constexpr size_t kOffChunks = kOffTiles + sizeof(Tile) * (size_t)kNoAllocMaxTiles;
+constexpr size_t kOffChunks = 512;
 constexpr size_t kScratchUsed = kOffChunks + sizeof(int32_t) * (size_t)kNoAllocMaxChunks * EMAX;
 constexpr size_t kScratchBytes = 256 * 1024;
 static_assert(kScratchBytes == STRATA_MOE_GROUP_NOALLOC_SCRATCH_BYTES, "header and library disagree");
@@ -73,9 +71,7 @@ extern "C" strata_status strata_moe_group_noalloc(const int32_t* ids, int32_t T,
   WsLayout L{};
   L.status = kOffStatus;
   L.n_active = kOffNActive;
-  L.tiles = kOffTiles;
   L.chunk_cnt = kOffChunks;
-  L.max_tiles = max_tiles_for(T);
   L.n_chunks = (T * K + GROUP_CHUNK - 1) / GROUP_CHUNK;
   const cudaError_t e = launch_group(ids, T, n_expert, expert_off, pair, active, n_active, L, scratch,
                                      (cudaStream_t)stream);

@@ -23,48 +23,24 @@ __device__ void top_k_warp(const float* logits, int E, TopKScratch& sc, int32_t*
 }
 
 // ---------------------------------------------------------------------------------------------
-// Grouping: counting sort of pair numbers p = t*K + k by expert (stable), active experts, tiles.
+// Grouping: counting sort of pair numbers p = t*K + k by expert (stable), active experts.
 // ---------------------------------------------------------------------------------------------
 
-// From per-expert counts (shared) build expert_off, active, n_active and the tile list.
-// Whole CTA; cnt is shared [E]; sh_off, sh_tile shared [E]; scratch shared [>= 32].
-__device__ void finish_grouping(const int* cnt, int E, int* sh_off, int* sh_tile, int* scratch,
-                                int32_t* expert_off, int32_t* active, int32_t* n_active_tiles, Tile* tiles,
-                                int max_tiles) {
+// From per-expert counts (shared) build expert_off, active and n_active.
+// Whole CTA; cnt is shared [E]; sh_off, sh_flag shared [E]; scratch shared [>= 32].
+__device__ void finish_grouping(const int* cnt, int E, int* sh_off, int* sh_flag, int* scratch,
+                                int32_t* expert_off, int32_t* active, int32_t* n_active) {
   const int tid = threadIdx.x;
   const int total = cta_exclusive_scan(cnt, sh_off, E, scratch);
   for (int e = tid; e < E; e += blockDim.x) expert_off[e] = sh_off[e];
   if (tid == 0) expert_off[E] = total;
-  // active list: exclusive scan of (cnt > 0) flags (reuse sh_tile as the flag array)
-  for (int e = tid; e < E; e += blockDim.x) sh_tile[e] = cnt[e] > 0 ? 1 : 0;
+  // active list: exclusive scan of (cnt > 0) flags
+  for (int e = tid; e < E; e += blockDim.x) sh_flag[e] = cnt[e] > 0 ? 1 : 0;
   __syncthreads();
-  const int na = cta_exclusive_scan(sh_tile, sh_tile, E, scratch);
+  const int na = cta_exclusive_scan(sh_flag, sh_flag, E, scratch);
   for (int e = tid; e < E; e += blockDim.x)
-    if (cnt[e] > 0) active[sh_tile[e]] = e;
-  __syncthreads();
-  // tiles: ceil(cnt / NT) per expert
-  for (int e = tid; e < E; e += blockDim.x) sh_tile[e] = (cnt[e] + NT - 1) / NT;
-  __syncthreads();
-  const int ntiles = cta_exclusive_scan(sh_tile, sh_tile, E, scratch);
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int c = cnt[e];
-    const int nt = (c + NT - 1) / NT;
-    for (int j = 0; j < nt; ++j) {
-      const int idx = sh_tile[e] + j;
-      if (idx < max_tiles) {
-        Tile tl;
-        tl.e = e;
-        tl.q0 = sh_off[e] + j * NT;
-        tl.n = min(NT, c - j * NT);
-        tl.pad = 0;
-        tiles[idx] = tl;
-      }
-    }
-  }
-  if (tid == 0) {
-    n_active_tiles[0] = na;
-    n_active_tiles[1] = ntiles < max_tiles ? ntiles : max_tiles;
-  }
+    if (cnt[e] > 0) active[sh_flag[e]] = e;
+  if (tid == 0) n_active[0] = na;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -78,7 +54,7 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
     const float* __restrict__ bias, int E, int q2_offset, float* __restrict__ logits,
     float* __restrict__ logits_user, int32_t* __restrict__ ids, float* __restrict__ weights,
     int32_t* __restrict__ expert_off, int32_t* __restrict__ pair, int32_t* __restrict__ active,
-    int32_t* __restrict__ n_active_tiles, Tile* __restrict__ tiles, int max_tiles, QBlock* __restrict__ qx,
+    int32_t* __restrict__ n_active, QBlock* __restrict__ qx,
     int* __restrict__ counter, int* __restrict__ status) {
   __shared__ float s_inv[TT];
   __shared__ float s_red[4][TT];
@@ -183,7 +159,7 @@ __global__ void __launch_bounds__(128) route_decode_kernel(
     else atomicAdd(&s_cnt[ee], 1);
   }
   __syncthreads();
-  finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
+  finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active);
   __syncthreads();
   if (warp == 0) stable_scatter_warp(ids, 0, P, E, s_off, pair, 0);
   if (tid == 0) *counter = 0;
@@ -240,25 +216,31 @@ __global__ void __launch_bounds__(256) group_hist_kernel(const int32_t* __restri
 }
 
 // One CTA of 512 threads: per-expert running base over chunks (chunk_cnt becomes exclusive bases
-// within each expert), then offsets, active list and tiles.
+// within each expert; each thread reads its expert's counts of eight chunks at a time with independent
+// loads), then offsets and the active list.
 __global__ void __launch_bounds__(512) group_scan_kernel(int n_chunks, int E, int32_t* __restrict__ chunk_cnt,
                                                          int32_t* __restrict__ expert_off,
                                                          int32_t* __restrict__ active,
-                                                         int32_t* __restrict__ n_active_tiles,
-                                                         Tile* __restrict__ tiles, int max_tiles) {
-  __shared__ int s_cnt[EMAX], s_off[EMAX], s_tile[EMAX], s_scratch[32];
+                                                         int32_t* __restrict__ n_active) {
+  __shared__ int s_cnt[EMAX], s_off[EMAX], s_flag[EMAX], s_scratch[32];
   const int e = threadIdx.x;
   if (e < E) {
     int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int v = chunk_cnt[(size_t)c * EMAX + e];
-      chunk_cnt[(size_t)c * EMAX + e] = run;
-      run += v;
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < n_chunks ? chunk_cnt[(size_t)(c0 + j) * EMAX + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < n_chunks) {
+          chunk_cnt[(size_t)(c0 + j) * EMAX + e] = run;
+          run += v[j];
+        }
     }
     s_cnt[e] = run;
   }
   __syncthreads();
-  finish_grouping(s_cnt, E, s_off, s_tile, s_scratch, expert_off, active, n_active_tiles, tiles, max_tiles);
+  finish_grouping(s_cnt, E, s_off, s_flag, s_scratch, expert_off, active, n_active);
 }
 
 // One warp per chunk: the chunk's ids staged in shared memory with independent loads, then the
@@ -286,7 +268,7 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
 #define STRATA_ROUTE_ARGS                                                                           \
   x, T, apply_rmsnorm, w_router, bias, E, q2_offset, (float*)(ws + L.logits), logits_out, ids, weights, \
       (int32_t*)(ws + L.expert_off), (int32_t*)(ws + L.pair), (int32_t*)(ws + L.active),              \
-      (int32_t*)(ws + L.n_active), (Tile*)(ws + L.tiles), L.max_tiles, (QBlock*)(ws + L.qx),           \
+      (int32_t*)(ws + L.n_active), (QBlock*)(ws + L.qx),                                            \
       (int*)(ws + L.cnt_route), (int*)(ws + L.status)
   kernel_begin(KID_ROUTE_DECODE, s);
   if (T <= 1) route_decode_kernel<1><<<grid, 128, 0, s>>>(STRATA_ROUTE_ARGS);
@@ -313,8 +295,7 @@ cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, 
   STRATA_LAUNCH(KID_GROUP_HIST, s,
                 group_hist_kernel<<<L.n_chunks, 256, 0, s>>>(ids, P, E, chunk_cnt, (int*)(ws + L.status)));
   STRATA_LAUNCH(KID_GROUP_SCAN, s,
-                group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat,
-                                                    (Tile*)(ws + L.tiles), L.max_tiles));
+                group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat));
   STRATA_LAUNCH(KID_GROUP_SCATTER, s,
                 group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
   if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
