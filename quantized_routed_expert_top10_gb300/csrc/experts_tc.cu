@@ -24,7 +24,8 @@
 //   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (one half for a tile of up to 128
 //               tokens, both for a wider one) and commits to the stages' "empty" mbarriers;
 //   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
-//               epilogue while the next item accumulates into the other buffer.
+//               epilogue while the next item accumulates into the other buffer; the down kernel runs
+//               four more (warps 16-19, 640 threads), two warps per lane quadrant splitting the columns.
 // Every wait is bounded (STRATA_E_TIMEOUT).
 //
 // In-block order: the dequantiser emits the 64 weights of a block in the order pi (per 16 weights:
@@ -252,13 +253,19 @@ struct TcParams {
 
 // Kernel geometry.  Warp 0: copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
 // dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each);
-// warps 12..15: epilogue (one TMEM lane = one weight row per thread).
+// warps 12..15 (down: 12..19): epilogue (one TMEM lane = one weight row per thread).
 // gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
 // down (GU = false): item = (tile, pair of row tiles 2rp, 2rp + 1 of down): both share the token tile.
 // TMEM: a tile of up to 128 tokens accumulates in half b (alternating) -- matrix j in columns
 // [b*256 + j*128, +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256
 // tokens, one dequantised weight tile serving all of them) takes both halves, matrix j in [j*256, +256).
-constexpr int TC_THREADS = 512;
+// Threads per CTA: 16 warps for gate/up (its 125 registers per thread allow no more); the down kernel
+// (96 registers) runs 20, the last 8 of them epilogue warps, two per TMEM lane quadrant, because its
+// epilogue -- 256 fp32 reductions per thread and 128-token item -- is what it waits on.
+template <bool GU>
+constexpr int tc_threads() { return GU ? 512 : 640; }
+template <bool GU>
+constexpr int tc_epi_warps() { return GU ? 4 : 8; }
 template <bool GU>
 struct TcGeo {
   static constexpr int NMAT = 2;
@@ -329,7 +336,7 @@ __device__ __forceinline__ TcTile item_tile(const TcParams& p, int item, int& rt
 }
 
 template <bool GU>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams p) {
+__global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const TcParams p) {
   using G = TcGeo<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 4);
+      mbar_init(&tmem_empty[b], tc_epi_warps<GU>());
     }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
@@ -536,8 +543,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
     if (GU && pend.wide) help_wide(pend);
   } else if (warp >= 12) {
     // ---------------- epilogue ----------------
+    constexpr int EPI = tc_epi_warps<GU>();
     const int q = warp & 3;
     const int erow = 32 * q + lane;
+    const int epart = (warp - 12) >> 2;  // down: which half of each item's 16-column chunks this warp drains
+    const int etid = tid - 12 * 32;      // 0 .. 32 * EPI - 1
     int n_small = 0;
     int uses[2] = {0, 0};  // items drained from each TMEM half so far (same assignment as the issuer)
     bool ok = true;
@@ -563,18 +573,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_expert_kernel(const TcParams
           named_barrier(WIDE_BAR + q, 96);
         }
       } else {
-        // the tile's pairs (and router weights) staged once per item by the 128 epilogue threads
-        named_barrier(2, 128);  // every epilogue thread is done with the previous item's
-        if (erow < tl.n) {
-          int pr = __ldg(p.pair + tl.q0 + erow);
+        // the tile's pairs (and router weights) staged once per item by the epilogue threads
+        named_barrier(2, 32 * EPI);  // every epilogue thread is done with the previous item's
+        if (etid < tl.n) {
+          int pr = __ldg(p.pair + tl.q0 + etid);
           if (pr < 0 || pr >= p.P) pr = -1;
-          s_ep_pair[erow] = pr;
-          if (p.out) s_ep_w[erow] = pr >= 0 ? __ldg(p.wts + pr) : 0.f;
+          s_ep_pair[etid] = pr;
+          if (p.out) s_ep_w[etid] = pr >= 0 ? __ldg(p.wts + pr) : 0.f;
         }
-        named_barrier(2, 128);
+        named_barrier(2, 32 * EPI);
         const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
+        const int nch = nrows / 16, half = (nch + 1) / 2;
 #pragma unroll 1
-        for (int ch = 0; ch < nrows / 16; ++ch) {
+        for (int ch = epart * half; ch < min(nch, (epart + 1) * half); ++ch) {
           uint32_t y0[16], y1[16];
           tc::tmem_ld16_async(acc + 16 * ch, y0);
           tc::tmem_ld16_async(acc + mat_cols + 16 * ch, y1);
@@ -667,7 +678,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<true>::SMEM)) != cudaSuccess)
     return err;
-  STRATA_LAUNCH(KID_TC_GATEUP, s, tc_expert_kernel<true><<<sms, TC_THREADS, TcGeo<true>::SMEM, s>>>(gp));
+  STRATA_LAUNCH(KID_TC_GATEUP, s, tc_expert_kernel<true><<<sms, tc_threads<true>(), TcGeo<true>::SMEM, s>>>(gp));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   TcParams dp = gp;
   dp.act = hg;
@@ -678,7 +689,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<false>::SMEM)) != cudaSuccess)
     return err;
-  STRATA_LAUNCH(KID_TC_DOWN, s, tc_expert_kernel<false><<<sms, TC_THREADS, TcGeo<false>::SMEM, s>>>(dp));
+  STRATA_LAUNCH(KID_TC_DOWN, s, tc_expert_kernel<false><<<sms, tc_threads<false>(), TcGeo<false>::SMEM, s>>>(dp));
   return cudaGetLastError();
 }
 
