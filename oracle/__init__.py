@@ -77,7 +77,7 @@ def lib():
             _c_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u16p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _c_f64p,
-            ctypes.c_int]
+            ctypes.c_int, ctypes.c_void_p]
         _lib = L
     return _lib
 
@@ -185,8 +185,9 @@ def route(x, w_router, bias=None, residual=False, K=10, n_threads=None):
 
 
 def moe_layer(x, w_router, bias, blobs, q2_offset=1, residual=False, ids_in=None, H=None, FF=None,
-              K=10, want_parts=False, n_threads=None):
-    """One MoE layer for x fp32[T][H]. blobs: list of E canonical blobs (None where unused).
+              K=10, want_parts=False, n_threads=None, shared=None):
+    """One MoE layer for x fp32[T][H]. blobs: list of E canonical blobs (None where unused); shared:
+    the layer's shared expert (canonical blob) or None.
 
     Returns dict(out, ids, w, logits[, parts])."""
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -204,10 +205,11 @@ def moe_layer(x, w_router, bias, blobs, q2_offset=1, residual=False, ids_in=None
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     ii = None if ids_in is None else np.ascontiguousarray(ids_in, dtype=np.int32)
     nt = n_threads if n_threads else max(1, min(os.cpu_count() or 1, T))
+    sh = None if shared is None else np.ascontiguousarray(shared, dtype=np.uint8)
     rc = lib().oracle_moe_layer(x, T, H, FF, E, K, np.ascontiguousarray(w_router, dtype=np.uint16),
                                 _ptr(b), ctypes.cast(arr, ctypes.c_void_p), q2_offset,
                                 1 if residual else 0, _ptr(ii), _ptr(ids), _ptr(w), _ptr(logits),
-                                _ptr(parts), out, nt)
+                                _ptr(parts), out, nt, _ptr(sh))
     if rc:
         raise ValueError("oracle_moe_layer: bad argument or a routed expert has no blob")
     res = dict(out=out, ids=ids, w=w, logits=logits)

@@ -192,6 +192,7 @@ typedef struct {
   const uint16_t* w_router;
   const float* bias;
   const uint8_t* const* blobs;
+  const uint8_t* shared_blob;
   int q2_offset, residual;
   const int32_t* ids_in;
   int32_t* ids_out;
@@ -204,7 +205,10 @@ typedef struct {
 } layer_job;
 
 /* One token: [zwxr] route -> top-10 -> experts -> "Combine" out = sum_k w_k * parts_k (k order),
- * then the residual for stacked layers. */
+ * then, when the layer has one, the shared expert's output on the same normalised input added with
+ * weight 1 ([wayneh] lists a shared expert that runs for every token; its size and any gate are not on
+ * the pages: it is read as an expert of the routed experts' shape and format, ungated), then the
+ * residual for stacked layers. */
 static int token_forward(const layer_job* j, int t) {
   const int H = j->H, E = j->E, K = j->K;
   double* xin = (double*)malloc(sizeof(double) * (size_t)H);
@@ -241,6 +245,10 @@ static int token_forward(const layer_job* j, int t) {
       if (j->parts_out) memcpy(j->parts_out + ((int64_t)t * K + k) * H, y, sizeof(double) * (size_t)H);
       for (int h = 0; h < H; ++h) acc[h] += w[k] * y[h];
     }
+    if (!rc && j->shared_blob) {
+      oracle_expert(j->shared_blob, H, j->FF, j->q2_offset, xn, y);
+      for (int h = 0; h < H; ++h) acc[h] += y[h];
+    }
     if (!rc && j->residual)
       for (int h = 0; h < H; ++h) acc[h] = xin[h] + acc[h];
   }
@@ -266,7 +274,7 @@ static void* layer_worker(void* arg) {
 int oracle_moe_layer(const float* x, int T, int H, int FF, int E, int K, const uint16_t* w_router,
                      const float* bias, const uint8_t* const* blobs, int q2_offset, int residual,
                      const int32_t* ids_in, int32_t* ids_out, double* w_out, double* logits_out,
-                     double* parts_out, double* out, int n_threads) {
+                     double* parts_out, double* out, int n_threads, const uint8_t* shared_blob) {
   if (T < 0 || H <= 0 || FF <= 0 || E <= 0 || K <= 0 || K > E || !out || !x || !w_router || !blobs)
     return -1;
   if (((int64_t)H * FF) % 64) return -1;
@@ -285,6 +293,7 @@ int oracle_moe_layer(const float* x, int T, int H, int FF, int E, int K, const u
     j->w_router = w_router;
     j->bias = bias;
     j->blobs = blobs;
+    j->shared_blob = shared_blob;
     j->q2_offset = q2_offset;
     j->residual = residual;
     j->ids_in = ids_in;

@@ -87,11 +87,15 @@ int oracle_route_tokens(const float* x, int T, int H, int E, int K, const uint16
  *   Outputs (each nullable except out): ids_out [T][K], w_out [T][K], logits_out [T][E],
  *   parts_out [T][K][H] (unweighted expert outputs), out [T][H].
  *   n_threads >= 1 splits tokens; results do not depend on it.
+ *   shared_blob (nullable): the layer's shared expert (canonical blob of the routed experts' shape);
+ *   its output on the same input is added with weight 1 after the routed combine, before the
+ *   residual.  Reading: the pages name a shared expert run for every token but give neither its width
+ *   nor a gate.
  * Returns 0, or -1 on a bad argument / a NULL blob that routing needs. */
 int oracle_moe_layer(const float* x, int T, int H, int FF, int E, int K, const uint16_t* w_router,
                      const float* bias, const uint8_t* const* blobs, int q2_offset, int residual,
                      const int32_t* ids_in, int32_t* ids_out, double* w_out, double* logits_out,
-                     double* parts_out, double* out, int n_threads);
+                     double* parts_out, double* out, int n_threads, const uint8_t* shared_blob);
 
 #ifdef __cplusplus
 }

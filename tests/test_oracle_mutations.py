@@ -76,6 +76,15 @@ MUTATIONS = [
     ("route_tokens_bias_dropped",
      "oracle_router_logits(xn, j->H, j->E, j->w_router, j->bias, logits);\n    oracle_top_k",
      "oracle_router_logits(xn, j->H, j->E, j->w_router, NULL, logits);\n    oracle_top_k"),
+    ("shared_expert_dropped",
+     "for (int h = 0; h < H; ++h) acc[h] += y[h];\n    }\n    if (!rc && j->residual)",
+     "(void)0;\n    }\n    if (!rc && j->residual)"),
+    ("shared_expert_on_raw_input",
+     "oracle_expert(j->shared_blob, H, j->FF, j->q2_offset, xn, y);",
+     "oracle_expert(j->shared_blob, H, j->FF, j->q2_offset, xin, y);"),
+    ("shared_expert_weighted_by_first_router_weight",
+     "for (int h = 0; h < H; ++h) acc[h] += y[h];\n    }\n    if (!rc && j->residual)",
+     "for (int h = 0; h < H; ++h) acc[h] += w[0] * y[h];\n    }\n    if (!rc && j->residual)"),
     ("combine_unweighted",
      "for (int h = 0; h < H; ++h) acc[h] += w[k] * y[h];",
      "for (int h = 0; h < H; ++h) acc[h] += y[h];"),

@@ -421,6 +421,44 @@ def test_residual_layer_routes_on_normalised_input():
     np.testing.assert_allclose(r["out"] - 3.0 * x, r1["out"] - x, rtol=1e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("residual", [False, True])
+@pytest.mark.parametrize("H,FF", [(64, 16), (2560, 640)])
+def test_shared_expert_closed_form_through_the_layer(H, FF, residual):
+    """Routed experts whose codes all equal the offset contribute nothing, so the layer's output is the
+    shared expert alone: a selection matrix's closed form on the (normalised) input, plus x when
+    residual."""
+    E, K, T, off = 8, 2, 3, 1
+    zero = make_blob((np.full((FF, H), off), np.full((FF, H), off), np.full((H, FF), off)))
+    shared, sig, tau, rho = selection_blob(H, FF, off)
+    x = (2.0 * gen.activations(11, T, H_=H)).astype(np.float32)
+    wr = gen.router_weights(3, 0, E_=E, H_=H)
+    r = oracle.moe_layer(x, wr, None, [zero] * E, K=K, residual=residual, shared=shared)
+    for t in range(T):
+        xd = x[t].astype(np.float64)
+        xn = xd / math.sqrt(np.mean(xd * xd) + 1e-6) if residual else xd
+        h = [silu(xn[sig[q]]) * xn[tau[q]] for q in range(FF)]
+        want = np.array([h[rho[n]] for n in range(H)]) + (xd if residual else 0.0)
+        np.testing.assert_allclose(r["out"][t], want, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_shared_expert_adds_its_output_with_weight_one(residual):
+    """The layer with a shared expert minus the same layer without it is that expert on the routed
+    experts' input (rmsnorm(x) for residual layers), unweighted; routing is unchanged."""
+    T, E, H, FF = 5, 8, 64, 16
+    x, wr, blobs = _tiny_layer_inputs(T)
+    x = (3.0 * x).astype(np.float32)
+    shared = gen.canonical_blob(9, 0, 99, H_=H, FF_=FF)
+    a = oracle.moe_layer(x, wr, None, blobs, K=2, residual=residual, shared=shared)
+    b = oracle.moe_layer(x, wr, None, blobs, K=2, residual=residual)
+    np.testing.assert_array_equal(a["ids"], b["ids"])
+    for t in range(T):
+        xd = x[t].astype(np.float64)
+        xn = xd / math.sqrt(np.mean(xd * xd) + 1e-6) if residual else xd
+        y = _numpy_expert(shared, H, FF, 1, xn)
+        np.testing.assert_allclose(a["out"][t] - b["out"][t], y, rtol=1e-9, atol=1e-12)
+
+
 def test_rmsnorm_mean_square():
     x = gen.activations(4, 1)[0].astype(np.float64) * 7.0
     xn = oracle.rmsnorm(x)
