@@ -86,6 +86,13 @@ typedef struct strata_experts {
   int64_t blob_stride; /* bytes; multiple of 256 and >= STRATA_MOE_BLOB_BYTES */
   int32_t n_expert;    /* E: experts routed over; multiple of 32 in [32, 512] */
   int32_t q2_offset;   /* 1: codes {0,1,2,3} = {-1,0,1,2} x d (the pages); 2: the c-2 reading */
+  /* device, nullable: the layer's shared expert, a packed blob (256-byte aligned) of the same shape and
+   * format.  wayneh.tw "strata-local-moe-inference" lists a shared expert that runs on the GPU for every
+   * token; the pages give neither its width nor a gate, so it is read as an expert of the routed
+   * experts' shape whose output on the same input is added with weight 1 to the routed experts'
+   * weighted sum (strata_moe_layer, strata_moe_stack and the host-buffer calls; strata_moe_experts
+   * computes the routed pairs only and ignores it).  NULL: no shared expert. */
+  const void* shared_blob;
 } strata_experts_t;
 
 /* Bytes of workspace a call with T tokens needs (any entry point below). */
@@ -158,8 +165,10 @@ strata_status strata_moe_combine(const float* parts, const float* weights, int32
 /* Steps 1-5 for one layer. flags = 0: out = moe(x); flags = STRATA_MOE_RESIDUAL_RMSNORM: out =
  * x + moe(rmsnorm(x)) with router and experts both reading rmsnorm(x).  out may alias x.  ids /
  * weights (nullable) receive the routing.  Workspace as for any call with T tokens.
- * Summation order: for T <= 8 the ten weighted expert outputs of a token are added in k order and
- * repeated calls give the same bits.  For T > 8 the combine is fused into the down projection: out is
+ * With ex->shared_blob, the shared expert's output (weight 1) is added to the routed experts' weighted
+ * sum before the residual.
+ * Summation order: for T <= 8 the ten weighted expert outputs of a token are added in k order (then
+ * the shared expert's) and repeated calls give the same bits.  For T > 8 the combine is fused into the down projection: out is
  * first set to x (residual layers) or 0, and each expert's weighted output is added into it with fp32
  * atomic additions as the expert finishes, so the order of a token's ten additions -- and the last
  * bits of out -- can differ from call to call (the routing, computed before, does not). */

@@ -56,7 +56,7 @@ class StrataError(RuntimeError):
 
 class strata_experts_t(ctypes.Structure):
     _fields_ = [("blobs", ctypes.c_void_p), ("blob_stride", ctypes.c_int64),
-                ("n_expert", ctypes.c_int32), ("q2_offset", ctypes.c_int32)]
+                ("n_expert", ctypes.c_int32), ("q2_offset", ctypes.c_int32), ("shared_blob", ctypes.c_void_p)]
 
 
 _lib = None
@@ -144,9 +144,11 @@ def _check(fn, rc):
         raise StrataError(fn, rc)
 
 
-def experts(blobs, n_expert: int = E_MAX, q2_offset: int = 1, blob_stride: int = BLOB_BYTES) -> strata_experts_t:
-    """A strata_experts_t for packed blobs at a device tensor (or address)."""
-    return strata_experts_t(_p(blobs), blob_stride, n_expert, q2_offset)
+def experts(blobs, n_expert: int = E_MAX, q2_offset: int = 1, blob_stride: int = BLOB_BYTES,
+            shared=None) -> strata_experts_t:
+    """A strata_experts_t for packed blobs at a device tensor (or address); shared: the layer's shared
+    expert (a packed blob, device tensor or address) or None."""
+    return strata_experts_t(_p(blobs), blob_stride, n_expert, q2_offset, _p(shared))
 
 
 def strata_moe_workspace_bytes(T: int) -> int:

@@ -31,6 +31,7 @@ strata_status check_experts(const strata_experts_t* ex) {
   if (ex->q2_offset != 1 && ex->q2_offset != 2) return STRATA_E_INVAL;
   if (ex->blob_stride < BLOB) return STRATA_E_INVAL;
   if (!aligned(ex->blobs, 256) || (ex->blob_stride % 256) != 0) return STRATA_E_ALIGN;
+  if (ex->shared_blob && !aligned(ex->shared_blob, 256)) return STRATA_E_ALIGN;
   return STRATA_OK;
 }
 
@@ -92,7 +93,7 @@ strata_status layer_impl(const strata_experts_t* ex, const uint16_t* w_router, c
                                 (const int32_t*)(w + L.pair), (const int32_t*)(w + L.active),
                                 (const int32_t*)(w + L.n_active), nullptr, wts_d, out, (uint8_t*)(w + L.xg),
                                 (uint8_t*)(w + L.hg),
-                                (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s));
+                                (uint8_t*)(w + L.tcmeta), (int*)(w + L.status), s, ex->shared_blob));
   return STRATA_OK;
 }
 

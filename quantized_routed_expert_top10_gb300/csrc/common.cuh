@@ -72,9 +72,11 @@ static_assert(WS_SYNC + sizeof(int32_t) * WS_SYNC_WORDS <= WS_HEADER, "decode sy
 // reader learns that a value is there from the value itself.  strata_moe_workspace_init zeroes it;
 // tag 0 never marks a value.
 constexpr size_t DX_DOTS = WS_HEADER;                                              // [WS_NREP][8][EMAX]
-constexpr size_t DX_H = DX_DOTS + sizeof(uint64_t) * WS_NREP * DECODE_T_MAX * EMAX;  // [8 * K][FF]
-constexpr size_t DX_PARTS = DX_H + sizeof(uint64_t) * DECODE_T_MAX * K * FF;          // [8 * K][H]
-constexpr size_t DX_PRED = DX_PARTS + sizeof(uint64_t) * DECODE_T_MAX * K * H;    // [8][EMAX] next layer
+// pair slots: the routed pairs t*K + k, then one per token for a layer's shared expert (K*T + t)
+constexpr int DECODE_PAIRS = DECODE_T_MAX * (K + 1);
+constexpr size_t DX_H = DX_DOTS + sizeof(uint64_t) * WS_NREP * DECODE_T_MAX * EMAX;  // [DECODE_PAIRS][FF]
+constexpr size_t DX_PARTS = DX_H + sizeof(uint64_t) * DECODE_PAIRS * FF;           // [DECODE_PAIRS][H]
+constexpr size_t DX_PRED = DX_PARTS + sizeof(uint64_t) * DECODE_PAIRS * H;         // [8][EMAX] next layer
 constexpr size_t DX_PRED_IDS = DX_PRED + sizeof(uint64_t) * DECODE_T_MAX * EMAX;     // [1 + 8 * K]
 constexpr size_t DX_END = (DX_PRED_IDS + sizeof(uint64_t) * (1 + DECODE_T_MAX * K) + 255) / 256 * 256;
 static_assert(DX_END % 256 == 0 && DX_PRED_IDS % 256 == 0, "exchange area regions stay 256-byte aligned");
@@ -298,11 +300,12 @@ bool make_tensor_map_2d(void* map, int dtype, const void* base, uint64_t inner, 
 // fp16 token copy X16 of x (times inv_rms[t] when non-null) for the tensor-core expert path.
 cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s);
 // Tile lists, then the gate/up and down kernels over the grouping.  out == null: y of every pair into
-// parts [T*K][H]; otherwise out[t] += weights[t][k] * y (out already holds the residual or zeros).
+// parts [T*K][H]; otherwise out[t] += weights[t][k] * y (out already holds the residual or zeros), and
+// a non-null shared_blob adds that expert's output for every token with weight 1.
 cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, int T, const int32_t* expert_off,
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
                               const float* weights, float* out, uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status,
-                              cudaStream_t s);
+                              cudaStream_t s, const void* shared_blob = nullptr);
 cudaError_t launch_combine(const float* parts, const float* weights, int T, const float* residual,
                            float* out, cudaStream_t s);
 // The next layer of a decode stack, for the lookahead (its router on this layer's input predicts its

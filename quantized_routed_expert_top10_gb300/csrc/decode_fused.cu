@@ -19,7 +19,9 @@
 //      routing is known.  A gate/up unit publishes h = silu(g) * u of its 16 rows; a down unit polls
 //      the h of its expert's tokens and publishes its 128 output rows per pair;
 //   4. the CTA of down unit (expert slot j, row tile r) then polls the outputs of every pair for
-//      share j of tile r's rows and writes their weighted sum in k order (+ the residual);
+//      share j of tile r's rows and writes their weighted sum in k order (+ the shared expert's
+//      output, + the residual).  A layer's shared expert is one more expert slot holding every token
+//      (pair slots K T + t, weight 1);
 //   5. decode stacks: the last CTA takes the next layer's predicted top-10 (its router on this
 //      layer's input) and publishes the distinct experts; at its start the next layer's CTAs
 //      prefetch their share of those experts' units into L2 (a hint; results never depend on it).
@@ -63,11 +65,12 @@ struct DecodeParams {
   const float* bias;   // [E] or null
   const uint8_t* blobs;
   int64_t stride;
+  const uint8_t* shared;  // the layer's shared expert (packed blob), or null
   int32_t* ids_out;  // [T][K]
   float* w_out;      // [T][K]
   uint64_t* dots;    // exchange area: router dot products [WS_NREP][DECODE_T_MAX][EMAX]
-  uint64_t* htag;    //                h of each slot [DECODE_T_MAX * K][FF]
-  uint64_t* ptag;    //                expert outputs of each pair [DECODE_T_MAX * K][H]
+  uint64_t* htag;    //                h of each slot [DECODE_PAIRS][FF]
+  uint64_t* ptag;    //                expert outputs of each pair [DECODE_PAIRS][H]
   uint64_t* pred;    //                next layer's predicted router logits [DECODE_T_MAX][EMAX]
   uint64_t* pred_ids;  //              [0]: D' predicted experts, [1 + j]: their ids, ascending
   const uint16_t* wr_next;  // next layer of a stack (lookahead), or null
@@ -272,13 +275,13 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   __shared__ float s_ssqt[DF_NW][TT];  // per warp and token (two or more tokens)
   __shared__ float s_dot[ROWS_MAX][TT];
   __shared__ __align__(16) int s_ids[(TT * K + 3) / 4 * 4];
-  __shared__ float s_w[TT * K];
-  __shared__ int s_te[DF_MAXD];   // expert slot j -> expert id
-  __shared__ int s_tn[DF_MAXD];   //               -> tokens routed to it
-  __shared__ int s_tq[DF_MAXD];   //               -> first slot in s_pair
+  __shared__ float s_w[TT * (K + 1)];  // weight of each pair (a shared-expert pair K T + t: 1)
+  __shared__ int s_te[DF_MAXD + 1];   // expert slot j -> expert id (-1: the shared expert)
+  __shared__ int s_tn[DF_MAXD + 1];   //               -> tokens routed to it
+  __shared__ int s_tq[DF_MAXD + 1];   //               -> first slot in s_pair
   __shared__ int s_first[TT * K];  // expert id of each slot (grouping)
   __shared__ int s_wcnt[DF_NW];
-  __shared__ int s_pair[TT * K];
+  __shared__ int s_pair[TT * (K + 1)];  // slot -> pair (routed t K + k; shared expert K T + t)
   __shared__ float s_rpart[DF_NW][TT];
   __shared__ float s_lpart[4][TT];  // lookahead rows' partial sums (warps 4-7)
   __shared__ float s_bias[EMAX];
@@ -651,6 +654,20 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       p.w_out[q] = s_w[q];
     }
   __syncthreads();
+  if (p.shared && routed) {  // the shared expert: one more expert slot, every token, weight 1
+    if (tid < T) {
+      s_pair[P + tid] = P + tid;
+      s_w[P + tid] = 1.f;
+    }
+    if (tid == 0) {
+      const int D = s_nact;
+      s_te[D] = -1;
+      s_tn[D] = T;
+      s_tq[D] = P;
+      s_nact = D + 1;
+    }
+    __syncthreads();
+  }
 
   // ---- 3. expert units ----
   if (s_ok) {
@@ -662,11 +679,12 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       const uint8_t* src;
       if (u < n_gu) {
         const int j = u / DF_GU, sl = u % DF_GU;
-        src = p.blobs + (int64_t)s_te[j] * p.stride + (int64_t)sl * SLAB_BYTES;
+        src = (s_te[j] >= 0 ? p.blobs + (int64_t)s_te[j] * p.stride : p.shared) + (int64_t)sl * SLAB_BYTES;
       } else {
         const int v = u - n_gu;
         const int j = v / DF_DN, rtd = v % DF_DN;
-        src = p.blobs + (int64_t)s_te[j] * p.stride + D_REGION + (int64_t)rtd * KB_D * D_CHUNK;
+        src = (s_te[j] >= 0 ? p.blobs + (int64_t)s_te[j] * p.stride : p.shared) + D_REGION +
+              (int64_t)rtd * KB_D * D_CHUNK;
       }
       s_pending[st] = (i / NS) & 1;
       mbar_expect_tx(&bars[st], DF_UNIT);
@@ -769,7 +787,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           __syncthreads();
           if (tid < SLAB * n) {
             const int r2 = tid % SLAB, ii = tid / SLAB;
-            const int tk = s_pair[q0 + ii] / K;
+            const int pq = s_pair[q0 + ii], tk = pq < P ? pq / K : pq - P;
             float gg = 0.f, uu = 0.f;
 #pragma unroll
             for (int w = 0; w < DF_NW; ++w) {
@@ -786,7 +804,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
           float tinv[TT];
 #pragma unroll
           for (int ii = 0; ii < TT; ++ii) {
-            tok[ii] = (ii < n) ? s_pair[q0 + ii] / K : 0;
+            const int pq = (ii < n) ? s_pair[q0 + ii] : 0;
+            tok[ii] = pq < P ? pq / K : pq - P;
             tinv[ii] = (ii < n) ? s_inv[tok[ii]] : 0.f;
           }
           float acc[TT];
@@ -981,9 +1000,13 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 
     // ---- 4. combine: for each down unit (slot j, tile rtd) of this CTA, rows [j rp, (j + 1) rp) of
     // the tile: every pair's output polled into shared memory, then the k-ordered weighted sums ----
-    const int rp = (RT + D - 1) / D;  // D >= K, so rp <= 13
+    const int rp = (RT + D - 1) / D;  // D >= K (K + 1 with a shared expert), so rp <= 13 (12)
+    const int NPQ = P + (p.shared ? T : 0);  // pairs polled: the routed ones, then the shared expert's
     float* cs = reinterpret_cast<float*>(sqx);  // [pair][row of the share]
-    static_assert(sizeof(float) * TT * K * ((RT + K - 1) / K) <= sizeof(QBlock) * TT * KB_GU, "share fits");
+    constexpr int CS_MAX = TT * K * ((RT + K - 1) / K) > TT * (K + 1) * ((RT + K) / (K + 1))
+                               ? TT * K * ((RT + K - 1) / K)
+                               : TT * (K + 1) * ((RT + K) / (K + 1));
+    static_assert(sizeof(float) * CS_MAX <= sizeof(QBlock) * TT * KB_GU, "share fits");
     for (int u = c; u < n_units && s_ok; u += G) {
       if (u < n_gu) continue;
       const int v = u - n_gu;
@@ -991,8 +1014,8 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
       const int r0 = j * rp, nr = min(RT, r0 + rp) - r0;
       if (nr <= 0) continue;
       const uint64_t* psrc = p.ptag + rtd * RT + r0;
-      constexpr int KC = (TT * K * ((RT + K - 1) / K) + DF_THREADS - 1) / DF_THREADS;
-      if (!poll_tagged<KC>(psrc, [nr](int x) { return (x / nr) * H + x % nr; }, P * nr, ep, cs, p.status)) {
+      constexpr int KC = (CS_MAX + DF_THREADS - 1) / DF_THREADS;
+      if (!poll_tagged<KC>(psrc, [nr](int x) { return (x / nr) * H + x % nr; }, NPQ * nr, ep, cs, p.status)) {
         if (tid == 0) s_ok = 0;
         __syncthreads();
         break;
@@ -1004,6 +1027,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
         float a = 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) a = fmaf(s_w[tt * K + k], cs[(tt * K + k) * nr + r], a);
+        if (p.shared) a += cs[(P + tt) * nr + r];
         p.out[(size_t)tt * H + row] = p.residual ? xv + a : a;
       }
       __syncthreads();
@@ -1151,6 +1175,7 @@ cudaError_t launch_decode_fused(const strata_experts_t& ex, const uint16_t* w_ro
   prm.bias = bias;
   prm.blobs = (const uint8_t*)ex.blobs;
   prm.stride = ex.blob_stride;
+  prm.shared = (const uint8_t*)ex.shared_blob;
   prm.ids_out = ids;
   prm.w_out = weights;
   prm.dots = (uint64_t*)(ws + DX_DOTS);

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
                                                          TcTile* __restrict__ half_tiles, int32_t* __restrict__ counts,
                                                          int max_tiles, int max_half_tiles, int64_t rows_cap,
-                                                         int* __restrict__ status) {
+                                                         int shared_n, int* __restrict__ status) {
   __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_nh[EMAX], s_scratch[32];
   __shared__ int s_e[EMAX], s_end[EMAX];
   __shared__ int s_bad;
@@ -110,9 +110,16 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   const int nfull = cta_exclusive_scan(s_full, s_full, EMAX, s_scratch);
   const int nwide = cta_exclusive_scan(s_wide, s_wide, EMAX, s_scratch);
   const int nnarrow = cta_exclusive_scan(s_narrow, s_narrow, EMAX, s_scratch);
-  const int ntiles = nfull + nwide + nnarrow;
   const int nhalf = cta_exclusive_scan(s_nh, s_nh, EMAX, s_scratch);
-  if ((int64_t)ppad + TCN > rows_cap) {  // cannot happen once the ranges are disjoint; kept as a bound
+  // a layer's shared expert (shared_n = T tokens, else 0): one more expert after the routed ones in
+  // every list, marked e = -1, on virtual slots [P, P + T) (slot P + t = token t) and padded rows from ppad
+  const int sfull = shared_n / TCN, srem = shared_n % TCN;
+  const int swide = srem > TCN_HALF ? 1 : 0, snarrow = (srem > 0 && srem <= TCN_HALF) ? 1 : 0;
+  const int shalf = (shared_n + TCN_HALF - 1) / TCN_HALF;
+  const int wbase = nfull + sfull, nbase = wbase + nwide + swide;  // first wide / narrow tile
+  const int ntiles = nbase + nnarrow + snarrow;
+  const int ppad_all = ppad + (shared_n + 7) / 8 * 8;
+  if ((int64_t)ppad_all + TCN > rows_cap) {  // cannot happen once the ranges are disjoint; kept as a bound
     if (i == 0) {
       set_status(status, ST_CORRUPT);
       counts[0] = counts[1] = counts[2] = counts[3] = 0;
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
     }
     if (rem > 0) {
       const int t0 = n / TCN * TCN;
-      const int idx = rem > TCN_HALF ? nfull + s_wide[i] : nfull + nwide + s_narrow[i];
+      const int idx = rem > TCN_HALF ? wbase + s_wide[i] : nbase + s_narrow[i];
       if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t0, rem, s_pad[i] + t0};
     }
     for (int t = 0; t * TCN_HALF < n; ++t) {
@@ -136,11 +143,24 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
         half_tiles[idx] = TcTile{e, q0 + t * TCN_HALF, min(TCN_HALF, n - t * TCN_HALF), s_pad[i] + t * TCN_HALF};
     }
   }
+  if (i == 0 && shared_n > 0) {
+    exps[na] = TcExpert{-1, P, shared_n, ppad};
+    for (int t = 0; t < sfull; ++t)
+      if (nfull + t < max_tiles) tiles[nfull + t] = TcTile{-1, P + t * TCN, TCN, ppad + t * TCN};
+    if (srem > 0) {
+      const int idx = swide ? wbase + nwide : nbase + nnarrow;
+      if (idx < max_tiles) tiles[idx] = TcTile{-1, P + sfull * TCN, srem, ppad + sfull * TCN};
+    }
+    for (int t = 0; t < shalf; ++t)
+      if (nhalf + t < max_half_tiles)
+        half_tiles[nhalf + t] =
+            TcTile{-1, P + t * TCN_HALF, min(TCN_HALF, shared_n - t * TCN_HALF), ppad + t * TCN_HALF};
+  }
   if (i == 0) {
-    counts[0] = na;
+    counts[0] = na + (shared_n > 0 ? 1 : 0);
     counts[1] = min(ntiles, max_tiles);
-    counts[2] = ppad;
-    counts[3] = min(nhalf, max_half_tiles);
+    counts[2] = ppad_all;
+    counts[3] = min(nhalf + shalf, max_half_tiles);
   }
 }
 
@@ -173,8 +193,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t
                                                                    const int32_t* __restrict__ counts,
                                                                    uint8_t* __restrict__ xg, int64_t rows_cap,
                                                                    int* __restrict__ status) {
-  __shared__ int s_q0[EMAX];
-  const int na = counts[0];
+  __shared__ int s_q0[EMAX + 1];  // the routed experts and a shared expert
+  const int na = min(counts[0], EMAX + 1);
   for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_q0[i] = exps[i].q0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
@@ -190,12 +210,16 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t
     const TcExpert ex = exps[lo];
     const int64_t row = ex.q0pad + (j - ex.q0);
     if (j - ex.q0 >= ex.n || row >= rows_cap) continue;  // cannot happen for a checked grouping
-    const int pr = pair[j];
-    if (pr < 0 || pr >= P) {  // a caller's bad pair: its row is left as it is (a wrong but finite column)
-      if (lane == 0) set_status(status, ST_CORRUPT);
-      continue;
+    int t = j - P;  // slots from P on are the shared expert's: slot P + t is token t
+    if (j < P) {
+      const int pr = pair[j];
+      if (pr < 0 || pr >= P) {  // a caller's bad pair: its row is left as it is (a wrong but finite column)
+        if (lane == 0) set_status(status, ST_CORRUPT);
+        continue;
+      }
+      t = pr / K;
     }
-    const int t = pr / K, c = lane & 7;
+    const int c = lane & 7;
     const uint8_t* src = x16 + (size_t)t * 128 + 16 * c;
     uint8_t* dst = xg + row * 128 + ((c ^ (int)(row & 7)) << 4);
 #pragma unroll 5
@@ -236,6 +260,7 @@ __device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_
 struct TcParams {
   const uint8_t* blobs;
   int64_t stride;
+  const uint8_t* shared_blob;  // the layer's shared expert (tiles with e = -1), or null
   int q2_offset;
   const TcTile* tiles;
   const int32_t* counts;
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
   __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_ep_pair[GU ? 1 : TCN_HALF];   // down epilogue: pair of each column of the current tile
+  __shared__ int s_ep_pair[GU ? 1 : TCN_HALF];   // down epilogue: token (fused) or pair of each column
   __shared__ float s_ep_w[GU ? 1 : TCN_HALF];     //                router weight of that pair (fused combine)
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
@@ -388,7 +413,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         const TcTile tl = item_tile<GU>(p, item, rt);
         if (tl.n == 0) continue;
         const int nrows = (tl.n + 15) / 16 * 16;
-        const uint8_t* blob = p.blobs + (int64_t)tl.e * p.stride;
+        const uint8_t* blob = tl.e >= 0 ? p.blobs + (int64_t)tl.e * p.stride : p.shared_blob;
         for (int kb = 0; kb < G::KBN; ++kb, ++it) {
           const int s = it % NS_TMA;
           if (it >= NS_TMA && !mbar_wait(&empty_tma[s], (uint32_t)((it / NS_TMA - 1) & 1), status)) {
@@ -575,11 +600,18 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
       } else {
         // the tile's pairs (and router weights) staged once per item by the epilogue threads
         named_barrier(2, 32 * EPI);  // every epilogue thread is done with the previous item's
+        // fused combine: (token, router weight) of each column, the shared expert's slots P + t with
+        // weight 1; strata_moe_experts: the pair number
         if (etid < tl.n) {
-          int pr = __ldg(p.pair + tl.q0 + etid);
-          if (pr < 0 || pr >= p.P) pr = -1;
-          s_ep_pair[etid] = pr;
-          if (p.out) s_ep_w[etid] = pr >= 0 ? __ldg(p.wts + pr) : 0.f;
+          const int slot = tl.q0 + etid;
+          int pr = slot < p.P ? __ldg(p.pair + slot) : -1;
+          if (slot < p.P && (pr < 0 || pr >= p.P)) pr = -1;
+          if (p.out) {
+            s_ep_pair[etid] = slot >= p.P ? slot - p.P : (pr >= 0 ? pr / K : -1);
+            s_ep_w[etid] = slot >= p.P ? 1.f : (pr >= 0 ? __ldg(p.wts + pr) : 0.f);
+          } else {
+            s_ep_pair[etid] = pr;
+          }
         }
         named_barrier(2, 32 * EPI);
         const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
@@ -596,9 +628,9 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
               const int col = 16 * ch + i;
               const int pr = col < tl.n ? s_ep_pair[col] : -1;
               if (pr >= 0) {
-                if (p.out) {  // fused combine: out[t] += w[t][k] * y
+                if (p.out) {  // fused combine: out[t] += w[t][k] * y (pr: the token here)
                   const float w = s_ep_w[col];
-                  float* dst = p.out + (size_t)(pr / K) * H + orow;
+                  float* dst = p.out + (size_t)pr * H + orow;
                   tc::red_add_f32(dst, w * __uint_as_float(y0[i]));
                   tc::red_add_f32(dst + 128, w * __uint_as_float(y1[i]));
                 } else {
@@ -634,12 +666,15 @@ int g_sms[64];
 
 // Rows of the padded h buffer Hg for a call with T tokens (every expert's slot range rounded up to 8
 // rows, plus a tile's width of slack for the last tile's over-read).
-int64_t tc_rows_cap(int T) { return (int64_t)T * K + 8 * EMAX + TCN; }
+int64_t tc_rows_cap(int T) { return (int64_t)T * (K + 1) + 8 * (EMAX + 1) + TCN; }
 size_t tc_x16_bytes(int T) { return (size_t)KB_GU * T * 128; }
 size_t tc_xg_bytes(int T) { return (size_t)KB_GU * tc_rows_cap(T) * 128; }
 size_t tc_hg_bytes(int T) { return (size_t)KB_D * tc_rows_cap(T) * 128; }
+// tile capacities: every expert's tiles plus the shared expert's (T more slots, one more expert)
+inline int tc_max_tiles(int T) { return T * (K + 1) / TCN + EMAX + 1; }
+inline int tc_max_half(int T) { return T * (K + 1) / TCN_HALF + EMAX + 1; }
 size_t tc_meta_bytes(int T) {
-  return sizeof(TcExpert) * EMAX + sizeof(TcTile) * (size_t)(T * K / TCN + EMAX + T * K / TCN_HALF + EMAX) + 64;
+  return sizeof(TcExpert) * (EMAX + 1) + sizeof(TcTile) * (size_t)(tc_max_tiles(T) + tc_max_half(T)) + 64;
 }
 
 cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s) {
@@ -650,17 +685,17 @@ cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16
 cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, int T, const int32_t* expert_off,
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
                               const float* weights, float* out, uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status,
-                              cudaStream_t s) {
-  const int max_tiles = T * K / TCN + EMAX, max_half = T * K / TCN_HALF + EMAX;
+                              cudaStream_t s, const void* shared_blob) {
+  const int max_tiles = tc_max_tiles(T), max_half = tc_max_half(T);
   TcExpert* exps = reinterpret_cast<TcExpert*>(meta);
-  TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * EMAX);
+  TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * (EMAX + 1));
   TcTile* half_tiles = tiles + max_tiles;
   int32_t* counts = reinterpret_cast<int32_t*>(half_tiles + max_half);
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
                                                     half_tiles, counts, max_tiles, max_half, rows_cap,
-                                                    status));
+                                                    shared_blob ? T : 0, status));
   STRATA_LAUNCH(KID_TC_GATHER, s,
                 tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x16, T, pair, T * K, exps, counts, xg,
                                                                           rows_cap, status));
@@ -673,7 +708,8 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) g_sms[dev] = sms;
   }
-  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, ex.q2_offset, tiles, counts, xg, hg, rows_cap, pair, T,
+  TcParams gp{(const uint8_t*)ex.blobs, ex.blob_stride, (const uint8_t*)shared_blob, ex.q2_offset, tiles, counts, xg,
+              hg, rows_cap, pair, T,
               T * K, nullptr, nullptr, nullptr, status};
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<true>::SMEM)) != cudaSuccess)

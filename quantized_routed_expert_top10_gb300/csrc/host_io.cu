@@ -108,7 +108,8 @@ struct HostKey {
       return false;
     for (size_t i = 0; i < ex.size(); ++i)
       if (ex[i].blobs != o.ex[i].blobs || ex[i].blob_stride != o.ex[i].blob_stride ||
-          ex[i].n_expert != o.ex[i].n_expert || ex[i].q2_offset != o.ex[i].q2_offset)
+          ex[i].n_expert != o.ex[i].n_expert || ex[i].q2_offset != o.ex[i].q2_offset ||
+          ex[i].shared_blob != o.ex[i].shared_blob)
         return false;
     return true;
   }

@@ -3,7 +3,7 @@ experts that the next router, applied to layer l's normalised input, selects for
 experts the next layer's CTAs prefetch into L2.  Checked against the oracle's routing of the same
 input with the next layer's router (up to the 1e-4 tie band).  The words are read from the decode
 exchange area of the workspace, whose layout (right after the 12 KiB header) is: router dot products
-[16][8][512], h [80][640], expert outputs [80][2560], predicted logits [8][512], then the prediction
+[16][8][512], h [88][640], expert outputs [88][2560] (routed pairs, then a shared expert's), predicted logits [8][512], then the prediction
 [1 + 80], all 64-bit (value bits, call tag) words."""
 import numpy as np
 import pytest
@@ -17,7 +17,7 @@ from gpu_common import DEV, B, device_packed_layer, to_dev, workspace
 pytestmark = pytest.mark.gpu
 
 WS_HEADER = 12288
-PRED_IDS = WS_HEADER + 8 * (16 * 8 * 512 + 80 * 640 + 80 * 2560 + 8 * 512)
+PRED_IDS = WS_HEADER + 8 * (16 * 8 * 512 + 88 * 640 + 88 * 2560 + 8 * 512)
 
 
 @pytest.mark.parametrize("T", [1, 4])
