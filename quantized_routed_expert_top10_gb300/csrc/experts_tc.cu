@@ -177,55 +177,66 @@ __global__ void __launch_bounds__(256) tc_x16_kernel(const float* __restrict__ x
   for (int i = 0; i < H / 128; ++i) tc::x16_store_chunk(__ldg(xr + lane + 32 * i), i, sc, t, T, x16);
 }
 
+// slot_of[p] = the grouping slot of pair p (the inverse of pair[]), -1 first for pairs a caller's
+// grouping leaves out; a pair number outside [0, P) sets ST_CORRUPT and is skipped.
+__global__ void __launch_bounds__(256) tc_slot_of_kernel(const int32_t* __restrict__ pair, int P,
+                                                         int32_t* __restrict__ slot_of, int* __restrict__ status) {
+  for (int j = blockIdx.x * 256 + threadIdx.x; j < P; j += gridDim.x * 256) {
+    const int pr = pair[j];
+    if (pr >= 0 && pr < P) slot_of[pr] = j;
+    else set_status(status, ST_CORRUPT);
+  }
+}
+
 // Xg[kb][row][128 B]: the padded-slot copy of the tokens the gate/up kernel bulk-copies its token tiles
 // from (one contiguous run of rows per tile and k-block): row q0pad(e) + s of expert e holds X16 row
 // (kb, token of the expert's slot s), its 16-byte chunks swizzled by row % 8 (the tensor core's 128B
-// K-major layout, so a bulk copy of a row range is an MMA operand as it lands).  One warp per slot (the
-// expert found by binary search over the experts' first slots, staged in shared memory); lane = (k-block
-// within a group of 4, chunk), so a warp moves four whole 128-byte rows per instruction.  Rows of the
-// 8-row padding between experts are not written: they only feed MMA columns the epilogues discard.
+// K-major layout, so a bulk copy of a row range is an MMA operand as it lands).  Token-major: one warp
+// per token reads its 40 X16 rows once (lane = (k-block within a group of 4, chunk): 10 16-byte pieces)
+// and writes them to the padded rows of its K slots (slot_of), and of its shared-expert slot P + t when
+// the layer has one; each slot's expert comes from a binary search over the experts' first slots,
+// staged in shared memory.  Rows of the 8-row padding between experts are not written: they only feed
+// MMA columns the epilogues discard.
 // ---------------------------------------------------------------------------------------------
 constexpr int GATHER_THREADS = 256;
-constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over slots; 4 CTAs per SM of a 152-SM GB300
+constexpr int GATHER_BLOCKS = 4 * 152;  // grid-stride over tokens; 4 CTAs per SM of a 152-SM GB300
 __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t* __restrict__ x16, int T,
-                                                                   const int32_t* __restrict__ pair, int P,
-                                                                   const TcExpert* __restrict__ exps,
+                                                                   const int32_t* __restrict__ slot_of, int P,
+                                                                   int shared, const TcExpert* __restrict__ exps,
                                                                    const int32_t* __restrict__ counts,
-                                                                   uint8_t* __restrict__ xg, int64_t rows_cap,
-                                                                   int* __restrict__ status) {
-  __shared__ int s_q0[EMAX + 1];  // the routed experts and a shared expert
+                                                                   uint8_t* __restrict__ xg, int64_t rows_cap) {
+  __shared__ int s_q0[EMAX + 1], s_shift[EMAX + 1];  // the routed experts and a shared expert
   const int na = min(counts[0], EMAX + 1);
-  for (int i = threadIdx.x; i < na; i += GATHER_THREADS) s_q0[i] = exps[i].q0;
+  for (int i = threadIdx.x; i < na; i += GATHER_THREADS) {
+    const TcExpert ex = exps[i];
+    s_q0[i] = ex.q0;
+    s_shift[i] = ex.q0pad - ex.q0;  // padded row - slot
+  }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  if (na == 0) return;
+  const int nslots = exps[na - 1].q0 + exps[na - 1].n;
+  const int lane = threadIdx.x & 31, c = lane & 7, kb0 = lane >> 3;
   const int warps = gridDim.x * (GATHER_THREADS / 32);
-  const int nslots = na > 0 ? exps[na - 1].q0 + exps[na - 1].n : 0;
-  for (int j = blockIdx.x * (GATHER_THREADS / 32) + (threadIdx.x >> 5); j < nslots; j += warps) {
-    int lo = 0, hi = na - 1;  // last expert whose first slot is <= j
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_q0[mid] <= j) lo = mid;
-      else hi = mid - 1;
-    }
-    const TcExpert ex = exps[lo];
-    const int64_t row = ex.q0pad + (j - ex.q0);
-    if (j - ex.q0 >= ex.n || row >= rows_cap) continue;  // cannot happen for a checked grouping
-    int t = j - P;  // slots from P on are the shared expert's: slot P + t is token t
-    if (j < P) {
-      const int pr = pair[j];
-      if (pr < 0 || pr >= P) {  // a caller's bad pair: its row is left as it is (a wrong but finite column)
-        if (lane == 0) set_status(status, ST_CORRUPT);
-        continue;
-      }
-      t = pr / K;
-    }
-    const int c = lane & 7;
+  for (int t = blockIdx.x * (GATHER_THREADS / 32) + (threadIdx.x >> 5); t < T; t += warps) {
+    uint4 v[KB_GU / 4];
     const uint8_t* src = x16 + (size_t)t * 128 + 16 * c;
-    uint8_t* dst = xg + row * 128 + ((c ^ (int)(row & 7)) << 4);
-#pragma unroll 5
-    for (int kb = lane >> 3; kb < KB_GU; kb += 4)
-      *reinterpret_cast<uint4*>(dst + (int64_t)kb * rows_cap * 128) =
-          __ldg(reinterpret_cast<const uint4*>(src + (size_t)kb * T * 128));
+#pragma unroll
+    for (int i = 0; i < KB_GU / 4; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(kb0 + 4 * i) * T * 128));
+    for (int k = 0; k < K + (shared ? 1 : 0); ++k) {
+      const int slot = k < K ? __ldg(slot_of + (size_t)t * K + k) : P + t;
+      if (slot < 0 || slot >= nslots) continue;  // a pair the caller's grouping leaves out
+      int lo = 0, hi = na - 1;  // last expert whose first slot is <= slot
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_q0[mid] <= slot) lo = mid;
+        else hi = mid - 1;
+      }
+      const int64_t row = (int64_t)slot + s_shift[lo];
+      if (row < 0 || row >= rows_cap) continue;  // cannot happen for a checked grouping
+      uint8_t* dst = xg + row * 128 + ((c ^ (int)(row & 7)) << 4);
+#pragma unroll
+      for (int i = 0; i < KB_GU / 4; ++i) *reinterpret_cast<uint4*>(dst + (int64_t)(kb0 + 4 * i) * rows_cap * 128) = v[i];
+    }
   }
 }
 
@@ -673,8 +684,9 @@ size_t tc_hg_bytes(int T) { return (size_t)KB_D * tc_rows_cap(T) * 128; }
 // tile capacities: every expert's tiles plus the shared expert's (T more slots, one more expert)
 inline int tc_max_tiles(int T) { return T * (K + 1) / TCN + EMAX + 1; }
 inline int tc_max_half(int T) { return T * (K + 1) / TCN_HALF + EMAX + 1; }
-size_t tc_meta_bytes(int T) {
-  return sizeof(TcExpert) * (EMAX + 1) + sizeof(TcTile) * (size_t)(tc_max_tiles(T) + tc_max_half(T)) + 64;
+size_t tc_meta_bytes(int T) {  // experts, tile lists, counts [4], slot_of [T * K]
+  return sizeof(TcExpert) * (EMAX + 1) + sizeof(TcTile) * (size_t)(tc_max_tiles(T) + tc_max_half(T)) +
+         sizeof(int32_t) * (4 + (size_t)T * K) + 64;
 }
 
 cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s) {
@@ -696,10 +708,14 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
                                                     half_tiles, counts, max_tiles, max_half, rows_cap,
                                                     shared_blob ? T : 0, status));
+  int32_t* slot_of = counts + 4;  // [T * K], after the counts in the tile-list area
+  cudaError_t err = cudaMemsetAsync(slot_of, 0xFF, sizeof(int32_t) * (size_t)T * K, s);
+  if (err != cudaSuccess) return err;
+  STRATA_LAUNCH(KID_TC_GATHER, s, tc_slot_of_kernel<<<GATHER_BLOCKS, 256, 0, s>>>(pair, T * K, slot_of, status));
   STRATA_LAUNCH(KID_TC_GATHER, s,
-                tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x16, T, pair, T * K, exps, counts, xg,
-                                                                          rows_cap, status));
-  cudaError_t err = cudaGetLastError();
+                tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x16, T, slot_of, T * K, shared_blob ? 1 : 0,
+                                                                          exps, counts, xg, rows_cap));
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
