@@ -186,9 +186,15 @@ KERNEL_SOURCES = {
 # time: once a source changes the figure no longer describes the kernel (null).  A stack workload's
 # per-launch figure is one layer's launch, captured on its first layer (--layers 1).
 NCU_TRAFFIC = {
-    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches (29,614,848 / 29,607,680 /
-    # 29,626,880 B read, 8,448 / 0 / 0 B written)
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29619285, "5ad4c6c9dc1077e8"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29598208, "82aebf2094784d96"),
+    ("decode_1tok_1layer", "DECODE_LAYER"): (16676864, "82aebf2094784d96"),
+    # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean over the 48 launches of one step
+    ("decode_1tok_48layer_stack", "DECODE_LAYER"): (19522256, "82aebf2094784d96"),
+    # profiles/tc_expert_kernel_prefill_8192tok_48layer_stack.md: mean over the 48 launches of each
+    # expert kernel in one step (a single-pass capture of the full workload)
+    ("prefill_8192tok_48layer_stack", "TC_GATEUP"): (546866048, "82bc9c2b8c6e2894"),
+    ("prefill_8192tok_48layer_stack", "TC_DOWN"): (259693445, "82bc9c2b8c6e2894"),
 }
 
 

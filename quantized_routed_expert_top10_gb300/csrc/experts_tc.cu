@@ -583,6 +583,8 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     const int q = warp & 3;
     const int erow = 32 * q + lane;
     const int epart = (warp - 12) >> 2;  // down: which half of each item's 16-column chunks this warp drains
+    // down, fused combine: the layer output's lines stay in L2 while every expert adds into them
+    const uint64_t keep = tc::policy_evict_last();
     const int etid = tid - 12 * 32;      // 0 .. 32 * EPI - 1
     int n_small = 0;
     int uses[2] = {0, 0};  // items drained from each TMEM half so far (same assignment as the issuer)
@@ -642,8 +644,8 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
                 if (p.out) {  // fused combine: out[t] += w[t][k] * y (pr: the token here)
                   const float w = s_ep_w[col];
                   float* dst = p.out + (size_t)pr * H + orow;
-                  tc::red_add_f32(dst, w * __uint_as_float(y0[i]));
-                  tc::red_add_f32(dst + 128, w * __uint_as_float(y1[i]));
+                  tc::red_add_f32_hint(dst, w * __uint_as_float(y0[i]), keep);
+                  tc::red_add_f32_hint(dst + 128, w * __uint_as_float(y1[i]), keep);
                 } else {
                   float* dst = p.parts + (size_t)pr * H + orow;
                   dst[0] = __uint_as_float(y0[i]);

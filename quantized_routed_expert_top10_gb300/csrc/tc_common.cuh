@@ -58,9 +58,14 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
-// fp32 reduction into global memory (no return value).
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+// fp32 reduction into global memory (no return value) with an L2 eviction-policy hint.
+__device__ __forceinline__ void red_add_f32_hint(float* p, float v, uint64_t policy) {
+  asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // The fp16 token copy the tensor-core expert path reads its token tiles from: X16[kb][t][128 bytes] =
