@@ -20,7 +20,7 @@
 //   warp 2      owns the TMEM allocation;
 //   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
 //               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
-//               exact) in a 2-stage ring of weight tiles;
+//               exact) in a 2-stage (gate/up) or 3-stage (down) ring of weight tiles;
 //   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (one half for a tile of up to 128
 //               tokens, both for a wider one) and commits to the stages' "empty" mbarriers;
 //   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
@@ -311,7 +311,9 @@ struct TcGeo {
   static constexpr uint32_t B_TILE = (GU ? TCN : TCN_HALF) * 128;  // token rows x 64 fp16
   static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
   static constexpr int NS_TMA = GU ? 4 : 6;            // stages of (token tile, code chunks)
-  static constexpr int NS_A = 2;                       // stages of dequantised weight tiles
+  // stages of dequantised weight tiles: down's k-block of MMAs is shorter than its dequantisation, so
+  // it takes a third stage (the dequantisers then work two k-blocks ahead of the tensor core)
+  static constexpr int NS_A = GU ? 2 : 3;
   static constexpr uint32_t A_STAGE = NMAT * A_TILE;
   static constexpr uint32_t TMEM_COLS = 512;           // two halves of NMAT x 128 columns
   static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
@@ -581,7 +583,6 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     // ---------------- epilogue ----------------
     constexpr int EPI = tc_epi_warps<GU>();
     const int q = warp & 3;
-    const int erow = 32 * q + lane;
     const int epart = (warp - 12) >> 2;  // down: which half of each item's 16-column chunks this warp drains
     // down, fused combine: the layer output's lines stay in L2 while every expert adds into them
     const uint64_t keep = tc::policy_evict_last();
@@ -627,7 +628,10 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
           }
         }
         named_barrier(2, 32 * EPI);
-        const int orow = 2 * rt * 128 + erow;  // rows of the pair's first tile; the second is 128 further
+        // each 4 x 4 block of (rows, columns) is transposed across 4 lanes, so that lane 4g + j writes
+        // rows 4g .. 4g + 3 of column j: one 16-byte reduction (or store) instead of four
+        const int j4 = lane & 3;
+        const int orow = 2 * rt * 128 + 32 * q + 4 * (lane >> 2);  // pair's first tile; the second is 128 further
         const int nch = nrows / 16, half = (nch + 1) / 2;
 #pragma unroll 1
         for (int ch = epart * half; ch < min(nch, (epart + 1) * half); ++ch) {
@@ -635,22 +639,26 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
           tc::tmem_ld16_async(acc + 16 * ch, y0);
           tc::tmem_ld16_async(acc + mat_cols + 16 * ch, y1);
           tc::tmem_wait_ld();
-          if (ok) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int col = 16 * ch + i;
-              const int pr = col < tl.n ? s_ep_pair[col] : -1;
-              if (pr >= 0) {
-                if (p.out) {  // fused combine: out[t] += w[t][k] * y (pr: the token here)
-                  const float w = s_ep_w[col];
-                  float* dst = p.out + (size_t)pr * H + orow;
-                  tc::red_add_f32_hint(dst, w * __uint_as_float(y0[i]), keep);
-                  tc::red_add_f32_hint(dst + 128, w * __uint_as_float(y1[i]), keep);
-                } else {
-                  float* dst = p.parts + (size_t)pr * H + orow;
-                  dst[0] = __uint_as_float(y0[i]);
-                  dst[128] = __uint_as_float(y1[i]);
-                }
+          for (int m = 0; m < 4; ++m) {
+            uint32_t a[4] = {y0[4 * m], y0[4 * m + 1], y0[4 * m + 2], y0[4 * m + 3]};
+            uint32_t b[4] = {y1[4 * m], y1[4 * m + 1], y1[4 * m + 2], y1[4 * m + 3]};
+            tc::transpose4_lanes(a, j4);
+            tc::transpose4_lanes(b, j4);
+            const int col = 16 * ch + 4 * m + j4;
+            const int pr = col < tl.n ? s_ep_pair[col] : -1;
+            if (ok && pr >= 0) {
+              if (p.out) {  // fused combine: out[t] += w[t][k] * y (pr: the token here)
+                const float w = s_ep_w[col];
+                float* dst = p.out + (size_t)pr * H + orow;
+                tc::red_add_v4_f32_hint(dst, w * __uint_as_float(a[0]), w * __uint_as_float(a[1]),
+                                        w * __uint_as_float(a[2]), w * __uint_as_float(a[3]), keep);
+                tc::red_add_v4_f32_hint(dst + 128, w * __uint_as_float(b[0]), w * __uint_as_float(b[1]),
+                                        w * __uint_as_float(b[2]), w * __uint_as_float(b[3]), keep);
+              } else {
+                float* dst = p.parts + (size_t)pr * H + orow;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(a[0], a[1], a[2], a[3]);
+                *reinterpret_cast<uint4*>(dst + 128) = make_uint4(b[0], b[1], b[2], b[3]);
               }
             }
           }

@@ -62,6 +62,26 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 __device__ __forceinline__ void red_add_f32_hint(float* p, float v, uint64_t policy) {
   asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
 }
+// Four consecutive fp32 reductions (16-byte aligned address) with an L2 eviction-policy hint.
+__device__ __forceinline__ void red_add_v4_f32_hint(float* p, float a, float b, float c, float d, uint64_t policy) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d), "l"(policy)
+               : "memory");
+}
+
+// 4 x 4 transpose across the lanes 4g .. 4g + 3 of a warp (j = lane & 3): lane j holds row j of the
+// block in v[0..3] on entry and column j (rows 0..3) on return.  Two butterfly steps, lane distance 2
+// then 1, each exchanging one half of the lane's values.
+__device__ __forceinline__ void transpose4_lanes(uint32_t (&v)[4], int j) {
+  const bool a2 = (j & 2) != 0, a1 = (j & 1) != 0;
+  uint32_t r0 = __shfl_xor_sync(0xffffffffu, a2 ? v[0] : v[2], 2);
+  uint32_t r1 = __shfl_xor_sync(0xffffffffu, a2 ? v[1] : v[3], 2);
+  if (a2) { v[0] = r0; v[1] = r1; } else { v[2] = r0; v[3] = r1; }
+  r0 = __shfl_xor_sync(0xffffffffu, a1 ? v[0] : v[1], 1);
+  r1 = __shfl_xor_sync(0xffffffffu, a1 ? v[2] : v[3], 1);
+  if (a1) { v[0] = r0; v[2] = r1; } else { v[1] = r0; v[3] = r1; }
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
