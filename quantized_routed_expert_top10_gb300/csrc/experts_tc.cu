@@ -9,23 +9,27 @@
 // Per expert e with n_e tokens (its slots in the grouping), two grouped GEMMs with the weights as the
 // M = 128 operand ("swap AB") and the expert's tokens as N (up to 256 per tile):
 //   gate/up:  [g; u] (2 x 128 rows x N) = [G_rt; U_rt] (128 x 2560) * X_e^T, h = silu(g) * u -> Hg (fp16)
-//   down:     [y_2rp; y_2rp+1] (2 x 128 rows x N) = [D_2rp; D_2rp+1] (128 x 640 each) * H_e^T; two row
-//             tiles per item so each token tile is read half as often.  In a layer call the epilogue
-//             adds w[t][k] * y into the layer output (fp32 reductions: the combine step, fused), so no
+//   down:     y_rt (128 rows x N) = D_rt (128 x 640) * H_e^T.  In a layer call the epilogue adds
+//             w[t][k] * y into the layer output (fp32 reductions: the combine step, fused), so no
 //             per-pair output is stored; strata_moe_experts stores y per pair instead.
+// A tcgen05.mma costs its issuing thread about 100 cycles whatever N is, and one of N = 128 only ~70
+// cycles of tensor time, so both kernels take the widest token tiles (N = 256): one MMA instruction
+// then carries 128 x 256 x 16 multiply-adds.
 // Warp roles in each persistent CTA (one per SM; work items = (tile, 128-row tile of the weights)):
 //   warp 0      streams the token tile (gate/up: from Xg, the tokens copied once per layer into padded-slot
 //               order by tc_gather_kernel; down: from Hg) and the Q2_0 code chunk of each 64-wide
-//               k-block with cp.async.bulk into a 4-stage (gate/up) or 6-stage (down) ring;
+//               k-block with cp.async.bulk into a 4-stage (gate/up) or 5-stage (down) ring;
 //   warp 2      owns the TMEM allocation;
 //   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
 //               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
 //               exact) in a 2-stage (gate/up) or 3-stage (down) ring of weight tiles;
-//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (one half for a tile of up to 128
-//               tokens, both for a wider one) and commits to the stages' "empty" mbarriers;
+//   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (gate/up: one half for a tile of up to
+//               128 tokens, both for a wider one; down: one half per item) and commits to the stages'
+//               "empty" mbarriers;
 //   warps 12-15 read the finished buffer with tcgen05.ld (one weight row per TMEM lane) and write the
 //               epilogue while the next item accumulates into the other buffer; the down kernel runs
-//               four more (warps 16-19, 640 threads), two warps per lane quadrant splitting the columns.
+//               twelve more (warps 16-27, 896 threads), four warps per lane quadrant splitting the
+//               columns.
 // Every wait is bounded (STRATA_E_TIMEOUT).
 //
 // In-block order: the dequantiser emits the 64 weights of a block in the order pi (per 16 weights:
@@ -45,10 +49,10 @@ constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 64 fp16
 __host__ __device__ __forceinline__ int pi16_inv(int j) { return 2 * (j & 3) + 8 * ((j >> 2) & 1) + ((j >> 3) & 1); }
 
 struct TcExpert { int32_t e, q0, n, q0pad; };    // grouping slots [q0, q0+n), padded rows from q0pad
-struct TcTile { int32_t e, q0, n, q0pad; };      // <= 128 tokens of one expert
+struct TcTile { int32_t e, q0, n, q0pad; };      // <= 256 tokens of one expert
 
 // ---------------------------------------------------------------------------------------------
-// Tile lists: experts' padded row ranges (multiples of 8) and tiles of at most 128 tokens.  The
+// Tile list: experts' padded row ranges (multiples of 8) and tiles of at most 256 tokens.  The
 // grouping may come from the caller, so it is checked before any tile is listed: every active entry
 // must name an expert in [0, E) whose slot range lies in [0, P), the entries must be strictly
 // increasing and their ranges in the same order without overlap (so the padded rows of all experts fit
@@ -59,10 +63,9 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ active,
                                                          const int32_t* __restrict__ n_active, int E, int P,
                                                          TcExpert* __restrict__ exps, TcTile* __restrict__ tiles,
-                                                         TcTile* __restrict__ half_tiles, int32_t* __restrict__ counts,
-                                                         int max_tiles, int max_half_tiles, int64_t rows_cap,
+                                                         int32_t* __restrict__ counts, int max_tiles, int64_t rows_cap,
                                                          int shared_n, int* __restrict__ status) {
-  __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_nh[EMAX], s_scratch[32];
+  __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_scratch[32];
   __shared__ int s_e[EMAX], s_end[EMAX];
   __shared__ int s_bad;
   const int i = threadIdx.x;
@@ -104,18 +107,15 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   s_full[i] = (i < na) ? n / TCN : 0;
   s_wide[i] = (i < na && rem > TCN_HALF) ? 1 : 0;
   s_narrow[i] = (i < na && rem > 0 && rem <= TCN_HALF) ? 1 : 0;
-  s_nh[i] = (i < na) ? (n + TCN_HALF - 1) / TCN_HALF : 0;
   __syncthreads();
   const int ppad = cta_exclusive_scan(s_pad, s_pad, EMAX, s_scratch);
   const int nfull = cta_exclusive_scan(s_full, s_full, EMAX, s_scratch);
   const int nwide = cta_exclusive_scan(s_wide, s_wide, EMAX, s_scratch);
   const int nnarrow = cta_exclusive_scan(s_narrow, s_narrow, EMAX, s_scratch);
-  const int nhalf = cta_exclusive_scan(s_nh, s_nh, EMAX, s_scratch);
   // a layer's shared expert (shared_n = T tokens, else 0): one more expert after the routed ones in
   // every list, marked e = -1, on virtual slots [P, P + T) (slot P + t = token t) and padded rows from ppad
   const int sfull = shared_n / TCN, srem = shared_n % TCN;
   const int swide = srem > TCN_HALF ? 1 : 0, snarrow = (srem > 0 && srem <= TCN_HALF) ? 1 : 0;
-  const int shalf = (shared_n + TCN_HALF - 1) / TCN_HALF;
   const int wbase = nfull + sfull, nbase = wbase + nwide + swide;  // first wide / narrow tile
   const int ntiles = nbase + nnarrow + snarrow;
   const int ppad_all = ppad + (shared_n + 7) / 8 * 8;
@@ -137,11 +137,6 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
       const int idx = rem > TCN_HALF ? wbase + s_wide[i] : nbase + s_narrow[i];
       if (idx < max_tiles) tiles[idx] = TcTile{e, q0 + t0, rem, s_pad[i] + t0};
     }
-    for (int t = 0; t * TCN_HALF < n; ++t) {
-      const int idx = s_nh[i] + t;
-      if (idx < max_half_tiles)
-        half_tiles[idx] = TcTile{e, q0 + t * TCN_HALF, min(TCN_HALF, n - t * TCN_HALF), s_pad[i] + t * TCN_HALF};
-    }
   }
   if (i == 0 && shared_n > 0) {
     exps[na] = TcExpert{-1, P, shared_n, ppad};
@@ -151,16 +146,12 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
       const int idx = swide ? wbase + nwide : nbase + nnarrow;
       if (idx < max_tiles) tiles[idx] = TcTile{-1, P + sfull * TCN, srem, ppad + sfull * TCN};
     }
-    for (int t = 0; t < shalf; ++t)
-      if (nhalf + t < max_half_tiles)
-        half_tiles[nhalf + t] =
-            TcTile{-1, P + t * TCN_HALF, min(TCN_HALF, shared_n - t * TCN_HALF), ppad + t * TCN_HALF};
   }
   if (i == 0) {
     counts[0] = na + (shared_n > 0 ? 1 : 0);
     counts[1] = min(ntiles, max_tiles);
     counts[2] = ppad_all;
-    counts[3] = min(nhalf + shalf, max_half_tiles);
+    counts[3] = 0;  // unused (keeps slot_of, after the counts, 16-byte aligned)
   }
 }
 
@@ -246,26 +237,41 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t
 // (bits 2m, 2m + 1) of both bytes.  OR-ing the field into the mantissa of M_m = 2^(10 - 2m), whose
 // last-place unit sits at bit 2m, gives M_m + code in one LOP3; subtracting M_m + q2_offset and
 // multiplying by d are exact.
-__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r) {
-  const __half2 d2 = __half2half2(d);
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-  __half2 sub[4];
+struct DequantConsts {
+  __half2 d2, sub[4];
+  __device__ __forceinline__ DequantConsts(__half d, int q2_offset) : d2(__half2half2(d)) {
 #pragma unroll
-  for (int m = 0; m < 4; ++m) sub[m] = __half2half2(__float2half_rn((float)((1024 >> (2 * m)) + q2_offset)));
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t word = (c & 1) ? (w[c >> 1] >> 8) : w[c >> 1];
-    uint32_t out[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t magic = (uint32_t)((25 - 2 * m) << 10) * 0x00010001u;  // half2(2^(10 - 2m))
-      const uint32_t bits = (word & (0x00030003u << (2 * m))) | magic;       // half2(M_m + code)
-      __half2 h = *reinterpret_cast<const __half2*>(&bits);
-      h = __hmul2(__hsub2(h, sub[m]), d2);                                   // (code - q2_offset) * d
-      out[m] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(tile + tc::swz_off(r, c)) = make_uint4(out[0], out[1], out[2], out[3]);
+    for (int m = 0; m < 4; ++m) sub[m] = __half2half2(__float2half_rn((float)((1024 >> (2 * m)) + q2_offset)));
   }
+};
+// Chunk c of row r from the code word holding its bytes in bits 0..7 and 16..23.
+__device__ __forceinline__ void dequant_chunk(uint32_t word, const DequantConsts& k, uint8_t* tile, int r, int c) {
+  uint32_t out[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t magic = (uint32_t)((25 - 2 * m) << 10) * 0x00010001u;  // half2(2^(10 - 2m))
+    const uint32_t bits = (word & (0x00030003u << (2 * m))) | magic;       // half2(M_m + code)
+    __half2 h = *reinterpret_cast<const __half2*>(&bits);
+    h = __hmul2(__hsub2(h, k.sub[m]), k.d2);                               // (code - q2_offset) * d
+    out[m] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(tile + tc::swz_off(r, c)) = make_uint4(out[0], out[1], out[2], out[3]);
+}
+__device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r) {
+  const DequantConsts k(d, q2_offset);
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) dequant_chunk((c & 1) ? (w[c >> 1] >> 8) : w[c >> 1], k, tile, r, c);
+}
+// Half hf of the row: chunks 4 hf .. 4 hf + 3, i.e. the 16-groups held by code words 2 hf and 2 hf + 1.
+__device__ __forceinline__ void dequant_half_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r,
+                                                 int hf) {
+  const DequantConsts k(d, q2_offset);
+  const uint32_t wa = hf ? codes.z : codes.x, wb = hf ? codes.w : codes.y;
+  dequant_chunk(wa, k, tile, r, 4 * hf);
+  dequant_chunk(wa >> 8, k, tile, r, 4 * hf + 1);
+  dequant_chunk(wb, k, tile, r, 4 * hf + 2);
+  dequant_chunk(wb >> 8, k, tile, r, 4 * hf + 3);
 }
 
 struct TcParams {
@@ -288,34 +294,36 @@ struct TcParams {
 };
 
 // Kernel geometry.  Warp 0: copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
-// dequantisers (256 threads, one weight row of one of the item's two 128-row matrices each);
-// warps 12..15 (down: 12..19): epilogue (one TMEM lane = one weight row per thread).
-// gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.
-// down (GU = false): item = (tile, pair of row tiles 2rp, 2rp + 1 of down): both share the token tile.
-// TMEM: a tile of up to 128 tokens accumulates in half b (alternating) -- matrix j in columns
-// [b*256 + j*128, +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256
-// tokens, one dequantised weight tile serving all of them) takes both halves, matrix j in [j*256, +256).
+// dequantisers (256 threads: gate/up, one weight row of one of the item's two 128-row matrices each;
+// down, half a row of its one matrix); warps 12..15 (down: 12..19): epilogue (one TMEM lane = one
+// weight row per thread).
+// gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.  TMEM: a
+// tile of up to 128 tokens accumulates in half b (alternating) -- matrix j in columns [b*256 + j*128,
+// +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256 tokens, one
+// dequantised weight tile serving all of them) takes both halves, matrix j in [j*256, +256).
+// down (GU = false): item = (tile, row tile rt of down), one matrix in half b (alternating), columns
+// [b*256, +256): every item's epilogue overlaps the next one's main loop.
 // Threads per CTA: 16 warps for gate/up (its 125 registers per thread allow no more); the down kernel
-// (96 registers) runs 20, the last 8 of them epilogue warps, two per TMEM lane quadrant, because its
-// epilogue -- 256 fp32 reductions per thread and 128-token item -- is what it waits on.
+// (at most 72 registers) runs 28, the last 16 of them epilogue warps, four per TMEM lane quadrant,
+// because its epilogue -- 32k fp32 reductions per item, latency-bound -- is what it waits on.
 template <bool GU>
-constexpr int tc_threads() { return GU ? 512 : 640; }
+constexpr int tc_epi_warps() { return GU ? 4 : 16; }
 template <bool GU>
-constexpr int tc_epi_warps() { return GU ? 4 : 8; }
+constexpr int tc_threads() { return 32 * (12 + tc_epi_warps<GU>()); }  // warps 0..11, then the epilogue
 template <bool GU>
 struct TcGeo {
-  static constexpr int NMAT = 2;
+  static constexpr int NMAT = GU ? 2 : 1;                 // weight matrices per item
   static constexpr int KBN = GU ? KB_GU : KB_D;          // k-blocks per item
-  static constexpr int RTN = GU ? RT_GU : RT_D / 2;      // weight row tiles (or pairs) per token tile
-  static constexpr int CODE = GU ? GU_CHUNK : 2 * D_CHUNK; // code bytes per k-block
-  static constexpr uint32_t B_TILE = (GU ? TCN : TCN_HALF) * 128;  // token rows x 64 fp16
+  static constexpr int RTN = GU ? RT_GU : RT_D;          // weight row tiles per token tile
+  static constexpr int CODE = GU ? GU_CHUNK : D_CHUNK;   // code bytes per k-block
+  static constexpr uint32_t B_TILE = TCN * 128;          // token rows x 64 fp16
   static constexpr uint32_t TMA_STAGE = (B_TILE + CODE + 1023) / 1024 * 1024;  // token tile, then codes
-  static constexpr int NS_TMA = GU ? 4 : 6;            // stages of (token tile, code chunks)
-  // stages of dequantised weight tiles: down's k-block of MMAs is shorter than its dequantisation, so
-  // it takes a third stage (the dequantisers then work two k-blocks ahead of the tensor core)
+  static constexpr int NS_TMA = GU ? 4 : 5;            // stages of (token tile, code chunks)
+  // stages of dequantised weight tiles: down's k-block of MMAs is short, so it takes a third stage (the
+  // dequantisers then work two k-blocks ahead of the tensor core)
   static constexpr int NS_A = GU ? 2 : 3;
   static constexpr uint32_t A_STAGE = NMAT * A_TILE;
-  static constexpr uint32_t TMEM_COLS = 512;           // two halves of NMAT x 128 columns
+  static constexpr uint32_t TMEM_COLS = 512;           // two halves of 256 columns
   static constexpr size_t SMEM = (size_t)NS_TMA * TMA_STAGE + (size_t)NS_A * A_STAGE + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
@@ -364,9 +372,19 @@ __device__ __forceinline__ void wide_split(int nch, int part, int& c0, int& c1) 
 }
 constexpr int WIDE_BAR = 3;  // named barriers 3..6: epilogue warp 12 + q with dequantiser warps 4 + q, 8 + q
 
-// Item -> (token tile, weight row tile rt).  Gate/up items take tiles of up to 256 tokens (one
-// dequantised weight tile serves all of them); down items take tiles of up to 128 tokens, so their
-// short 10-k-block main loops keep double-buffered accumulators.
+// Items so far in each TMEM half (two counters read and bumped by selects, so that a runtime half
+// number never indexes a local array).
+struct HalfUses {
+  int u0 = 0, u1 = 0;
+  __device__ __forceinline__ int operator[](int h) const { return h ? u1 : u0; }
+  __device__ __forceinline__ void bump(int h) {
+    u0 += h ? 0 : 1;
+    u1 += h ? 1 : 0;
+  }
+};
+
+// Item -> (token tile of up to 256 tokens, weight row tile rt): one dequantised weight tile serves all
+// of the tile's tokens.
 template <bool GU>
 __device__ __forceinline__ TcTile item_tile(const TcParams& p, int item, int& rt) {
   rt = item % TcGeo<GU>::RTN;
@@ -386,8 +404,8 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   __shared__ uint64_t full_tma[NS_TMA], empty_tma[NS_TMA], full_a[NS_A], empty_a[NS_A];
   __shared__ uint64_t tmem_full[2], tmem_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_ep_pair[GU ? 1 : TCN_HALF];   // down epilogue: token (fused) or pair of each column
-  __shared__ float s_ep_w[GU ? 1 : TCN_HALF];     //                router weight of that pair (fused combine)
+  __shared__ int s_ep_pair[GU ? 1 : TCN];   // down epilogue: token (fused) or pair of each column
+  __shared__ float s_ep_w[GU ? 1 : TCN];     //                router weight of that pair (fused combine)
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -413,7 +431,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int n_items = p.counts[GU ? 1 : 3] * G::RTN;
+  const int n_items = p.counts[1] * G::RTN;
   int* status = p.status;
 
   if (warp == 0) {
@@ -443,10 +461,8 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
                               blob + ((int64_t)(rt * (RT / SLAB) + sl) * KB_GU + kb) * SLAB_KB, SLAB_KB,
                               &full_tma[s], pol);
           } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              bulk_g2s_stream(st + B_TILE + h * D_CHUNK, blob + D_REGION + ((int64_t)(2 * rt + h) * KB_D + kb) * D_CHUNK,
-                              D_CHUNK, &full_tma[s], pol);
+            bulk_g2s_stream(st + B_TILE, blob + D_REGION + ((int64_t)rt * KB_D + kb) * D_CHUNK, D_CHUNK, &full_tma[s],
+                            pol);
           }
         }
       }
@@ -457,16 +473,16 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       int it = 0, n_small = 0;
-      int uses[2] = {0, 0};  // items issued into each TMEM half so far
+      HalfUses uses;  // items issued into each TMEM half so far
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
         int rt;
         const TcTile tl = item_tile<GU>(p, item, rt);
         if (tl.n == 0) continue;
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
-        // a tile wider than 128 takes both halves (matrix j in half j); a narrower one takes half b,
-        // alternating, matrix j at column b * 256 + 128 j
-        const bool wide = nrows > TCN_HALF;
+        // gate/up: a tile wider than 128 takes both halves (matrix j in half j); a narrower one takes
+        // half b, alternating, matrix j at column b * 256 + 128 j.  down: half b, alternating.
+        const bool wide = GU && nrows > TCN_HALF;
         const int b = wide ? 0 : (n_small++ & 1);
         bool okw = true;
         for (int h = 0; h < 2; ++h)
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         for (int h = 0; h < 2; ++h)
           if (wide || h == b) {
             tc::mma_commit(&tmem_full[h]);
-            ++uses[h];
+            uses.bump(h);
           }
       }
       tc::mma_commit(&mma_done);  // every MMA this thread issued has finished before TMEM is released
@@ -513,12 +529,13 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   } else if (warp >= 4 && warp < 12) {
     // ---------------- dequantisers ----------------
     const int dt = tid - 128;
-    const int row = dt & 127, sub = dt >> 7;  // matrix of the item
+    const int row = dt & 127, sub = dt >> 7;  // gate/up: matrix of the item; down: half of the row
     int it = 0;
     bool ok = true;
     // gate/up: the TMEM use of every item, tracked as the issuer assigns it, so that a 256-token tile's
     // epilogue can be joined once the next item's first NS_A stages are dequantised (or after the last item)
-    int n_small = 0, uses[2] = {0, 0};
+    int n_small = 0;
+    HalfUses uses;
     struct Pending { bool wide; TcTile tl; int rt; uint32_t par0, par1; };
     Pending pend{false, TcTile{0, 0, 0, 0}, 0, 0u, 0u};
     auto help_wide = [&](const Pending& pd) {
@@ -541,7 +558,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         const int b = wide ? 0 : (n_small++ & 1);
         cur.wide = wide;
         for (int h = 0; h < 2; ++h)
-          if (wide || h == b) ++uses[h];
+          if (wide || h == b) uses.bump(h);
       }
       for (int kb = 0; kb < G::KBN; ++kb, ++it) {
         const int s = it % NS_TMA, sa = it % NS_A;
@@ -563,11 +580,11 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
             cw = *reinterpret_cast<const uint4*>(pc + sub * 256 + 16 * rr);
             d = *reinterpret_cast<const __half*>(pc + 512 + 4 * rr + 2 * sub);
           } else {
-            const uint8_t* cb = code + sub * D_CHUNK;
-            cw = *reinterpret_cast<const uint4*>(cb + 16 * row);
-            d = *reinterpret_cast<const __half*>(cb + 2048 + 2 * row);
+            cw = *reinterpret_cast<const uint4*>(code + 16 * row);
+            d = *reinterpret_cast<const __half*>(code + 2048 + 2 * row);
           }
-          dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
+          if (GU) dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
+          else dequant_half_row(cw, d, p.q2_offset, ast, row, sub);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -583,19 +600,19 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     // ---------------- epilogue ----------------
     constexpr int EPI = tc_epi_warps<GU>();
     const int q = warp & 3;
-    const int epart = (warp - 12) >> 2;  // down: which half of each item's 16-column chunks this warp drains
+    const int epart = (warp - 12) >> 2;  // down: which part of each item's 16-column chunks this warp drains
     // down, fused combine: the layer output's lines stay in L2 while every expert adds into them
     const uint64_t keep = tc::policy_evict_last();
     const int etid = tid - 12 * 32;      // 0 .. 32 * EPI - 1
     int n_small = 0;
-    int uses[2] = {0, 0};  // items drained from each TMEM half so far (same assignment as the issuer)
+    HalfUses uses;  // items drained from each TMEM half so far (same assignment as the issuer)
     bool ok = true;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       int rt;
       const TcTile tl = item_tile<GU>(p, item, rt);
       if (tl.n == 0) continue;
       const int nrows = (tl.n + 15) / 16 * 16;
-      const bool wide = nrows > TCN_HALF;
+      const bool wide = GU && nrows > TCN_HALF;
       const int b = wide ? 0 : (n_small++ & 1);
       for (int h = 0; h < 2; ++h)
         if (wide || h == b) ok = ok && mbar_wait(&tmem_full[h], (uint32_t)(uses[h] & 1), status);
@@ -631,34 +648,28 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         // each 4 x 4 block of (rows, columns) is transposed across 4 lanes, so that lane 4g + j writes
         // rows 4g .. 4g + 3 of column j: one 16-byte reduction (or store) instead of four
         const int j4 = lane & 3;
-        const int orow = 2 * rt * 128 + 32 * q + 4 * (lane >> 2);  // pair's first tile; the second is 128 further
-        const int nch = nrows / 16, half = (nch + 1) / 2;
+        const int orow = rt * 128 + 32 * q + 4 * (lane >> 2);
+        constexpr int EPARTS = EPI / 4;  // warps per TMEM lane quadrant
+        const int nch = nrows / 16, per = (nch + EPARTS - 1) / EPARTS;
 #pragma unroll 1
-        for (int ch = epart * half; ch < min(nch, (epart + 1) * half); ++ch) {
-          uint32_t y0[16], y1[16];
-          tc::tmem_ld16_async(acc + 16 * ch, y0);
-          tc::tmem_ld16_async(acc + mat_cols + 16 * ch, y1);
+        for (int ch = epart * per; ch < min(nch, (epart + 1) * per); ++ch) {
+          uint32_t y[16];
+          tc::tmem_ld16_async(acc + 16 * ch, y);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            uint32_t a[4] = {y0[4 * m], y0[4 * m + 1], y0[4 * m + 2], y0[4 * m + 3]};
-            uint32_t b[4] = {y1[4 * m], y1[4 * m + 1], y1[4 * m + 2], y1[4 * m + 3]};
+            uint32_t a[4] = {y[4 * m], y[4 * m + 1], y[4 * m + 2], y[4 * m + 3]};
             tc::transpose4_lanes(a, j4);
-            tc::transpose4_lanes(b, j4);
             const int col = 16 * ch + 4 * m + j4;
             const int pr = col < tl.n ? s_ep_pair[col] : -1;
-            if (ok && pr >= 0) {
+            if (ok && pr >= 0 && pr < (p.out ? p.T : p.P)) {
               if (p.out) {  // fused combine: out[t] += w[t][k] * y (pr: the token here)
                 const float w = s_ep_w[col];
-                float* dst = p.out + (size_t)pr * H + orow;
-                tc::red_add_v4_f32_hint(dst, w * __uint_as_float(a[0]), w * __uint_as_float(a[1]),
-                                        w * __uint_as_float(a[2]), w * __uint_as_float(a[3]), keep);
-                tc::red_add_v4_f32_hint(dst + 128, w * __uint_as_float(b[0]), w * __uint_as_float(b[1]),
-                                        w * __uint_as_float(b[2]), w * __uint_as_float(b[3]), keep);
+                tc::red_add_v4_f32_hint(p.out + (size_t)pr * H + orow, w * __uint_as_float(a[0]),
+                                        w * __uint_as_float(a[1]), w * __uint_as_float(a[2]),
+                                        w * __uint_as_float(a[3]), keep);
               } else {
-                float* dst = p.parts + (size_t)pr * H + orow;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(a[0], a[1], a[2], a[3]);
-                *reinterpret_cast<uint4*>(dst + 128) = make_uint4(b[0], b[1], b[2], b[3]);
+                *reinterpret_cast<uint4*>(p.parts + (size_t)pr * H + orow) = make_uint4(a[0], a[1], a[2], a[3]);
               }
             }
           }
@@ -670,7 +681,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         for (int h = 0; h < 2; ++h)
           if (wide || h == b) mbar_arrive(&tmem_empty[h]);
       for (int h = 0; h < 2; ++h)
-        if (wide || h == b) ++uses[h];
+        if (wide || h == b) uses.bump(h);
     }
   }
   tc::fence_before_sync();
@@ -691,11 +702,10 @@ int64_t tc_rows_cap(int T) { return (int64_t)T * (K + 1) + 8 * (EMAX + 1) + TCN;
 size_t tc_x16_bytes(int T) { return (size_t)KB_GU * T * 128; }
 size_t tc_xg_bytes(int T) { return (size_t)KB_GU * tc_rows_cap(T) * 128; }
 size_t tc_hg_bytes(int T) { return (size_t)KB_D * tc_rows_cap(T) * 128; }
-// tile capacities: every expert's tiles plus the shared expert's (T more slots, one more expert)
+// tile capacity: every expert's tiles plus the shared expert's (T more slots, one more expert)
 inline int tc_max_tiles(int T) { return T * (K + 1) / TCN + EMAX + 1; }
-inline int tc_max_half(int T) { return T * (K + 1) / TCN_HALF + EMAX + 1; }
-size_t tc_meta_bytes(int T) {  // experts, tile lists, counts [4], slot_of [T * K]
-  return sizeof(TcExpert) * (EMAX + 1) + sizeof(TcTile) * (size_t)(tc_max_tiles(T) + tc_max_half(T)) +
+size_t tc_meta_bytes(int T) {  // experts, tile list, counts [4], slot_of [T * K]
+  return sizeof(TcExpert) * (EMAX + 1) + sizeof(TcTile) * (size_t)tc_max_tiles(T) +
          sizeof(int32_t) * (4 + (size_t)T * K) + 64;
 }
 
@@ -708,15 +718,14 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
                               const int32_t* pair, const int32_t* active, const int32_t* n_active, float* parts,
                               const float* weights, float* out, uint8_t* xg, uint8_t* hg, uint8_t* meta, int* status,
                               cudaStream_t s, const void* shared_blob) {
-  const int max_tiles = tc_max_tiles(T), max_half = tc_max_half(T);
+  const int max_tiles = tc_max_tiles(T);
   TcExpert* exps = reinterpret_cast<TcExpert*>(meta);
   TcTile* tiles = reinterpret_cast<TcTile*>(meta + sizeof(TcExpert) * (EMAX + 1));
-  TcTile* half_tiles = tiles + max_tiles;
-  int32_t* counts = reinterpret_cast<int32_t*>(half_tiles + max_half);
+  int32_t* counts = reinterpret_cast<int32_t*>(tiles + max_tiles);
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
                 tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
-                                                    half_tiles, counts, max_tiles, max_half, rows_cap,
+                                                    counts, max_tiles, rows_cap,
                                                     shared_blob ? T : 0, status));
   int32_t* slot_of = counts + 4;  // [T * K], after the counts in the tile-list area
   cudaError_t err = cudaMemsetAsync(slot_of, 0xFF, sizeof(int32_t) * (size_t)T * K, s);
@@ -744,7 +753,6 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   TcParams dp = gp;
   dp.act = hg;
-  dp.tiles = half_tiles;
   dp.parts = out ? nullptr : parts;
   dp.wts = weights;
   dp.out = out;
