@@ -70,13 +70,29 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed sleeps until it does (or
+// the hint runs out) instead of spinning, so waiting threads take no issue slots from their neighbours.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase; false (and ST_TIMEOUT recorded) if it never completed within
-// limit_ns (the library's kernels use the default; the wait self-test passes a short one).
+// limit_ns (the library's kernels use the default; the wait self-test passes a short one).  Each try
+// sleeps at most 1 ms (or the limit, if shorter) before the clock is checked again.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  const uint32_t hint = (uint32_t)(limit_ns < 1000000ull ? limit_ns : 1000000ull);
+  while (!mbar_try_wait_sleep(bar, parity, hint)) {
     if (globaltimer() - t0 > limit_ns) {
       set_status(status, ST_TIMEOUT);
       return false;

@@ -471,9 +471,16 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // One thread; its per-k-block work is all latency, so it waits only on full_a (every dequantiser
+    // waits for the stage's copies before it arrives there, so full_a implies full_tma) and keeps the
+    // stage numbers, parities and descriptors incrementally.
     if (lane == 0) {
-      int it = 0, n_small = 0;
+      int n_small = 0;
+      int s = 0, sa = 0;     // copy stage and weight stage of the next k-block
+      uint32_t ph_a = 0;     // parity of sa's current use
       HalfUses uses;  // items issued into each TMEM half so far
+      const uint64_t bd0 = tc::smem_desc_sw128(smem_u32(tma_ring));
+      const uint64_t ad00 = tc::smem_desc_sw128(smem_u32(a_ring));
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
         int rt;
         const TcTile tl = item_tile<GU>(p, item, rt);
@@ -495,18 +502,16 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         tc::fence_after_sync();
         const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u);
         const uint32_t mat_cols = wide ? 256u : 128u;
-        for (int kb = 0; kb < G::KBN; ++kb, ++it) {
-          const int s = it % NS_TMA, sa = it % NS_A;
-          if (!mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status) ||
-              !mbar_wait(&full_a[sa], (uint32_t)((it / NS_A) & 1), status)) {
+        for (int kb = 0; kb < G::KBN; ++kb) {
+          if (!mbar_wait(&full_a[sa], ph_a, status)) {
             s_fail = 1;
             break;
           }
           tc::fence_after_sync();
-          const uint64_t bd = tc::smem_desc_sw128(smem_u32(tma_ring + (size_t)s * G::TMA_STAGE));
-          const uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
+          // descriptor address fields are (address >> 4) below 2^14: stage offsets add without carry
+          const uint64_t bd = bd0 + (uint64_t)(s * (G::TMA_STAGE >> 4));
+          const uint64_t ad0 = ad00 + (uint64_t)(sa * (G::A_STAGE >> 4));
           // the two matrices' MMAs alternate, so each accumulator's next MMA never waits on its last
-          const uint64_t ad0 = tc::smem_desc_sw128(smem_u32(ast));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
@@ -515,6 +520,11 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
                           (kb > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&empty_tma[s]);
           tc::mma_commit(&empty_a[sa]);
+          if (++s == NS_TMA) s = 0;
+          if (++sa == NS_A) {
+            sa = 0;
+            ph_a ^= 1u;
+          }
         }
         if (s_fail) break;
         for (int h = 0; h < 2; ++h)
