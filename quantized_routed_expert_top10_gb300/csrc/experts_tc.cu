@@ -331,15 +331,15 @@ struct TcGeo {
 // h = silu(g) * u for 16-column chunks [ch0, ch1) of a gate/up accumulator pair, by the warp of TMEM lane
 // quadrant q (one weight row per thread): g in columns [0, mat_cols) of acc, u in [mat_cols, 2 mat_cols),
 // written to Hg (fp16, the down kernel's operand layout).  The fast exponential and division (relative
-// error ~1e-6) stay far below the fp16 rounding of h (2^-11).
+// error ~1e-6) stay far below the fp16 rounding of h (2^-11).  The quadrant's 32 rows are half of one
+// 64-wide k-block of h: 64 bytes of each token's Hg row.  Each chunk's 16 tokens x 64 bytes are put
+// together in the warp's 1 KB of shared memory (stage) in Hg order, then written out as 16-byte pieces.
 __device__ __forceinline__ void swiglu_chunks(const TcParams& p, const TcTile& tl, int rt, int q, uint32_t acc,
-                                              uint32_t mat_cols, int ch0, int ch1, bool ok) {
-  const int erow = 32 * q + (threadIdx.x & 31);
-  const int k = rt * 128 + erow;  // h index = the down projection's contraction index
-  const int kbd = k >> 6, k64 = k & 63;
-  const int pos = 16 * (k64 >> 4) + pi16_inv(k64 & 15);
-  uint8_t* hbase = p.hg + (int64_t)kbd * p.rows_cap * 128 + 2 * (pos & 7);
-  const int pc = pos >> 3;
+                                              uint32_t mat_cols, int ch0, int ch1, bool ok, uint8_t* stage) {
+  const int lane = threadIdx.x & 31;
+  const int pos = 16 * (lane >> 4) + pi16_inv(lane & 15);  // this row's place among the quadrant's 32
+  uint8_t* hblk = p.hg + (int64_t)(2 * rt + (q >> 1)) * p.rows_cap * 128;  // the rows' k-block of Hg
+  const int cbase = 4 * (q & 1);  // the quadrant's first 16-byte chunk in a 128-byte Hg row
 #pragma unroll 1
   for (int ch = ch0; ch < ch1; ++ch) {
     uint32_t g[16], u[16];
@@ -349,15 +349,24 @@ __device__ __forceinline__ void swiglu_chunks(const TcParams& p, const TcTile& t
     if (ok) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
+        const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+        *reinterpret_cast<__half*>(stage + i * 64 + 2 * pos) = __float2half_rn(__fdividef(gv * uv, 1.f + __expf(-gv)));
+      }
+    }
+    __syncwarp();
+    if (ok) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {  // pieces lane and lane + 32: token i, chunk c
+        const int i = (lane >> 2) + 8 * r, c = lane & 3;
         const int col = 16 * ch + i;
         if (col < tl.n) {
           const int hrow = tl.q0pad + col;
-          const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-          const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
-          *reinterpret_cast<__half*>(hbase + (int64_t)hrow * 128 + (((pc ^ hrow) & 7) << 4)) = __float2half_rn(h);
+          *reinterpret_cast<uint4*>(hblk + (int64_t)hrow * 128 + ((((cbase + c) ^ hrow) & 7) << 4)) =
+              *reinterpret_cast<const uint4*>(stage + i * 64 + 16 * c);
         }
       }
     }
+    __syncwarp();
   }
 }
 
@@ -406,6 +415,9 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   __shared__ uint32_t tmem_base;
   __shared__ int s_ep_pair[GU ? 1 : TCN];   // down epilogue: token (fused) or pair of each column
   __shared__ float s_ep_w[GU ? 1 : TCN];     //                router weight of that pair (fused combine)
+  // gate/up: h staging, 1 KB per warp that runs swiglu_chunks (epilogue warps 12..15 -> 0..3, the
+  // dequantising warps 4..11 helping with 256-token tiles -> 4..11)
+  __shared__ __align__(16) uint8_t s_hstage[GU ? 12 : 1][1024];
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -554,7 +566,8 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
       tc::fence_after_sync();
       int c0, c1;
       wide_split((pd.tl.n + 15) / 16, warp < 8 ? 1 : 2, c0, c1);
-      swiglu_chunks(p, pd.tl, pd.rt, warp & 3, tmem + ((uint32_t)(32 * (warp & 3)) << 16), 256u, c0, c1, ok);
+      swiglu_chunks(p, pd.tl, pd.rt, warp & 3, tmem + ((uint32_t)(32 * (warp & 3)) << 16), 256u, c0, c1, ok,
+                    s_hstage[warp]);
       tc::fence_before_sync();
       named_barrier(WIDE_BAR + (warp & 3), 96);
     };
@@ -633,7 +646,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         const int nch = nrows / 16;
         int c0 = 0, c1 = nch;
         if (wide) wide_split(nch, 0, c0, c1);
-        swiglu_chunks(p, tl, rt, q, acc, mat_cols, c0, c1, ok);
+        swiglu_chunks(p, tl, rt, q, acc, mat_cols, c0, c1, ok, s_hstage[warp - 12]);
         if (wide) {  // the dequantising warps of this quadrant drain the rest
           tc::fence_before_sync();
           named_barrier(WIDE_BAR + q, 96);
