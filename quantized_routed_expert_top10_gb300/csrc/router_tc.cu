@@ -8,6 +8,9 @@
 // A prep pass writes x (times the token's 1/rms for residual layers) as two bf16 matrices,
 // x_hi = bf16(x) and x_lo = bf16(x - x_hi); both products accumulate into the same fp32 TMEM
 // accumulator, so each term carries x to about 16 significant bits (relative error ~2^-17).
+// The x_hi and x_lo tiles of a k-block lie one after the other in shared memory, so together they are
+// one 256-row operand: a single MMA (N = 256) takes both products, x_hi's into accumulator columns
+// [0, 128) and x_lo's into [128, 256).
 // The contraction is split two ways over CTAs (ROUTER_KSPLIT; 1,280 columns each) and, inside a
 // CTA, into four accumulators in TMEM (even / odd k-blocks x the x_hi / x_lo products); a CTA writes
 // the sum of its four to its slice of the partial-logit buffer and the top-k kernel adds the slices in a fixed order (and the
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
       mbar_wait(&full[(kbl - back) % RT_NS], (uint32_t)(((kbl - back) / RT_NS) & 1), status);
   } else if (tid == 32) {
     // ---- MMA issuer ----
-    const uint32_t idesc = idesc_bf16_f32(RT_E, RT_T);
+    const uint32_t idesc = idesc_bf16_f32(RT_E, 2 * RT_T);  // N: the tile's tokens as x_hi, then as x_lo
     for (int kbl = 0; kbl < RT_KBS; ++kbl) {
       const int s = kbl % RT_NS;
       if (!mbar_wait(&full[s], (uint32_t)((kbl / RT_NS) & 1), status)) {
@@ -169,39 +172,40 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
       }
       tc::fence_after_sync();
       const uint8_t* st = smem + (size_t)s * RT_STAGE;
-      const uint64_t ah = tc::smem_desc_sw128(smem_u32(st));
-      const uint64_t al = tc::smem_desc_sw128(smem_u32(st + RT_TILE));
+      const uint64_t bx = tc::smem_desc_sw128(smem_u32(st));  // x_hi rows, then x_lo rows
       const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + 2 * RT_TILE));
-      // four accumulation chains -- (k-block parity) x (x_hi, x_lo) -- interleaved, so consecutive MMAs
-      // never wait on each other's accumulator
+      // even and odd k-blocks accumulate apart, so consecutive k-blocks' MMAs never wait on each other
       const uint32_t acc0 = tmem + (uint32_t)((kbl & 1) * 2 * RT_T);
       const bool first = kbl < 2;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        tc::mma_f16(acc0, bd + 2 * kk, ah + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
-        tc::mma_f16(acc0 + RT_T, bd + 2 * kk, al + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < 4; ++kk) tc::mma_f16(acc0, bd + 2 * kk, bx + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
       tc::mma_commit(&empty[s]);
     }
     tc::mma_commit(&done);  // after every MMA this thread issued
   }
-  // ---- epilogue: warps 0..3 own TMEM lane quadrants = expert rows; columns are tokens, so a warp's
-  // stores for one token cover 32 consecutive experts ----
+  // ---- epilogue: warps 0..3 own TMEM lane quadrants = expert rows; columns are tokens.  Each 4 x 4
+  // block of (experts, tokens) is transposed across 4 lanes, so lane 4g + j stores experts 4g .. 4g + 3
+  // of token j as one 16-byte store (experts past E land in the row's unused tail: rows hold EMAX) ----
   __syncwarp();
   ok = mbar_wait(&done, 0u, status) && ok;
   tc::fence_after_sync();
-  const int e = e0 + 32 * warp + lane;
+  const int j4 = lane & 3;
+  const int e4 = e0 + 32 * warp + 4 * (lane >> 2);
 #pragma unroll 1
   for (int ch = 0; ch < RT_T / 16; ++ch) {
     float v[4][16];
 #pragma unroll
     for (int c = 0; c < 4; ++c) tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c * RT_T + 16 * ch, v[c]);
-    if (ok && e < E) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = t0 + 16 * ch + i;
-        if (t < T) parts[((size_t)blockIdx.z * T + t) * EMAX + e] = (v[0][i] + v[1][i]) + (v[2][i] + v[3][i]);
-      }
+    for (int m = 0; m < 4; ++m) {
+      uint32_t a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        a[i] = __float_as_uint((v[0][4 * m + i] + v[1][4 * m + i]) + (v[2][4 * m + i] + v[3][4 * m + i]));
+      tc::transpose4_lanes(a, j4);
+      const int t = t0 + 16 * ch + 4 * m + j4;
+      if (ok && e4 < E && t < T)
+        *reinterpret_cast<uint4*>(parts + ((size_t)blockIdx.z * T + t) * EMAX + e4) = make_uint4(a[0], a[1], a[2], a[3]);
     }
   }
   tc::fence_before_sync();
