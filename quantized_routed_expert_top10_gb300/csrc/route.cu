@@ -179,13 +179,20 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
   if (t >= T) return;
   const size_t slice = (size_t)T * EMAX;
   const float* p = parts + (size_t)t * EMAX;
-  float lg[16];
+  // every load is issued before the first sum, so the warp waits for memory once, not once per j
+  float a[16], b[16], lg[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int e = lane + 32 * j;
+    a[j] = e < E ? __ldcg(p + e) : 0.f;
+    b[j] = e < E ? __ldcg(p + slice + e) : 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int e = lane + 32 * j;
     float v = 0.f;
     if (e < E) {
-      v = __ldcg(p + e) + __ldcg(p + slice + e);
+      v = a[j] + b[j];
       if (bias) v += __ldg(bias + e);
       if (logits_out) logits_out[(size_t)t * E + e] = v;
     }
@@ -206,8 +213,16 @@ __global__ void __launch_bounds__(256) group_hist_kernel(const int32_t* __restri
   for (int i = threadIdx.x; i < E; i += 256) cnt[i] = 0;
   __syncthreads();
   const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
-  for (int p = p0 + threadIdx.x; p < p1; p += 256) {
-    const int e = ids[p];
+  int ev[GROUP_CHUNK / 256];  // the thread's ids, loaded before any is counted
+#pragma unroll
+  for (int j = 0; j < GROUP_CHUNK / 256; ++j) {
+    const int p = p0 + (int)threadIdx.x + 256 * j;
+    ev[j] = p < p1 ? __ldg(ids + p) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < GROUP_CHUNK / 256; ++j) {
+    if (p0 + (int)threadIdx.x + 256 * j >= p1) break;
+    const int e = ev[j];
     if (e < 0 || e >= E) set_status(status, ST_CORRUPT);
     else atomicAdd(&cnt[e], 1);
   }
@@ -243,20 +258,40 @@ __global__ void __launch_bounds__(512) group_scan_kernel(int n_chunks, int E, in
   finish_grouping(s_cnt, E, s_off, s_flag, s_scratch, expert_off, active, n_active);
 }
 
-// One warp per chunk: the chunk's ids staged in shared memory with independent loads, then the
-// stable scatter starting from expert_off[e] + chunk base.
-__global__ void __launch_bounds__(32) group_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                                           const int32_t* __restrict__ chunk_cnt,
-                                                           const int32_t* __restrict__ expert_off,
-                                                           int32_t* __restrict__ pair) {
-  __shared__ int fill[EMAX];
+// One CTA of 8 warps per chunk: the chunk's ids staged in shared memory with independent loads; each
+// warp counts its 256-pair slice, the slices' bases per expert are a prefix over the warps starting at
+// expert_off[e] + the chunk's base, and each warp scatters its slice stably (the order is the
+// chunk's, as one warp walking the whole chunk would give).
+constexpr int SCATTER_WARPS = 8;
+constexpr int SCATTER_SLICE = GROUP_CHUNK / SCATTER_WARPS;
+__global__ void __launch_bounds__(32 * SCATTER_WARPS) group_scatter_kernel(const int32_t* __restrict__ ids, int P,
+                                                                           int E, const int32_t* __restrict__ chunk_cnt,
+                                                                           const int32_t* __restrict__ expert_off,
+                                                                           int32_t* __restrict__ pair) {
   __shared__ int s_ids[GROUP_CHUNK];
-  for (int i = threadIdx.x; i < E; i += 32)
-    fill[i] = expert_off[i] + chunk_cnt[(size_t)blockIdx.x * EMAX + i];
+  __shared__ int s_base[SCATTER_WARPS][EMAX];  // per-slice counts, then per-slice bases
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
-  for (int p = p0 + (int)threadIdx.x; p < p1; p += 32) s_ids[p - p0] = __ldg(ids + p);
-  __syncwarp();
-  stable_scatter_warp(s_ids, 0, p1 - p0, E, fill, pair, p0);
+  for (int i = threadIdx.x; i < SCATTER_WARPS * EMAX; i += 32 * SCATTER_WARPS) (&s_base[0][0])[i] = 0;
+  for (int p = p0 + (int)threadIdx.x; p < p1; p += 32 * SCATTER_WARPS) s_ids[p - p0] = __ldg(ids + p);
+  __syncthreads();
+  const int q0 = warp * SCATTER_SLICE, q1 = min(p1 - p0, q0 + SCATTER_SLICE);
+  for (int q = q0 + lane; q < q1; q += 32) {
+    const int e = s_ids[q];
+    if (e >= 0 && e < E) atomicAdd(&s_base[warp][e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 32 * SCATTER_WARPS) {
+    int run = expert_off[e] + chunk_cnt[(size_t)blockIdx.x * EMAX + e];
+#pragma unroll
+    for (int w = 0; w < SCATTER_WARPS; ++w) {
+      const int c = s_base[w][e];
+      s_base[w][e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (q0 < q1) stable_scatter_warp(s_ids, q0, q1, E, s_base[warp], pair, p0);
 }
 
 }  // namespace
@@ -297,7 +332,7 @@ cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, 
   STRATA_LAUNCH(KID_GROUP_SCAN, s,
                 group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat));
   STRATA_LAUNCH(KID_GROUP_SCATTER, s,
-                group_scatter_kernel<<<L.n_chunks, 32, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
+                group_scatter_kernel<<<L.n_chunks, 32 * SCATTER_WARPS, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
   if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
   return cudaGetLastError();
 }
