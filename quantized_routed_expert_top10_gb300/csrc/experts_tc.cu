@@ -22,7 +22,8 @@
 //   warp 2      owns the TMEM allocation;
 //   warps 4-11  dequantise the codes straight into the 128B-swizzled K-major shared-memory layout
 //               (fp16: (c + 1024) built by one LOP3 per pair, minus (1024 + q2_offset), times d -- all
-//               exact) in a 2-stage (gate/up) or 3-stage (down) ring of weight tiles;
+//               exact) in a 2-stage (gate/up) or 3-stage (down) ring of weight tiles, as two groups of
+//               four warps taking alternate k-blocks;
 //   warp 1      issues tcgen05.mma (fp16 x fp16 -> fp32) into TMEM (gate/up: one half for a tile of up to
 //               128 tokens, both for a wider one; down: one half per item) and commits to the stages'
 //               "empty" mbarriers;
@@ -263,17 +264,6 @@ __device__ __forceinline__ void dequant_row(const uint4 codes, __half d, int q2_
 #pragma unroll
   for (int c = 0; c < 8; ++c) dequant_chunk((c & 1) ? (w[c >> 1] >> 8) : w[c >> 1], k, tile, r, c);
 }
-// Half hf of the row: chunks 4 hf .. 4 hf + 3, i.e. the 16-groups held by code words 2 hf and 2 hf + 1.
-__device__ __forceinline__ void dequant_half_row(const uint4 codes, __half d, int q2_offset, uint8_t* tile, int r,
-                                                 int hf) {
-  const DequantConsts k(d, q2_offset);
-  const uint32_t wa = hf ? codes.z : codes.x, wb = hf ? codes.w : codes.y;
-  dequant_chunk(wa, k, tile, r, 4 * hf);
-  dequant_chunk(wa >> 8, k, tile, r, 4 * hf + 1);
-  dequant_chunk(wb, k, tile, r, 4 * hf + 2);
-  dequant_chunk(wb >> 8, k, tile, r, 4 * hf + 3);
-}
-
 struct TcParams {
   const uint8_t* blobs;
   int64_t stride;
@@ -294,9 +284,9 @@ struct TcParams {
 };
 
 // Kernel geometry.  Warp 0: copy producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 4..11:
-// dequantisers (256 threads: gate/up, one weight row of one of the item's two 128-row matrices each;
-// down, half a row of its one matrix); warps 12..15 (down: 12..19): epilogue (one TMEM lane = one
-// weight row per thread).
+// dequantisers (two groups of 128 threads on alternate k-blocks, one weight row per thread: gate/up,
+// that row of both matrices); warps 12..15 (down: 12..27): epilogue (one TMEM lane = one weight row
+// per thread).
 // gate/up (GU = true): item = (tile, row tile rt of gate and up): matrices gate_rt, up_rt.  TMEM: a
 // tile of up to 128 tokens accumulates in half b (alternating) -- matrix j in columns [b*256 + j*128,
 // +128) -- so its epilogue overlaps the next tile's main loop; a wider tile (up to 256 tokens, one
@@ -428,7 +418,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
       mbar_init(&empty_tma[s], 1);
     }
     for (int s = 0; s < NS_A; ++s) {
-      mbar_init(&full_a[s], 8);
+      mbar_init(&full_a[s], 4);  // the four warps of the dequantising group that fills it
       mbar_init(&empty_a[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -550,8 +540,11 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     }
   } else if (warp >= 4 && warp < 12) {
     // ---------------- dequantisers ----------------
-    const int dt = tid - 128;
-    const int row = dt & 127, sub = dt >> 7;  // gate/up: matrix of the item; down: half of the row
+    // Two groups of four warps take alternate k-blocks (items have an even number of them), so each
+    // group's fixed cost per k-block -- its waits, the proxy fence, the arrival -- comes every other
+    // k-block; each thread expands one weight row (gate/up: that row of both matrices).
+    const int grp = (warp - 4) >> 2;
+    const int row = (tid - 128) & 127;
     int it = 0;
     bool ok = true;
     // gate/up: the TMEM use of every item, tracked as the issuer assigns it, so that a 256-token tile's
@@ -584,8 +577,9 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
           if (wide || h == b) uses.bump(h);
       }
       for (int kb = 0; kb < G::KBN; ++kb, ++it) {
+        if ((kb & 1) != grp) continue;
         const int s = it % NS_TMA, sa = it % NS_A;
-        if (GU && kb == NS_A && pend.wide) {
+        if (GU && kb >= NS_A && pend.wide) {  // the group's stages of this item are filled
           help_wide(pend);
           pend.wide = false;
         }
@@ -594,20 +588,21 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         if (ok) {
           const uint8_t* code = tma_ring + (size_t)s * G::TMA_STAGE + B_TILE;
           uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
-          // gate/up: 8 slab pieces {gate codes, up codes, {gate d, up d} per row}; down: two chunks
-          uint4 cw;
-          __half d;
+          // gate/up: 8 slab pieces {gate codes, up codes, {gate d, up d} per row}; down: one chunk
           if (GU) {
             const uint8_t* pc = code + (row / SLAB) * SLAB_KB;
             const int rr = row % SLAB;
-            cw = *reinterpret_cast<const uint4*>(pc + sub * 256 + 16 * rr);
-            d = *reinterpret_cast<const __half*>(pc + 512 + 4 * rr + 2 * sub);
+            const uint4 cg = *reinterpret_cast<const uint4*>(pc + 16 * rr);
+            const uint4 cu = *reinterpret_cast<const uint4*>(pc + 256 + 16 * rr);
+            const __half dg = *reinterpret_cast<const __half*>(pc + 512 + 4 * rr);
+            const __half du = *reinterpret_cast<const __half*>(pc + 512 + 4 * rr + 2);
+            dequant_row(cg, dg, p.q2_offset, ast, row);
+            dequant_row(cu, du, p.q2_offset, ast + A_TILE, row);
           } else {
-            cw = *reinterpret_cast<const uint4*>(code + 16 * row);
-            d = *reinterpret_cast<const __half*>(code + 2048 + 2 * row);
+            const uint4 cw = *reinterpret_cast<const uint4*>(code + 16 * row);
+            const __half d = *reinterpret_cast<const __half*>(code + 2048 + 2 * row);
+            dequant_row(cw, d, p.q2_offset, ast, row);
           }
-          if (GU) dequant_row(cw, d, p.q2_offset, ast + sub * A_TILE, row);
-          else dequant_half_row(cw, d, p.q2_offset, ast, row, sub);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
