@@ -474,18 +474,21 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     // One thread; its per-k-block work is all latency, so it waits only on full_a (every dequantiser
-    // waits for the stage's copies before it arrives there, so full_a implies full_tma) and keeps the
-    // stage numbers, parities and descriptors incrementally.
+    // waits for the stage's copies before it arrives there, so full_a implies full_tma), keeps the
+    // stage numbers, parities and descriptors incrementally and loads each item's tile one item ahead.
     if (lane == 0) {
       int n_small = 0;
       int s = 0, sa = 0;     // copy stage and weight stage of the next k-block
       uint32_t ph_a = 0;     // parity of sa's current use
+      bool ready = false;    // the next k-block's full_a phase was seen complete
       HalfUses uses;  // items issued into each TMEM half so far
       const uint64_t bd0 = tc::smem_desc_sw128(smem_u32(tma_ring));
       const uint64_t ad00 = tc::smem_desc_sw128(smem_u32(a_ring));
+      int rt_next = 0;
+      TcTile tl_next = blockIdx.x < n_items ? item_tile<GU>(p, blockIdx.x, rt_next) : TcTile{0, 0, 0, 0};
       for (int item = blockIdx.x; item < n_items && !s_fail; item += gridDim.x) {
-        int rt;
-        const TcTile tl = item_tile<GU>(p, item, rt);
+        const TcTile tl = tl_next;
+        if (item + (int)gridDim.x < n_items) tl_next = item_tile<GU>(p, item + gridDim.x, rt_next);
         if (tl.n == 0) continue;
         const int nrows = (tl.n + 15) / 16 * 16;
         const uint32_t idesc = tc::idesc_f16_f32(128, nrows);
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         const uint32_t acc = tmem + (wide ? 0u : (uint32_t)b * 256u);
         const uint32_t mat_cols = wide ? 256u : 128u;
         for (int kb = 0; kb < G::KBN; ++kb) {
-          if (!mbar_wait(&full_a[sa], ph_a, status)) {
+          if (!ready && !mbar_wait(&full_a[sa], ph_a, status)) {
             s_fail = 1;
             break;
           }
@@ -513,13 +516,21 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
           // descriptor address fields are (address >> 4) below 2^14: stage offsets add without carry
           const uint64_t bd = bd0 + (uint64_t)(s * (G::TMA_STAGE >> 4));
           const uint64_t ad0 = ad00 + (uint64_t)(sa * (G::A_STAGE >> 4));
-          // the two matrices' MMAs alternate, so each accumulator's next MMA never waits on its last
+          if (GU) {
+            // the two matrices' MMAs alternate, so each accumulator's next MMA never waits on its last
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int mat = 0; mat < G::NMAT; ++mat)
-              tc::mma_f16(acc + mat * mat_cols, ad0 + (uint64_t)((mat * A_TILE) >> 4) + 2 * kk, bd + 2 * kk, idesc,
-                          (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int mat = 0; mat < G::NMAT; ++mat)
+                tc::mma_f16(acc + mat * mat_cols, ad0 + (uint64_t)((mat * A_TILE) >> 4) + 2 * kk, bd + 2 * kk, idesc,
+                            (kb > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            // down's k-block is four MMAs, shorter than the issuer's own loop: the next k-block's full_a
+            // is tested while they issue
+            const int sa1 = sa + 1 == NS_A ? 0 : sa + 1;
+            const uint32_t ph1 = sa + 1 == NS_A ? (ph_a ^ 1u) : ph_a;
+            ready = tc::mma_kblock_test_next(acc, ad0, bd, idesc, kb > 0 ? 1u : 0u, smem_u32(&full_a[sa1]), ph1) != 0;
+          }
           tc::mma_commit(&empty_tma[s]);
           tc::mma_commit(&empty_a[sa]);
           if (++s == NS_TMA) s = 0;

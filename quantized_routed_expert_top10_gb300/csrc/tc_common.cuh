@@ -58,6 +58,32 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// One 64-wide k-block of MMAs (K = 16 each; descriptors advance 32 bytes per step) into accumulator d0
+// from a0 against b; the first step accumulates only if acc_first != 0.  The mbarrier at next_bar is
+// tested (non-blocking) for phase parity next_par before the MMAs and its result read after them, so
+// the test's latency hides behind their issue; returns 1 if that phase had completed.
+__device__ __forceinline__ uint32_t mma_kblock_test_next(uint32_t d0, uint64_t a0, uint64_t b, uint32_t idesc,
+                                                         uint32_t acc_first, uint32_t next_bar, uint32_t next_par) {
+  uint32_t ready;
+  asm volatile(
+      "{\n\t.reg .pred pr, pa, pt;\n\t.reg .b64 ta, tb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pr, [%6], %7;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+      "add.s64 ta, %2, 2;\n\tadd.s64 tb, %3, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], ta, tb, %4, pt;\n\t"
+      "add.s64 ta, %2, 4;\n\tadd.s64 tb, %3, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], ta, tb, %4, pt;\n\t"
+      "add.s64 ta, %2, 6;\n\tadd.s64 tb, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], ta, tb, %4, pt;\n\t"
+      "selp.u32 %0, 1, 0, pr;\n\t}"
+      : "=r"(ready)
+      : "r"(d0), "l"(a0), "l"(b), "r"(idesc), "r"(acc_first), "r"(next_bar), "r"(next_par)
+      : "memory");
+  return ready;
+}
+
 // fp32 reduction into global memory (no return value) with an L2 eviction-policy hint.
 __device__ __forceinline__ void red_add_f32_hint(float* p, float v, uint64_t policy) {
   asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
