@@ -556,7 +556,12 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
     // k-block; each thread expands one weight row (gate/up: that row of both matrices).
     const int grp = (warp - 4) >> 2;
     const int row = (tid - 128) & 127;
-    int it = 0;
+    // the group's k-blocks are it = grp, grp + 2, ... (counted over all items): copy stage s = it % NS_TMA
+    // and weight stage sa = it % NS_A, with the parities of it / NS_TMA and it / NS_A, kept incrementally
+    // (a step of two k-blocks wraps each ring at most once: NS_A, NS_TMA >= 2)
+    static_assert(NS_A >= 2 && NS_TMA >= 2 && G::KBN % 2 == 0, "two groups on alternate k-blocks");
+    int it = grp, s = grp, sa = grp % NS_A;
+    uint32_t ph_t = 0, ph_a = 0;
     bool ok = true;
     // gate/up: the TMEM use of every item, tracked as the issuer assigns it, so that a 256-token tile's
     // epilogue can be joined once the next item's first NS_A stages are dequantised (or after the last item)
@@ -575,9 +580,12 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
       tc::fence_before_sync();
       named_barrier(WIDE_BAR + (warp & 3), 96);
     };
+    int rt_next = 0;
+    TcTile tl_next = blockIdx.x < n_items ? item_tile<GU>(p, blockIdx.x, rt_next) : TcTile{0, 0, 0, 0};
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      int rt_cur;
-      const TcTile tl_cur = item_tile<GU>(p, item, rt_cur);
+      const int rt_cur = rt_next;
+      const TcTile tl_cur = tl_next;  // loaded one item ahead
+      if (item + (int)gridDim.x < n_items) tl_next = item_tile<GU>(p, item + gridDim.x, rt_next);
       if (tl_cur.n == 0) continue;
       Pending cur{false, tl_cur, rt_cur, (uint32_t)(uses[0] & 1), (uint32_t)(uses[1] & 1)};
       if (GU) {
@@ -587,15 +595,13 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         for (int h = 0; h < 2; ++h)
           if (wide || h == b) uses.bump(h);
       }
-      for (int kb = 0; kb < G::KBN; ++kb, ++it) {
-        if ((kb & 1) != grp) continue;
-        const int s = it % NS_TMA, sa = it % NS_A;
+      for (int kb = grp; kb < G::KBN; kb += 2) {
         if (GU && kb >= NS_A && pend.wide) {  // the group's stages of this item are filled
           help_wide(pend);
           pend.wide = false;
         }
-        if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], (uint32_t)((it / NS_A - 1) & 1), status);
-        ok = ok && mbar_wait(&full_tma[s], (uint32_t)((it / NS_TMA) & 1), status);
+        if (it >= NS_A) ok = ok && mbar_wait(&empty_a[sa], ph_a ^ 1u, status);  // MMAs of k-block it - NS_A
+        ok = ok && mbar_wait(&full_tma[s], ph_t, status);
         if (ok) {
           const uint8_t* code = tma_ring + (size_t)s * G::TMA_STAGE + B_TILE;
           uint8_t* ast = a_ring + (size_t)sa * G::A_STAGE;
@@ -618,6 +624,17 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[sa]);
+        it += 2;
+        s += 2;
+        if (s >= NS_TMA) {
+          s -= NS_TMA;
+          ph_t ^= 1u;
+        }
+        sa += 2;
+        if (sa >= NS_A) {
+          sa -= NS_A;
+          ph_a ^= 1u;
+        }
       }
       if (GU) {
         if (pend.wide) help_wide(pend);  // an item shorter than NS_A k-blocks (never for gate/up)
