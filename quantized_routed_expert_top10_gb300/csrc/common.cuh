@@ -265,6 +265,27 @@ bool profiling_armed();
 void count_launches(unsigned long long n);
 // Launch sites the calling thread has passed so far (captured ones included).
 unsigned long long launches_this_thread();
+// Launch of a kernel of the prefill chain with programmatic stream serialisation: it may start while
+// the kernel before it on the stream finishes (that kernel lets it once every CTA has begun), and it
+// reaches past its prologue only through griddep_wait(), which returns once the kernel before it has
+// completed and its memory is visible.  Kernels launched this way call griddep_launch_dependents()
+// and griddep_wait() (device_common.cuh) before touching memory that other launches write or read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 #define STRATA_LAUNCH(kid, s, ...) \
   do {                             \
     kernel_begin((kid), (s));      \

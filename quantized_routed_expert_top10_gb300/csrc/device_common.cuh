@@ -6,6 +6,14 @@ namespace strata {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any wait in a correct run
 
+// Programmatic dependent launch (launch_pdl): the next kernel on the stream may be scheduled once every
+// CTA of this one has signalled; griddep_wait blocks until the previous kernel has completed and its
+// memory is visible (at once for a kernel launched without the attribute).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t sm_id() {
   uint32_t v;
   asm volatile("mov.u32 %0, %%smid;" : "=r"(v));

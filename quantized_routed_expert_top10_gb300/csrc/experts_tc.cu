@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
   __shared__ int s_pad[EMAX], s_full[EMAX], s_wide[EMAX], s_narrow[EMAX], s_scratch[32];
   __shared__ int s_e[EMAX], s_end[EMAX];
   __shared__ int s_bad;
+  griddep_launch_dependents();
+  griddep_wait();
   const int i = threadIdx.x;
   if (i == 0) s_bad = 0;
   const int na = max(0, min(*n_active, E));
@@ -161,6 +163,8 @@ __global__ void __launch_bounds__(512) tc_prepare_kernel(const int32_t* __restri
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tc_x16_kernel(const float* __restrict__ x, const float* __restrict__ inv_rms,
                                                      int T, uint8_t* __restrict__ x16) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
@@ -173,6 +177,8 @@ __global__ void __launch_bounds__(256) tc_x16_kernel(const float* __restrict__ x
 // grouping leaves out; a pair number outside [0, P) sets ST_CORRUPT and is skipped.
 __global__ void __launch_bounds__(256) tc_slot_of_kernel(const int32_t* __restrict__ pair, int P,
                                                          int32_t* __restrict__ slot_of, int* __restrict__ status) {
+  griddep_launch_dependents();
+  griddep_wait();
   for (int j = blockIdx.x * 256 + threadIdx.x; j < P; j += gridDim.x * 256) {
     const int pr = pair[j];
     if (pr >= 0 && pr < P) slot_of[pr] = j;
@@ -198,6 +204,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) tc_gather_kernel(const uint8_t
                                                                    const int32_t* __restrict__ counts,
                                                                    uint8_t* __restrict__ xg, int64_t rows_cap) {
   __shared__ int s_q0[EMAX + 1], s_shift[EMAX + 1];  // the routed experts and a shared expert
+  griddep_launch_dependents();
+  griddep_wait();
   const int na = min(counts[0], EMAX + 1);
   for (int i = threadIdx.x; i < na; i += GATHER_THREADS) {
     const TcExpert ex = exps[i];
@@ -411,6 +419,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   __shared__ int s_fail_flag;
   volatile int& s_fail = s_fail_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();
   if (warp == 2) tc::tmem_alloc(&tmem_base, G::TMEM_COLS);
   if (tid == 0) {
     for (int s = 0; s < NS_TMA; ++s) {
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(tc_threads<GU>(), 1) tc_expert_kernel(const Tc
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  griddep_wait();  // tile lists, token and h copies come from the kernels before
   const uint32_t tmem = tmem_base;
   const int n_items = p.counts[1] * G::RTN;
   int* status = p.status;
@@ -756,7 +766,7 @@ size_t tc_meta_bytes(int T) {  // experts, tile list, counts [4], slot_of [T * K
 }
 
 cudaError_t launch_x16(const float* x, const float* inv_rms, int T, uint8_t* x16, cudaStream_t s) {
-  STRATA_LAUNCH(KID_ROUTER_PREP, s, tc_x16_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, inv_rms, T, x16));
+  STRATA_LAUNCH(KID_ROUTER_PREP, s, launch_pdl(tc_x16_kernel, (T + 7) / 8, 256, 0, s, x, inv_rms, T, x16));
   return cudaGetLastError();
 }
 
@@ -770,15 +780,17 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   int32_t* counts = reinterpret_cast<int32_t*>(tiles + max_tiles);
   const int64_t rows_cap = tc_rows_cap(T);
   STRATA_LAUNCH(KID_TC_PREPARE, s,
-                tc_prepare_kernel<<<1, 512, 0, s>>>(expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
+                launch_pdl(tc_prepare_kernel, 1, 512, 0, s, expert_off, active, n_active, ex.n_expert, T * K, exps, tiles,
                                                     counts, max_tiles, rows_cap,
                                                     shared_blob ? T : 0, status));
   int32_t* slot_of = counts + 4;  // [T * K], after the counts in the tile-list area
-  cudaError_t err = cudaMemsetAsync(slot_of, 0xFF, sizeof(int32_t) * (size_t)T * K, s);
-  if (err != cudaSuccess) return err;
-  STRATA_LAUNCH(KID_TC_GATHER, s, tc_slot_of_kernel<<<GATHER_BLOCKS, 256, 0, s>>>(pair, T * K, slot_of, status));
+  cudaError_t err = cudaSuccess;
+  // a layer call (out set) groups every pair itself, so every slot_of entry is written; a caller's
+  // grouping (strata_moe_experts) may leave pairs out, whose entries must read -1
+  if (!out && (err = cudaMemsetAsync(slot_of, 0xFF, sizeof(int32_t) * (size_t)T * K, s)) != cudaSuccess) return err;
+  STRATA_LAUNCH(KID_TC_GATHER, s, launch_pdl(tc_slot_of_kernel, GATHER_BLOCKS, 256, 0, s, pair, T * K, slot_of, status));
   STRATA_LAUNCH(KID_TC_GATHER, s,
-                tc_gather_kernel<<<GATHER_BLOCKS, GATHER_THREADS, 0, s>>>(x16, T, slot_of, T * K, shared_blob ? 1 : 0,
+                launch_pdl(tc_gather_kernel, GATHER_BLOCKS, GATHER_THREADS, 0, s, x16, T, slot_of, T * K, shared_blob ? 1 : 0,
                                                                           exps, counts, xg, rows_cap));
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -795,7 +807,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<true>::SMEM)) != cudaSuccess)
     return err;
-  STRATA_LAUNCH(KID_TC_GATEUP, s, tc_expert_kernel<true><<<sms, tc_threads<true>(), TcGeo<true>::SMEM, s>>>(gp));
+  STRATA_LAUNCH(KID_TC_GATEUP, s, launch_pdl(tc_expert_kernel<true>, sms, tc_threads<true>(), TcGeo<true>::SMEM, s, gp));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   TcParams dp = gp;
   dp.act = hg;
@@ -805,7 +817,7 @@ cudaError_t launch_experts_tc(const strata_experts_t& ex, const uint8_t* x16, in
   if ((err = cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)TcGeo<false>::SMEM)) != cudaSuccess)
     return err;
-  STRATA_LAUNCH(KID_TC_DOWN, s, tc_expert_kernel<false><<<sms, tc_threads<false>(), TcGeo<false>::SMEM, s>>>(dp));
+  STRATA_LAUNCH(KID_TC_DOWN, s, launch_pdl(tc_expert_kernel<false>, sms, tc_threads<false>(), TcGeo<false>::SMEM, s, dp));
   return cudaGetLastError();
 }
 

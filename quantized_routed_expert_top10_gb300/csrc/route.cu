@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
                                                     int32_t* __restrict__ ids, float* __restrict__ weights) {
   static_assert(ROUTER_KSPLIT == 2, "the fixed summation order below assumes two slices");
   __shared__ TopKScratch s_topk[4];
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const size_t slice = (size_t)T * EMAX;
@@ -210,6 +212,8 @@ __global__ void __launch_bounds__(128) top_k_kernel(const float* __restrict__ pa
 __global__ void __launch_bounds__(256) group_hist_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                          int32_t* __restrict__ chunk_cnt, int* status) {
   __shared__ int cnt[EMAX];
+  griddep_launch_dependents();
+  griddep_wait();
   for (int i = threadIdx.x; i < E; i += 256) cnt[i] = 0;
   __syncthreads();
   const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
@@ -238,6 +242,8 @@ __global__ void __launch_bounds__(512) group_scan_kernel(int n_chunks, int E, in
                                                          int32_t* __restrict__ active,
                                                          int32_t* __restrict__ n_active) {
   __shared__ int s_cnt[EMAX], s_off[EMAX], s_flag[EMAX], s_scratch[32];
+  griddep_launch_dependents();
+  griddep_wait();
   const int e = threadIdx.x;
   if (e < E) {
     int run = 0;
@@ -270,6 +276,8 @@ __global__ void __launch_bounds__(32 * SCATTER_WARPS) group_scatter_kernel(const
                                                                            int32_t* __restrict__ pair) {
   __shared__ int s_ids[GROUP_CHUNK];
   __shared__ int s_base[SCATTER_WARPS][EMAX];  // per-slice counts, then per-slice bases
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = blockIdx.x * GROUP_CHUNK, p1 = min(P, p0 + GROUP_CHUNK);
   for (int i = threadIdx.x; i < SCATTER_WARPS * EMAX; i += 32 * SCATTER_WARPS) (&s_base[0][0])[i] = 0;
@@ -318,7 +326,7 @@ cudaError_t launch_route_decode(const float* x, int T, int apply_rmsnorm, const 
 cudaError_t launch_top_k(const float* parts, int T, int E, const float* bias, float* logits_out, int32_t* ids,
                          float* weights, cudaStream_t s) {
   STRATA_LAUNCH(KID_TOP_K, s,
-                top_k_kernel<<<(T + 3) / 4, 128, 0, s>>>(parts, T, E, bias, logits_out, ids, weights));
+                launch_pdl(top_k_kernel, (T + 3) / 4, 128, 0, s, parts, T, E, bias, logits_out, ids, weights));
   return cudaGetLastError();
 }
 
@@ -328,11 +336,11 @@ cudaError_t launch_group(const int32_t* ids, int T, int E, int32_t* expert_off, 
   int32_t* chunk_cnt = (int32_t*)(ws + L.chunk_cnt);
   int32_t* nat = (int32_t*)(ws + L.n_active);
   STRATA_LAUNCH(KID_GROUP_HIST, s,
-                group_hist_kernel<<<L.n_chunks, 256, 0, s>>>(ids, P, E, chunk_cnt, (int*)(ws + L.status)));
+                launch_pdl(group_hist_kernel, L.n_chunks, 256, 0, s, ids, P, E, chunk_cnt, (int*)(ws + L.status)));
   STRATA_LAUNCH(KID_GROUP_SCAN, s,
-                group_scan_kernel<<<1, 512, 0, s>>>(L.n_chunks, E, chunk_cnt, expert_off, active, nat));
+                launch_pdl(group_scan_kernel, 1, 512, 0, s, L.n_chunks, E, chunk_cnt, expert_off, active, nat));
   STRATA_LAUNCH(KID_GROUP_SCATTER, s,
-                group_scatter_kernel<<<L.n_chunks, 32 * SCATTER_WARPS, 0, s>>>(ids, P, E, chunk_cnt, expert_off, pair));
+                launch_pdl(group_scatter_kernel, L.n_chunks, 32 * SCATTER_WARPS, 0, s, ids, P, E, chunk_cnt, expert_off, pair));
   if (n_active && n_active != nat) cudaMemcpyAsync(n_active, nat, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
   return cudaGetLastError();
 }

@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* x, int T,
                                                           __nv_bfloat16* __restrict__ xl,
                                                           float* __restrict__ inv_rms, uint8_t* __restrict__ x16,
                                                           float* out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
   const int kb0 = blockIdx.z * RT_KBS;
+  griddep_launch_dependents();
   if (warp == 2) tc::tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
     for (int s = 0; s < RT_NS; ++s) {
@@ -141,6 +144,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  griddep_wait();  // x_hi / x_lo come from the prep kernel
   const uint32_t tmem = tmem_base;
   bool ok = true;
   if (tid == 0) {
@@ -231,7 +235,7 @@ cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16
   __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(xbf);
   __nv_bfloat16* xl = xh + (size_t)T * H;
   STRATA_LAUNCH(KID_ROUTER_PREP, s,
-                router_prep_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, xh, xl, inv_rms, x16, out));
+                launch_pdl(router_prep_kernel, (T + 7) / 8, 256, 0, s, x, T, xh, xl, inv_rms, x16, out));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap mh, ml, mw;
@@ -246,7 +250,7 @@ cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16
     if (dev >= 0 && dev < 64) g_rt_attr[dev] = 1;
   }
   dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ROUTER_KSPLIT);
-  STRATA_LAUNCH(KID_ROUTER_TC, s, router_tc_kernel<<<grid, RT_THREADS, smem, s>>>(mh, ml, mw, T, E, parts, status));
+  STRATA_LAUNCH(KID_ROUTER_TC, s, launch_pdl(router_tc_kernel, grid, RT_THREADS, smem, s, mh, ml, mw, T, E, parts, status));
   return cudaGetLastError();
 }
 
