@@ -10,15 +10,16 @@
 // accumulator, so each term carries x to about 16 significant bits (relative error ~2^-17).
 // The x_hi and x_lo tiles of a k-block lie one after the other in shared memory, so together they are
 // one 256-row operand: a single MMA (N = 256) takes both products, x_hi's into accumulator columns
-// [0, 128) and x_lo's into [128, 256).
-// The contraction is split two ways over CTAs (ROUTER_KSPLIT; 1,280 columns each) and, inside a
-// CTA, into four accumulators in TMEM (even / odd k-blocks x the x_hi / x_lo products); a CTA writes
-// the sum of its four to its slice of the partial-logit buffer and the top-k kernel adds the slices in a fixed order (and the
-// bias), so results do not depend on scheduling.  Short accumulation chains keep the tensor core's
-// accumulation error (~1e-5 on a logit) far below the 1e-4 band within which tied logits may order
-// either way.
-// Pipeline: one thread streams the three 128 x 64 operand tiles of each k-block with TMA (tensor
-// maps, 128-byte swizzle) into a 4-stage ring, one thread issues the MMAs, four warps drain TMEM.
+// [0, 128) and x_lo's into [128, 256).  A CTA covers 128 tokens and ET 128-row tiles of router rows
+// against the one token operand, with one accumulator of 256 columns per expert tile: two tiles when
+// that still gives every SM a CTA (each token tile is then read once per 256 experts), else one.
+// The contraction is split two ways over CTAs (ROUTER_KSPLIT; 1,280 columns each); a CTA writes
+// x_hi's + x_lo's product to its slice of the partial-logit buffer and the top-k kernel adds the
+// slices in a fixed order (and the bias), so results do not depend on scheduling.  The tensor core's
+// fp32 accumulation over 80 steps keeps the error on a logit (~1e-5) far below the 1e-4 band within
+// which tied logits may order either way.
+// Pipeline: one thread streams the 2 + ET 128 x 64 operand tiles of each k-block with TMA (tensor
+// maps, 128-byte swizzle) into a ring of stages, one thread issues the MMAs, four warps drain TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -54,9 +55,13 @@ namespace {
 constexpr int RT_T = 128;  // tokens per tile (MMA N)
 constexpr int RT_E = 128;  // experts per tile (MMA M)
 constexpr int RT_THREADS = 128;
-constexpr int RT_NS = 4;   // ring stages
-constexpr uint32_t RT_TILE = 128 * 128;     // 128 rows x 64 bf16
-constexpr uint32_t RT_STAGE = 3 * RT_TILE;  // x_hi, x_lo, router rows
+constexpr uint32_t RT_TILE = 128 * 128;  // 128 rows x 64 bf16
+template <int ET>
+struct RtGeo {  // ET expert tiles per CTA
+  static constexpr uint32_t STAGE = (2 + ET) * RT_TILE;  // x_hi, x_lo, then the router rows of each tile
+  static constexpr int NS = ET == 1 ? 4 : 3;              // ring stages
+  static constexpr size_t SMEM = (size_t)NS * STAGE + 1024;
+};
 constexpr int RT_KBS = KB_GU / ROUTER_KSPLIT;  // k-blocks per CTA
 static_assert(KB_GU % ROUTER_KSPLIT == 0 && RT_KBS % 2 == 0, "even split of the contraction");
 
@@ -120,16 +125,19 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* x, int T,
   }
 }
 
+template <int ET>
 __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_constant__ CUtensorMap map_xh,
                                                                   const __grid_constant__ CUtensorMap map_xl,
                                                                   const __grid_constant__ CUtensorMap map_wr, int T,
                                                                   int E, float* __restrict__ parts, int* status) {
+  constexpr int RT_ET = ET, RT_NS = RtGeo<ET>::NS;
+  constexpr uint32_t RT_STAGE = RtGeo<ET>::STAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[RT_NS], empty[RT_NS], done;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+  const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E * RT_ET;
   const int kb0 = blockIdx.z * RT_KBS;
   griddep_launch_dependents();
   if (warp == 2) tc::tmem_alloc(&tmem_base, 512);
@@ -161,7 +169,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
       mbar_expect_tx(&full[s], RT_STAGE);
       tma_load_2d(st, &map_xh, k, t0, &full[s]);
       tma_load_2d(st + RT_TILE, &map_xl, k, t0, &full[s]);
-      tma_load_2d(st + 2 * RT_TILE, &map_wr, k, e0, &full[s]);
+#pragma unroll
+      for (int j = 0; j < RT_ET; ++j)  // rows past E read as zeros
+        tma_load_2d(st + (2 + j) * RT_TILE, &map_wr, k, e0 + j * RT_E, &full[s]);
     }
     for (int back = 1; back <= RT_NS && back <= kbl; ++back)  // copies still in flight after a failure
       mbar_wait(&full[(kbl - back) % RT_NS], (uint32_t)(((kbl - back) / RT_NS) & 1), status);
@@ -178,11 +188,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
       const uint8_t* st = smem + (size_t)s * RT_STAGE;
       const uint64_t bx = tc::smem_desc_sw128(smem_u32(st));  // x_hi rows, then x_lo rows
       const uint64_t bd = tc::smem_desc_sw128(smem_u32(st + 2 * RT_TILE));
-      // even and odd k-blocks accumulate apart, so consecutive k-blocks' MMAs never wait on each other
-      const uint32_t acc0 = tmem + (uint32_t)((kbl & 1) * 2 * RT_T);
-      const bool first = kbl < 2;
+      // the expert tiles' MMAs alternate, so each accumulator's next MMA never waits on its last
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) tc::mma_f16(acc0, bd + 2 * kk, bx + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int j = 0; j < RT_ET; ++j)
+          tc::mma_f16(tmem + (uint32_t)(j * 2 * RT_T), bd + (uint64_t)((j * RT_TILE) >> 4) + 2 * kk, bx + 2 * kk, idesc,
+                      (kbl > 0 || kk > 0) ? 1u : 0u);
       tc::mma_commit(&empty[s]);
     }
     tc::mma_commit(&done);  // after every MMA this thread issued
@@ -194,18 +206,19 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
   ok = mbar_wait(&done, 0u, status) && ok;
   tc::fence_after_sync();
   const int j4 = lane & 3;
-  const int e4 = e0 + 32 * warp + 4 * (lane >> 2);
 #pragma unroll 1
-  for (int ch = 0; ch < RT_T / 16; ++ch) {
-    float v[4][16];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c * RT_T + 16 * ch, v[c]);
+  for (int c = 0; c < RT_ET * (RT_T / 16); ++c) {
+    const int j = c / (RT_T / 16), ch = c % (RT_T / 16);  // expert tile, 16-token chunk
+    const int e4 = e0 + j * RT_E + 32 * warp + 4 * (lane >> 2);
+    float hi[16], lo[16];
+    const uint32_t acc = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(j * 2 * RT_T + 16 * ch);
+    tc::tmem_ld16(acc, hi);
+    tc::tmem_ld16(acc + RT_T, lo);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       uint32_t a[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        a[i] = __float_as_uint((v[0][4 * m + i] + v[1][4 * m + i]) + (v[2][4 * m + i] + v[3][4 * m + i]));
+      for (int i = 0; i < 4; ++i) a[i] = __float_as_uint(hi[4 * m + i] + lo[4 * m + i]);
       tc::transpose4_lanes(a, j4);
       const int t = t0 + 16 * ch + 4 * m + j4;
       if (ok && e4 < E && t < T)
@@ -226,7 +239,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows) {
   return make_tensor_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, H, rows, (uint64_t)H * 2, 64, 128);
 }
 
-int g_rt_attr[64];
+int g_rt_attr[64];  // per device: dynamic shared memory set; multiprocessor count
+int g_rt_sms[64];
 
 }  // namespace
 
@@ -240,17 +254,32 @@ cudaError_t launch_router_tc(const float* x, float* inv_rms, int T, const uint16
   if (err != cudaSuccess) return err;
   CUtensorMap mh, ml, mw;
   if (!make_map(&mh, xh, T) || !make_map(&ml, xl, T) || !make_map(&mw, w_router, E)) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)RT_NS * RT_STAGE + 1024;
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  int sms = (dev >= 0 && dev < 64) ? g_rt_sms[dev] : 0;
+  if (sms == 0) {
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) g_rt_sms[dev] = sms;
+  }
   if (dev < 0 || dev >= 64 || !g_rt_attr[dev]) {
-    if ((err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
+    if ((err = cudaFuncSetAttribute(router_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)RtGeo<1>::SMEM)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(router_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)RtGeo<2>::SMEM)) != cudaSuccess)
       return err;
     if (dev >= 0 && dev < 64) g_rt_attr[dev] = 1;
   }
-  dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ROUTER_KSPLIT);
-  STRATA_LAUNCH(KID_ROUTER_TC, s, launch_pdl(router_tc_kernel, grid, RT_THREADS, smem, s, mh, ml, mw, T, E, parts, status));
+  const int tt = (T + RT_T - 1) / RT_T;
+  const int et2 = (E + 2 * RT_E - 1) / (2 * RT_E);
+  if (tt * et2 * ROUTER_KSPLIT >= sms) {  // two expert tiles per CTA still give every SM a CTA
+    dim3 grid(tt, et2, ROUTER_KSPLIT);
+    STRATA_LAUNCH(KID_ROUTER_TC, s, launch_pdl(router_tc_kernel<2>, grid, RT_THREADS, RtGeo<2>::SMEM, s, mh, ml, mw, T, E,
+                                               parts, status));
+  } else {
+    dim3 grid(tt, (E + RT_E - 1) / RT_E, ROUTER_KSPLIT);
+    STRATA_LAUNCH(KID_ROUTER_TC, s, launch_pdl(router_tc_kernel<1>, grid, RT_THREADS, RtGeo<1>::SMEM, s, mh, ml, mw, T, E,
+                                               parts, status));
+  }
   return cudaGetLastError();
 }
 
