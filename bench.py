@@ -643,11 +643,11 @@ def measure_gb300(args, rank, world, local_rank):
     W = max(3, args.warmup)
     K = args.steps if args.steps is not None else DEFAULT_STEPS[head]
     rec = measure_workload(qre, arena, head, args, K, W, world, dev, local_rank,
-                           e2e_calls=max(20, min(K, 500)) if gen.CONFIGS[head]["T"] <= 8 else max(3, min(K, 20)))
+                           e2e_calls=max(20, min(K, 500)) if gen.CONFIGS[head]["T"] <= 8 else max(10, min(K, 30)))
     sub = {}
     for c in subs:
         r = measure_workload(qre, arena, c, args, SUB_STEPS[c], W, world, dev, local_rank,
-                             e2e_calls=200 if gen.CONFIGS[c]["T"] <= 8 else 10)
+                             e2e_calls=200 if gen.CONFIGS[c]["T"] <= 8 else 30)
         sub[str(c)] = r
     result = {
         "metric": METRIC,
