@@ -187,14 +187,17 @@ KERNEL_SOURCES = {
 # per-launch figure is one layer's launch, captured on its first layer (--layers 1).
 NCU_TRAFFIC = {
     # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29598208, "82aebf2094784d96"),
-    ("decode_1tok_1layer", "DECODE_LAYER"): (16676864, "82aebf2094784d96"),
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29569792, "49b51a3eebb448c0"),
+    ("decode_1tok_1layer", "DECODE_LAYER"): (16675840, "49b51a3eebb448c0"),
     # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean over the 48 launches of one step
-    ("decode_1tok_48layer_stack", "DECODE_LAYER"): (19522256, "82aebf2094784d96"),
+    ("decode_1tok_48layer_stack", "DECODE_LAYER"): (19528171, "49b51a3eebb448c0"),
+    # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (299592704, "3dc5937e06b40e84"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (132304896, "3dc5937e06b40e84"),
     # profiles/tc_expert_kernel_prefill_8192tok_48layer_stack.md: mean over the 48 launches of each
     # expert kernel in one step (a single-pass capture of the full workload)
-    ("prefill_8192tok_48layer_stack", "TC_GATEUP"): (546866048, "82bc9c2b8c6e2894"),
-    ("prefill_8192tok_48layer_stack", "TC_DOWN"): (259693445, "82bc9c2b8c6e2894"),
+    ("prefill_8192tok_48layer_stack", "TC_GATEUP"): (558071115, "3dc5937e06b40e84"),
+    ("prefill_8192tok_48layer_stack", "TC_DOWN"): (274568283, "3dc5937e06b40e84"),
 }
 
 
