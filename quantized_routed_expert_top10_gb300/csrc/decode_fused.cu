@@ -292,8 +292,7 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, P = T * K;
   int* exit_cnt = p.sync + WS_SYNC_EXIT;
-  // this call's tag: one more than the previous call's (the CTAs advance the epoch as they leave)
-  const uint32_t ep = (uint32_t)ld_relaxed(p.sync + WS_SYNC_EPOCH) + 1u;
+  griddep_launch_dependents();
 
   // up to four tokens: every token's x (fp32) into the ring (idle until the units) with bulk copies,
   // read from there by the staging, the router rows and the lookahead
@@ -310,18 +309,10 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
     mbar_init(&bar_x, 1);
     fence_mbar_init();
     s_ok = 1;
-    if (XS) {
-      mbar_expect_tx(&bar_x, (uint32_t)(sizeof(float) * T * H));
-      for (int t = 0; t < T; ++t)
-        bulk_g2s(ring + 8192 + sizeof(float) * t * XSTR, p.x + (size_t)t * H, (uint32_t)(sizeof(float) * H), &bar_x);
-    }
-    // the router words this CTA will poll into L2 now, so the publishers' stores and the polls meet
-    // in L2 instead of each paying a miss later
-    bulk_prefetch_l2(p.dots + (size_t)(c % WS_NREP) * DECODE_T_MAX * EMAX, (uint32_t)(sizeof(uint64_t) * T * EMAX));
   }
-  // loads for later steps, issued first: the bias (used by the top-k) and this CTA's first router
-  // row (two warps per row, each over one half of the columns), with the x values it multiplies
-  // when there is one token
+  // loads for later steps, issued first (they read only the layer's constant router rows and bias, so
+  // they may run while the previous kernel on the stream finishes): the bias (used by the top-k) and
+  // this CTA's first router row (two warps per row, each over one half of the columns)
   float bias_v[EMAX / DF_THREADS];
 #pragma unroll
   for (int i = 0; i < EMAX / DF_THREADS; ++i) {
@@ -337,6 +328,20 @@ __global__ void __launch_bounds__(DF_THREADS, 2) decode_layer_kernel(const Decod
 #pragma unroll
       for (int i = 0; i < H / 512; ++i) wq[i] = __ldg(wrow + ((half * (H / 2) + 8 * lane + 256 * i) >> 3));
     }
+  }
+  // everything else -- the call epoch, x, the exchange area -- only once the previous kernel is done
+  griddep_wait();
+  // this call's tag: one more than the previous call's (the CTAs advance the epoch as they leave)
+  const uint32_t ep = (uint32_t)ld_relaxed(p.sync + WS_SYNC_EPOCH) + 1u;
+  if (tid == 0) {
+    if (XS) {
+      mbar_expect_tx(&bar_x, (uint32_t)(sizeof(float) * T * H));
+      for (int t = 0; t < T; ++t)
+        bulk_g2s(ring + 8192 + sizeof(float) * t * XSTR, p.x + (size_t)t * H, (uint32_t)(sizeof(float) * H), &bar_x);
+    }
+    // the router words this CTA will poll into L2 now, so the publishers' stores and the polls meet
+    // in L2 instead of each paying a miss later
+    bulk_prefetch_l2(p.dots + (size_t)(c % WS_NREP) * DECODE_T_MAX * EMAX, (uint32_t)(sizeof(uint64_t) * T * EMAX));
   }
   // x of token t at column col: the ring copy (up to four tokens) or global memory
   auto x4 = [&](int t, int col) {
@@ -1130,9 +1135,22 @@ cudaError_t launch_tt(const DecodeParams& prm, cudaStream_t s) {
     if (grid < 32) return cudaErrorInvalidConfiguration;  // router rows per CTA are bounded by 16
     if (dev >= 0 && dev < 64) g_info[dev].grid[vi] = grid;
   }
-  void* args[] = {(void*)&prm};
-  STRATA_LAUNCH(KID_DECODE_LAYER, s,
-                err = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(DF_THREADS), args, smem, s));
+  // cooperative (every CTA resident: the layer's exchanges wait on one another), and with programmatic
+  // stream serialisation: the kernel's constant-weight loads may overlap the previous kernel's tail;
+  // it waits for that kernel (griddepcontrol.wait) before reading anything else
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(DF_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  STRATA_LAUNCH(KID_DECODE_LAYER, s, err = cudaLaunchKernelEx(&cfg, kern, prm));
   return err;
 }
 
