@@ -84,10 +84,6 @@ __device__ __forceinline__ uint32_t mma_kblock_test_next(uint32_t d0, uint64_t a
   return ready;
 }
 
-// fp32 reduction into global memory (no return value) with an L2 eviction-policy hint.
-__device__ __forceinline__ void red_add_f32_hint(float* p, float v, uint64_t policy) {
-  asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
-}
 // Four consecutive fp32 reductions (16-byte aligned address) with an L2 eviction-policy hint.
 __device__ __forceinline__ void red_add_v4_f32_hint(float* p, float a, float b, float c, float d, uint64_t policy) {
   asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
