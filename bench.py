@@ -187,17 +187,17 @@ KERNEL_SOURCES = {
 # per-launch figure is one layer's launch, captured on its first layer (--layers 1).
 NCU_TRAFFIC = {
     # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean of 3 launches
-    ("verify_4tok_1layer", "DECODE_LAYER"): (29569792, "49b51a3eebb448c0"),
-    ("decode_1tok_1layer", "DECODE_LAYER"): (16675840, "49b51a3eebb448c0"),
+    ("verify_4tok_1layer", "DECODE_LAYER"): (29646336, "e149b7c83497eb48"),
+    ("decode_1tok_1layer", "DECODE_LAYER"): (16677120, "e149b7c83497eb48"),
     # profiles/decode_layer_kernel_verify_4tok_1layer.md: mean over the 48 launches of one step
-    ("decode_1tok_48layer_stack", "DECODE_LAYER"): (19528171, "49b51a3eebb448c0"),
+    ("decode_1tok_48layer_stack", "DECODE_LAYER"): (19518325, "e149b7c83497eb48"),
     # profiles/tc_expert_kernel_prefill_2048tok_1layer.md: one launch of each expert kernel
-    ("prefill_2048tok_1layer", "TC_GATEUP"): (299592704, "3dc5937e06b40e84"),
-    ("prefill_2048tok_1layer", "TC_DOWN"): (132304896, "3dc5937e06b40e84"),
+    ("prefill_2048tok_1layer", "TC_GATEUP"): (299194112, "86eb6d87c4faf3a8"),
+    ("prefill_2048tok_1layer", "TC_DOWN"): (132272640, "86eb6d87c4faf3a8"),
     # profiles/tc_expert_kernel_prefill_8192tok_48layer_stack.md: mean over the 48 launches of each
     # expert kernel in one step (a single-pass capture of the full workload)
-    ("prefill_8192tok_48layer_stack", "TC_GATEUP"): (558071115, "3dc5937e06b40e84"),
-    ("prefill_8192tok_48layer_stack", "TC_DOWN"): (274568283, "3dc5937e06b40e84"),
+    ("prefill_8192tok_48layer_stack", "TC_GATEUP"): (554060512, "86eb6d87c4faf3a8"),
+    ("prefill_8192tok_48layer_stack", "TC_DOWN"): (259167040, "86eb6d87c4faf3a8"),
 }
 
 
