@@ -358,6 +358,7 @@ def measure_workload(qre, arena, cfg_id, args, K, W, world, dev, local_rank, e2e
         rec["kernel_ms_per_step"] = step_breakdown(qre, step_args, stream, L)
         rec["step_tc"] = step_tensor_fraction(cfg, total_ms / K)
         rec["expert_load"] = expert_load(ids_layers)
+        rec["expert_roofline"] = expert_roofline(cfg, ids_layers, roof)
     else:
         rec["distinct_experts_per_layer"] = float(np.mean([len(np.unique(l)) for l in ids_layers]))
     rec["e2e"] = measure_e2e(qre, cfg, exs, wr, bias, x_host, ws, flush, dev, e2e_calls, world)
@@ -482,6 +483,29 @@ def step_tensor_fraction(cfg, step_ms):
     achieved = flops / (step_ms / 1e3) / 1e12
     return {"flops_per_step": flops, "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "frac_of": f"{'bf16_tflops' if L == 1 else 'bf16_tflops_sustained'}, {how}"}
+
+
+def expert_roofline(cfg, ids_layers, roof):
+    """The expert kernels against a roofline that takes each touched expert as it is: an expert with
+    n tokens needs n x 9,830,400 flops on the tensor cores but also its 1,382,400-byte blob from HBM, so
+    its ideal time is max(flops / tensor peak, bytes / HBM peak); the layer's ideal is the sum over its
+    touched experts (tiny experts are bound by their weight bytes, big ones by their flops).  Compared
+    with the measured gate/up + down time per layer."""
+    hbm, tc_burst, tc_sust, how = load_peaks()
+    tc = tc_burst if cfg["L"] == 1 else tc_sust
+    per_pair = FLOPS_PER_PAIR["TC_GATEUP"] + FLOPS_PER_PAIR["TC_DOWN"]
+    ideal = []
+    for l in ids_layers:
+        c = np.bincount(l.reshape(-1), minlength=E)
+        c = c[c > 0].astype(np.float64)
+        ideal.append(float(np.sum(np.maximum(c * per_pair / (tc * 1e12), BLOB / (hbm * 1e9)))) * 1e3)
+    other = roof.get("other_expert_kernel", {})
+    measured = roof.get("avg_launch_ms", 0.0) + other.get("avg_launch_ms", 0.0)
+    ideal_ms = float(np.mean(ideal))
+    return {"ideal_ms_per_layer": ideal_ms, "expert_kernels_ms_per_layer": measured,
+            "frac": ideal_ms / measured if measured > 0 else None,
+            "of": f"{'bf16_tflops' if cfg['L'] == 1 else 'bf16_tflops_sustained'} and hbm_gbs, {how}",
+            "formula": "sum over touched experts of max(n_e x 9,830,400 flop / tensor peak, 1,382,400 B / HBM peak)"}
 
 
 def expert_load(ids_layers):

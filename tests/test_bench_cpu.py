@@ -63,3 +63,16 @@ def test_expert_load_record():
 def test_step_tensor_fraction_counts_expert_and_router_flops():
     rec = bench.step_tensor_fraction({"T": 8192, "L": 48}, 100.0)
     assert rec["flops_per_step"] == 48 * 8192 * (10 * 9830400 + 2 * 512 * 2560)
+
+
+def test_expert_roofline_takes_each_expert_by_its_bound():
+    """One expert with 10,000 tokens is bound by its flops, 100 experts with one token each by their
+    blobs' bytes; the ideal time is the sum of the two, and frac is ideal / measured."""
+    hbm, tc, _, _ = bench.load_peaks()
+    ids = np.concatenate([np.zeros(10000, dtype=np.int32), np.arange(1, 101, dtype=np.int32)])[None]
+    roof = {"avg_launch_ms": 1.0, "other_expert_kernel": {"avg_launch_ms": 1.0}}
+    rec = bench.expert_roofline({"T": 10100, "L": 1}, ids, roof)
+    per_pair = bench.FLOPS_PER_PAIR["TC_GATEUP"] + bench.FLOPS_PER_PAIR["TC_DOWN"]
+    want = (10000 * per_pair / (tc * 1e12) + 100 * bench.BLOB / (hbm * 1e9)) * 1e3
+    assert abs(rec["ideal_ms_per_layer"] - want) < 1e-12
+    assert rec["expert_kernels_ms_per_layer"] == 2.0 and abs(rec["frac"] - want / 2.0) < 1e-12

@@ -1,5 +1,5 @@
 """strata_moe_group_noalloc -- grouping for callers that cannot allocate device memory -- against
-strata_moe_group, both through the C ABI.
+strata_moe_group, both through the C ABI, and against the oracle's grouping.
 
 The no-alloc entry point keeps its scratch in a fixed array inside the library (no workspace
 argument), for callers that cannot call cudaMalloc.  Its results must equal the workspace entry
@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import quantized_routed_expert_top10_gb300 as qre
 
 pytestmark = pytest.mark.gpu
@@ -67,3 +68,19 @@ def test_noalloc_grouping_limits():
     _same(_with_workspace(ids_d, T), got)
     with pytest.raises(qre.StrataError):
         qre.strata_moe_group_noalloc(ids_d, T + 1, 512, *got)
+
+
+@pytest.mark.parametrize("T", [1, 37, 2048])
+def test_noalloc_grouping_matches_the_oracle(T):
+    """Bit for bit against oracle.group: expert offsets, the stable pair order within each expert, and
+    the active list in ascending expert order."""
+    ids = _ids(T, 100 + T)
+    got = _outputs(T)
+    qre.strata_moe_group_noalloc(torch.from_numpy(ids).to(DEV), T, 512, *got)
+    torch.cuda.synchronize()
+    off, pair, active, na = (t.cpu().numpy() for t in got)
+    ref_off, ref_pair, ref_active = oracle.group(ids, 512)
+    np.testing.assert_array_equal(off, ref_off)
+    np.testing.assert_array_equal(pair, ref_pair)
+    assert int(na[0]) == len(ref_active)
+    np.testing.assert_array_equal(active[: int(na[0])], ref_active)
