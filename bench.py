@@ -695,7 +695,7 @@ def measure_gb300(args, rank, world, local_rank):
         "e2e": rec["e2e"],
         "gpu_launches": rec["gpu_launches"],
     }
-    for key in ("step_tc", "kernel_ms_per_step", "expert_load", "distinct_experts_per_layer"):
+    for key in ("step_tc", "kernel_ms_per_step", "expert_load", "expert_roofline", "distinct_experts_per_layer"):
         if key in rec:
             result[key] = rec[key]
     if sub:
