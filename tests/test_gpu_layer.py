@@ -150,3 +150,39 @@ def test_epoch_wrap_clears_the_exchange_area(layer0):
     out, ids, _ = run_layer(blobs, wr, None, x, ws=ws)
     np.testing.assert_array_equal(out, ref_out)
     assert int(epoch.cpu().numpy().view(np.uint32)[0]) == 1
+
+
+@pytest.mark.parametrize("T", [4, 300])
+def test_layers_interleaved_with_other_kernels_on_the_stream(layer0, T):
+    """A layer call, a PyTorch kernel that rewrites its output on the same stream, then a second layer
+    call on that: the second call must see the rewritten values (the prefill chain's kernels overlap
+    one another's prologues, never the caller's work).  Each call is checked against the oracle on
+    the input it was given."""
+    blobs, cache = layer0
+    wr = gen.router_weights(0, 0)
+    bias = gen.zipf_bias(0, 0)
+    x = gen.activations_fast(21, T)
+    ws = workspace(T)
+    ex = qre.experts(blobs)
+    wr_d, bias_d = to_dev(wr), to_dev(bias)
+    xd = to_dev(x)
+    out1 = torch.empty(T, qre.H, dtype=torch.float32, device=DEV)
+    out2 = torch.empty_like(out1)
+    ids1 = torch.empty(T, qre.K, dtype=torch.int32, device=DEV)
+    ids2 = torch.empty_like(ids1)
+    w1 = torch.empty(T, qre.K, dtype=torch.float32, device=DEV)
+    w2 = torch.empty_like(w1)
+    qre.strata_moe_layer(ex, wr_d, bias_d, xd, T, 1, out1, ids1, w1, ws)
+    first = out1.clone()  # a kernel reading the first call's output
+    y = out1.mul_(0.5).add_(xd)  # in place on the layer's output, same stream, no synchronisation
+    qre.strata_moe_layer(ex, wr_d, bias_d, y, T, 1, out2, ids2, w2, ws)
+    torch.cuda.synchronize()
+    assert qre.strata_poll_status(ws) == 0
+    y_h = y.cpu().numpy()
+    for inp, ids, w, out, what in ((x, ids1, w1, first, "first"), (y_h, ids2, w2, out2, "second")):
+        ids_h = ids.cpu().numpy()
+        ref_r = oracle.route(inp, wr, bias, residual=True)
+        check_routing(ids_h, ref_r["ids"], ref_r["logits"])
+        ref = oracle.moe_layer(inp, wr, bias, cache.layer_list(0, ids_h), residual=True, ids_in=ids_h)
+        np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=0, atol=W_TOL)
+        check_close(out.cpu().numpy() - inp, ref["out"] - inp.astype(np.float64), f"{what} layer's moe part")
