@@ -91,6 +91,27 @@ MUTATIONS = [
     ("residual_dropped",
      "for (int h = 0; h < H; ++h) acc[h] = xin[h] + acc[h];",
      "for (int h = 0; h < H; ++h) acc[h] = acc[h];"),
+    ("experts_on_raw_input",
+     "      oracle_expert(blob, H, j->FF, j->q2_offset, xn, y);",
+     "      oracle_expert(blob, H, j->FF, j->q2_offset, xin, y);"),
+    ("rmsnorm_epsilon_in_layer",
+     "    oracle_rmsnorm(xin, H, 1e-6, xn);",
+     "    oracle_rmsnorm(xin, H, 1e-5, xn);"),
+    ("rmsnorm_epsilon_in_route",
+     "if (j->residual) oracle_rmsnorm(xn, j->H, 1e-6, xn);",
+     "if (j->residual) oracle_rmsnorm(xn, j->H, 1e-5, xn);"),
+    ("forced_ids_not_renormalised",
+     "  for (int k = 0; k < K; ++k) w[k] = p[ids[k]] / denom;\n  free(p);\n}",
+     "  for (int k = 0; k < K; ++k) w[k] = p[ids[k]];\n  free(p);\n}"),
+    ("forced_ids_all_take_the_first_weight",
+     "  for (int k = 0; k < K; ++k) w[k] = p[ids[k]] / denom;\n  free(p);\n}",
+     "  for (int k = 0; k < K; ++k) w[k] = p[ids[0]] / denom;\n  free(p);\n}"),
+    ("parts_stored_slot_major",
+     "memcpy(j->parts_out + ((int64_t)t * K + k) * H",
+     "memcpy(j->parts_out + ((int64_t)k * j->T + t) * H"),
+    ("active_list_descending",
+     "  for (int e = 0; e < E; ++e)\n    if (count[e]) active[na++] = e;",
+     "  for (int e = E - 1; e >= 0; --e)\n    if (count[e]) active[na++] = e;"),
 ]
 
 # the child process: load the scratch library in place of the oracle's, then run the pins
