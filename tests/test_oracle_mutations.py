@@ -91,6 +91,21 @@ MUTATIONS = [
     ("residual_dropped",
      "for (int h = 0; h < H; ++h) acc[h] = xin[h] + acc[h];",
      "for (int h = 0; h < H; ++h) acc[h] = acc[h];"),
+    ("residual_added_to_the_normalised_input",
+     "for (int h = 0; h < H; ++h) acc[h] = xin[h] + acc[h];",
+     "for (int h = 0; h < H; ++h) acc[h] = xn[h] + acc[h];"),
+    ("router_rows_transposed",
+     "    const uint16_t* row = w_router + (int64_t)e * H;\n    for (int h = 0; h < H; ++h) acc += oracle_bf16_to_double(row[h]) * xn[h];",
+     "    for (int h = 0; h < H; ++h) acc += oracle_bf16_to_double(w_router[(int64_t)h * E + e]) * xn[h];"),
+    ("up_and_down_regions_swapped",
+     "  const uint8_t* up = blob + 18 * nb;\n  const uint8_t* down = blob + 36 * nb;",
+     "  const uint8_t* down = blob + 18 * nb;\n  const uint8_t* up = blob + 36 * nb;"),
+    ("gate_transposed",
+     "      g += q2_weight(gate, H, r, c, q2_offset) * x[c];",
+     "      g += q2_weight(gate, FF, c, r, q2_offset) * x[c];"),
+    ("swiglu_without_up",
+     "hbuf[r] = g / (1.0 + exp(-g)) * u;",
+     "hbuf[r] = g / (1.0 + exp(-g));"),
     ("experts_on_raw_input",
      "      oracle_expert(blob, H, j->FF, j->q2_offset, xn, y);",
      "      oracle_expert(blob, H, j->FF, j->q2_offset, xin, y);"),
